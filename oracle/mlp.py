@@ -1,0 +1,104 @@
+"""The MLP contractions and the SwiGLU requantize, in float64.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+W4A4 GEMM ([P3] "关键源码片段", fp4_gemm with quant_mode "w4a4"):
+    D[m, n] = alpha * sum_k (E2M1(A)*SF_A)[m, k] * (E2M1(B)*SF_B)[n, k]
+in float64, then rounded once to bf16 (RNE).  alpha is the fp32 device scalar
+1/(gs_a*gs_b), widened exactly to double.
+
+W4A16 GEMM ([P3] "关键源码片段", fp4_gemm with quant_mode "w4a16";
+"实现拆解" item 3: alpha holds only the weight dequant factor):
+    D[m, n] = alpha * sum_k x[m, k] * (E2M1(B)*SF_B)[n, k], alpha = 1/gs_b.
+
+SwiGLU ([P2] "实现拆解" item 1: gate_up GEMM -> silu -> FP4 quantize;
+[P2] "关键源码片段": gate_up rows are [gate; up]):
+    g = D[:, :I], u = D[:, I:] taken in float64 *before* bf16 rounding,
+    silu(g) = g / (1 + exp(-g)),  h = fp32(silu(g) * u),
+then h is quantized to NVFP4 with the static down_proj input scale.  Reading:
+the fused path does not round h to bf16 (the pages are silent; their fused
+kernel was checked against the unfused quantize "up to FP4 rounding ties").
+
+silu_mul_nvfp4_quantize ([P1] "关键源码片段", qwen2_moe.py excerpt: one
+kernel replaces act_fn + FP4 quant): the same h from a bf16 gate_up [M, 2I].
+silu_mul_bf16 (the unfused ``act_fn``, used by the W4A16 chain): h rounded
+once to bf16 from float64.
+
+Pins (tests/test_oracle_mlp.py): brute-force triple loops on tiny shapes,
+exact integer results with power-of-two scales, silu closed forms
+(silu(0)=0, silu(x)-silu(-x)=x, limits), the fused == unfused invariant, and
+W4A16 == W4A4 when x is exactly representable.  The whole-MLP numbers have no
+external implementation to compare against: parity unpinned beyond these.
+"""
+import numpy as np
+
+from .formats import bf16_round
+from .quant import dequantize_nvfp4, quantize_nvfp4
+
+
+def gemm_w4a4(a_packed, a_sf, b_packed, b_sf, alpha, round_bf16=True):
+    """A [M, K/2] + linear SF [M, K/16]; B [N, K/2] + linear SF [N, K/16]."""
+    a = dequantize_nvfp4(a_packed, a_sf)
+    b = dequantize_nvfp4(b_packed, b_sf)
+    d = float(np.float32(alpha)) * (a @ b.T)
+    return bf16_round(d) if round_bf16 else d
+
+
+def gemm_w4a16(x, b_packed, b_sf, alpha, round_bf16=True):
+    """x: bf16 values as float32/float64 [M, K]."""
+    b = dequantize_nvfp4(b_packed, b_sf)
+    d = float(np.float32(alpha)) * (np.asarray(x, dtype=np.float64) @ b.T)
+    return bf16_round(d) if round_bf16 else d
+
+
+def silu(g):
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def swiglu_h(gate_up):
+    """float64 [M, 2I] = [gate | up] -> h = fp32(silu(gate) * up)."""
+    gate_up = np.asarray(gate_up, dtype=np.float64)
+    i = gate_up.shape[1] // 2
+    return (silu(gate_up[:, :i]) * gate_up[:, i:]).astype(np.float32)
+
+
+def silu_mul_quant(gate_up_bf16, gs_h, detail=False):
+    """bf16 [M, 2I] (as float) -> NVFP4 (packed [M, I/2], linear SF)."""
+    return quantize_nvfp4(swiglu_h(gate_up_bf16), gs_h, detail=detail)
+
+
+def silu_mul_bf16(gate_up_bf16):
+    gate_up = np.asarray(gate_up_bf16, dtype=np.float64)
+    i = gate_up.shape[1] // 2
+    return bf16_round(silu(gate_up[:, :i]) * gate_up[:, i:])
+
+
+def gemm_swiglu_quant(a_packed, a_sf, w_packed, w_sf, alpha, gs_h, detail=False):
+    """The fused gate_up: plain [gate; up] weight (never the interleaved one)."""
+    d = gemm_w4a4(a_packed, a_sf, w_packed, w_sf, alpha, round_bf16=False)
+    return quantize_nvfp4(swiglu_h(d), gs_h, detail=detail)
+
+
+def mlp_w4a4_fused(x, gs_x, w_gu, alpha_gu, gs_h, w_down, alpha_down):
+    """quantize -> fused gate_up+SwiGLU+requant -> down_proj, bf16 out.
+    w_gu / w_down are (packed, linear SF) tuples."""
+    xq, xs = quantize_nvfp4(x, gs_x)
+    hq, hs = gemm_swiglu_quant(xq, xs, *w_gu, alpha_gu, gs_h)
+    return gemm_w4a4(hq, hs, *w_down, alpha_down)
+
+
+def mlp_w4a4_unfused(x, gs_x, w_gu, alpha_gu, gs_h, w_down, alpha_down):
+    """quantize -> gate_up GEMM (bf16) -> silu_mul_quant -> down_proj."""
+    xq, xs = quantize_nvfp4(x, gs_x)
+    gu = gemm_w4a4(xq, xs, *w_gu, alpha_gu)
+    hq, hs = silu_mul_quant(gu, gs_h)
+    return gemm_w4a4(hq, hs, *w_down, alpha_down)
+
+
+def mlp_w4a16(x, w_gu, alpha_gu, w_down, alpha_down):
+    """bf16 x -> gate_up (bf16) -> silu_mul_bf16 -> down_proj (bf16)."""
+    gu = gemm_w4a16(x, *w_gu, alpha_gu)
+    h = silu_mul_bf16(gu)
+    return gemm_w4a16(h, *w_down, alpha_down)

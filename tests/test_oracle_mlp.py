@@ -1,0 +1,129 @@
+"""Pins of the oracle's contractions, SwiGLU and requantize."""
+import itertools
+import math
+
+import ml_dtypes
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+def _lib_decode(packed, sf):
+    """Independent decode: ml_dtypes for E2M1 codes and E4M3 scales."""
+    codes = np.empty((packed.shape[0], packed.shape[1] * 2), dtype=np.uint8)
+    codes[:, 0::2], codes[:, 1::2] = packed & 0xF, packed >> 4
+    vals = codes.view(ml_dtypes.float4_e2m1fn).astype(np.float64)
+    sc = sf.view(ml_dtypes.float8_e4m3fn).astype(np.float64)
+    return vals * np.repeat(sc, 16, axis=1)
+
+
+def _rand_nvfp4(rows, k, seed):
+    g = np.random.default_rng(seed)
+    packed = g.integers(0, 256, (rows, k // 2), dtype=np.uint8)
+    sf = g.integers(0x20, 0x48, (rows, k // 16), dtype=np.uint8)
+    return packed, sf
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 1, 16), (3, 5, 32), (4, 8, 64), (2, 7, 48)])
+def test_w4a4_gemm_brute_force(m, n, k):
+    a, sa = _rand_nvfp4(m, k, 1)
+    b, sb = _rand_nvfp4(n, k, 2)
+    alpha = np.float32(0.37)
+    d = oracle.gemm_w4a4(a, sa, b, sb, alpha, round_bf16=False)
+    av, bv = _lib_decode(a, sa), _lib_decode(b, sb)
+    for i, j in itertools.product(range(m), range(n)):
+        acc = 0.0
+        for kk in range(k):
+            acc += av[i, kk] * bv[j, kk]
+        assert d[i, j] == pytest.approx(float(alpha) * acc, rel=1e-12, abs=1e-12)
+
+
+def test_w4a4_gemm_exact_integers():
+    # SF = 1.0 (0x38) and codes whose values are integers: the GEMM is an exact integer matmul
+    g = np.random.default_rng(3)
+    m, n, k = 6, 10, 128
+    ia = g.choice([0, 2, 4, 5, 6, 7, 10, 12, 13, 14, 15], (m, k)).astype(np.uint8)  # |v| in {0,1,2,3,4,6}
+    ib = g.choice([0, 2, 4, 5, 6, 7, 10, 12, 13, 14, 15], (n, k)).astype(np.uint8)
+    pk = lambda c: (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    one = np.full((m, k // 16), 0x38, np.uint8), np.full((n, k // 16), 0x38, np.uint8)
+    d = oracle.gemm_w4a4(pk(ia), one[0], pk(ib), one[1], np.float32(1.0), round_bf16=False)
+    lut = np.array([0, 0, 1, 0, 2, 3, 4, 6, 0, 0, -1, 0, -2, -3, -4, -6], dtype=np.int64)
+    exact = lut[ia] @ lut[ib].T
+    assert np.array_equal(d, exact.astype(np.float64))
+
+
+def test_w4a16_gemm_brute_force_and_alpha():
+    g = np.random.default_rng(4)
+    x = synth.to_bf16_bits(g.standard_normal((3, 32)).astype(np.float32))[1]
+    b, sb = _rand_nvfp4(5, 32, 5)
+    d = oracle.gemm_w4a16(x, b, sb, np.float32(0.5), round_bf16=False)
+    bv = _lib_decode(b, sb)
+    for i in range(3):
+        for j in range(5):
+            assert d[i, j] == pytest.approx(0.5 * sum(float(x[i, t]) * bv[j, t] for t in range(32)), rel=1e-12)
+
+
+def test_w4a16_equals_w4a4_on_representable_x():
+    # every block holds a +-6 code and a power-of-two scale, so quantize(x, gs=1) recovers x exactly
+    g = np.random.default_rng(11)
+    m, k = 4, 128
+    codes = g.integers(0, 16, (m, k), dtype=np.uint8)
+    codes[:, ::16] = 7
+    sf = g.choice([0x30, 0x38, 0x40, 0x48], (m, k // 16)).astype(np.uint8)  # 0.5, 1, 2, 4
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    x = oracle.dequantize_nvfp4(packed, sf).astype(np.float32)
+    qp, qs = oracle.quantize_nvfp4(x, np.float32(1.0))
+    assert np.array_equal(qs, sf)
+    assert np.array_equal(oracle.e2m1_decode(oracle.unpack_codes(qp)), oracle.e2m1_decode(codes))
+    b, sb = _rand_nvfp4(9, k, 12)
+    d16 = oracle.gemm_w4a16(x, b, sb, np.float32(0.25), round_bf16=False)
+    d44 = oracle.gemm_w4a4(qp, qs, b, sb, np.float32(0.25), round_bf16=False)
+    assert np.array_equal(d16, d44)
+
+
+def test_silu_closed_forms():
+    x = np.linspace(-30, 30, 1201)
+    s = oracle.silu(x)
+    assert oracle.silu(0.0) == 0.0
+    assert np.allclose(s - oracle.silu(-x), x, rtol=0, atol=1e-12)       # silu(x) - silu(-x) = x
+    sig = s / np.where(x == 0, 1, x)
+    assert np.allclose((sig + oracle.silu(-x) / np.where(x == 0, 1, -x))[x != 0], 1.0, atol=1e-12)
+    assert oracle.silu(-800.0) == 0.0 and oracle.silu(800.0) == 800.0
+    assert oracle.silu(1.0) == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+
+
+def test_swiglu_uses_gate_first_half():
+    gu = np.array([[1.0, -2.0, 3.0, 0.5]])
+    h = oracle.swiglu_h(gu)
+    assert h[0, 0] == np.float32(oracle.silu(1.0) * 3.0)
+    assert h[0, 1] == np.float32(oracle.silu(-2.0) * 0.5)
+
+
+def test_silu_mul_bf16_single_rounding():
+    gu = np.array([[2.0, 1.0 + 2.0 ** -7]])
+    want = oracle.bf16_round(oracle.silu(2.0) * (1.0 + 2.0 ** -7))
+    assert oracle.silu_mul_bf16(gu)[0, 0] == want
+
+
+def test_fused_and_unfused_requant_agree_within_tolerance():
+    """The fused path (h from the unrounded GEMM) and the unfused one (h from
+    the bf16-rounded gate_up) give the same NVFP4 codes except near rounding
+    boundaries -- the agreement the pages report for their fused kernel."""
+    from tolerance import check_requant
+    w = synth.WORKLOADS[0]
+    _, x = synth.activations(0, 4)
+    gs_x = oracle.global_scale(np.abs(x).max())
+    wgu = synth.weight(0, "gate_up")
+    gs_w = oracle.global_scale(np.abs(wgu).max())
+    wq, ws = oracle.quantize_nvfp4(wgu, gs_w)
+    xq, xs = oracle.quantize_nvfp4(x, gs_x)
+    alpha = np.float32(1.0) / (gs_x * gs_w)
+    d = oracle.gemm_w4a4(xq, xs, wq, ws, alpha, round_bf16=False)
+    h = oracle.swiglu_h(d)
+    gs_h = oracle.global_scale(np.abs(h).max())
+    uq, us = oracle.silu_mul_quant(oracle.bf16_round(d), gs_h)
+    # bf16 rounding of gate_up moves h by up to ~2^-8 relative: widen the window accordingly
+    check_requant(uq, us, h, gs_h, max_frac=0.05, what="fused vs unfused", window=2.0 ** -7)
+    assert h.shape == (4, w.inter)
