@@ -1,0 +1,227 @@
+/*
+ * nvfp4mlp.h -- C ABI of the NVFP4-quantized dense MLP library (sm_103a).
+ *
+ * NVFP4: E2M1 4-bit values, two per byte (element 2j in the low nibble,
+ * element 2j+1 in the high nibble), one unsigned E4M3 block scale per 16
+ * consecutive elements along K, and an fp32 per-tensor global scale gs.  A
+ * value dequantizes as E2M1(code) * E4M3(scale); the 1/gs factors of both
+ * operands are folded into one fp32 GEMM alpha.
+ *
+ * Sources, cited by page title and section:
+ *  [P1] sglang PR #34859 digest "Add Qwen3.8-27B": fused SiLU*mul + NVFP4
+ *       quantize of the down_proj input; 6-D -> dense swizzled scale layout
+ *       (section "关键源码片段", qwen2_moe.py excerpt).
+ *  [P2] sglang PR #26626 digest "fused NVFP4 gate_up GEMM + SwiGLU + output
+ *       quantize": fp4_quantize -> nvfp4_gemm_swiglu_nvfp4_quant -> down_proj
+ *       call chain (deepseek_v2.py excerpt), gate/up interleave in groups of 64
+ *       and the block-scale 2-D swizzle (modelopt_quant.py excerpt).
+ *  [P3] sglang PR #35120 report "FlashInfer CuTe DSL NVFP4 W4A16 mode":
+ *       fp4_gemm W4A4 / W4A16 entry (section "关键源码片段", fp4_gemm), linear
+ *       [rows, K/16] scale view (MoE excerpt), W4A16 alpha holds only the weight
+ *       dequant factor (section "实现拆解", item 3).
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument except status_out is a DEVICE pointer to memory
+ *    the caller owns (allocated by the caller, e.g. through PyTorch).  The
+ *    library never allocates, frees or logs, and holds no state between calls
+ *    other than the device status word (nvfp4_get_device_status).
+ *  - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
+ *  - Scalars (global_scale, alpha, out_global_scale) are 1-element fp32
+ *    DEVICE buffers, so a call sequence can be captured in a CUDA graph.
+ *  - Calls are asynchronous and ordered on `stream` (NULL = legacy default
+ *    stream); they do not synchronize, except nvfp4_get_device_status.
+ *  - Pointers must be 16-byte aligned.  Outputs must not alias inputs.
+ *  - Validation happens on the host before any launch; a call that returns
+ *    anything but NVFP4_OK launched nothing and wrote nothing.
+ *  - The device must be compute capability 10.3 (GB300, sm_103a); otherwise
+ *    NVFP4_ERR_ARCH.  A failed launch returns NVFP4_ERR_CUDA.
+ *  - m == 0 (no tokens) is valid and launches nothing.
+ *
+ * Block-scale layouts (nvfp4_sf_layout)
+ *  - NVFP4_SF_LINEAR: uint8 [rows, K/16], row-major ([P3] MoE excerpt).
+ *  - NVFP4_SF_SWIZZLED_128x4: the "dense swizzled layout fp4_gemm expects"
+ *    ([P1] qwen2_moe.py excerpt, the permute of a (32, 4, m_blocks, 4, K/64)
+ *    tensor).  Rows pad to Rp = ceil(rows/128)*128 and scale columns to
+ *    Cp = ceil(K/16 / 4)*4; the scale of (row r, column j) sits at byte
+ *        ((((r/128)*(Cp/4) + j/4)*32 + r%32)*4 + (r%128)/32)*4 + j%4
+ *    i.e. 512-byte tiles of 128 rows x 4 columns, tiles ordered row block
+ *    major.  Padding bytes are written as 0x00 by every producer here.
+ *    Every GEMM operand scale is in this layout.
+ */
+#ifndef NVFP4MLP_H
+#define NVFP4MLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *nvfp4_stream_t;
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, negative size, aliasing   */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* size / alignment outside the supported set */
+  NVFP4_ERR_ARCH = 3,              /* current device is not sm_103           */
+  NVFP4_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed   */
+  NVFP4_ERR_DEVICE_TIMEOUT = 5     /* a kernel gave up a bounded wait        */
+} nvfp4_status;
+
+typedef enum {
+  NVFP4_SF_SWIZZLED_128x4 = 0,
+  NVFP4_SF_LINEAR = 1
+} nvfp4_sf_layout;
+
+/* Kernel family selection for the GEMM entry points' *_ex forms.  AUTO picks
+ * by M: the weight-streaming small-M kernels for decode-sized M, the
+ * tcgen05 tensor-core kernels above that. */
+typedef enum {
+  NVFP4_ALGO_AUTO = 0,
+  NVFP4_ALGO_GEMV = 1,     /* CUDA-core split-row GEMV (any M, meant for M <= 16) */
+  NVFP4_ALGO_TC = 2,       /* tcgen05 block-scaled MMA, accumulators in TMEM      */
+  NVFP4_ALGO_TC_SWAPAB = 3 /* tcgen05 with weights as the MMA M operand (small M) */
+} nvfp4_algo;
+
+/* Human-readable name of a status code (static storage). */
+const char *nvfp4_status_string(nvfp4_status s);
+
+/* Library ABI version: (major << 16) | minor. */
+int nvfp4_version(void);
+
+/* Bytes of a block-scale buffer for `rows` rows of K elements (K % 16 == 0):
+ * SWIZZLED_128x4 -> ceil(rows/128)*128 * ceil(K/64)*4; LINEAR -> rows*K/16.
+ * Returns 0 for invalid arguments. */
+size_t nvfp4_sf_bytes(int64_t rows, int64_t k, nvfp4_sf_layout layout);
+
+/* Scratch bytes the GEMM entry points need for (m, n, k) with `algo`.  All
+ * current kernels return 0 (no scratch); pass workspace = NULL, ws_bytes = 0. */
+size_t nvfp4_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo);
+
+/* NVFP4 quantize of bf16 activations ([P2] deepseek_v2.py excerpt:
+ * fp4_quantize(x, input_scale_inv); [P3] MoE excerpt for the linear layout).
+ *   x            bf16 [m, k] row-major
+ *   global_scale fp32 [1]  gs (e.g. 448*6/amax(x), static per tensor)
+ *   out_fp4      uint8 [m, k/2]
+ *   out_sf       uint8, nvfp4_sf_bytes(m, k, sf_layout) bytes (padding -> 0)
+ * Per 16-block, in fp32 with IEEE round-to-nearest-even at each step:
+ *   s = fp32(amax/6) * gs;  SF = E4M3(s) (RNE, saturating at 448);
+ *   r = SF == 0 ? 0 : gs / SF;  code_i = E2M1(x_i * r) (RNE, saturating at 6,
+ *   sign bit kept, so a negative value that rounds to zero is -0).
+ * Requires k > 0, k % 16 == 0. */
+nvfp4_status nvfp4_quantize(const uint16_t *x, int64_t m, int64_t k, const float *global_scale,
+                            uint8_t *out_fp4, uint8_t *out_sf, nvfp4_sf_layout sf_layout,
+                            nvfp4_stream_t stream);
+
+/* Fused SiLU * mul + NVFP4 quantize of the down_proj input ([P1]
+ * qwen2_moe.py excerpt: one kernel replaces act_fn + FP4 quantize).
+ *   gate_up      bf16 [m, 2*i]: columns [0, i) gate, [i, 2i) up
+ *   global_scale fp32 [1]: the down_proj input global scale
+ *   out_fp4      uint8 [m, i/2];  out_sf: swizzled, nvfp4_sf_bytes(m, i, SWIZZLED)
+ * h = fp32(silu(gate) * up), silu(g) = g / (1 + exp(-g)), h is not rounded
+ * to bf16, then quantized exactly as nvfp4_quantize.  Requires i % 16 == 0. */
+nvfp4_status silu_mul_nvfp4_quantize(const uint16_t *gate_up, int64_t m, int64_t i,
+                                     const float *global_scale, uint8_t *out_fp4, uint8_t *out_sf,
+                                     nvfp4_stream_t stream);
+
+/* Unfused activation of the W4A16 chain: out = bf16(silu(gate) * up).
+ *   gate_up bf16 [m, 2*i] ([gate | up]);  out bf16 [m, i].  Requires i % 8 == 0. */
+nvfp4_status silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
+                           nvfp4_stream_t stream);
+
+/* W4A4 NVFP4 GEMM ([P3] fp4_gemm, quant_mode "w4a4"):
+ *   d[m, n] = bf16( alpha * sum_k (E2M1(a)*SF_a)[m, k] * (E2M1(b)*SF_b)[n, k] )
+ *   a_fp4 uint8 [m, k/2], a_sf swizzled over m rows (e.g. from nvfp4_quantize)
+ *   b_fp4 uint8 [n, k/2], b_sf swizzled over n rows (nvfp4_prepare_weights)
+ *   alpha fp32 [1] = 1 / (gs_a * gs_b);  d bf16 [m, n] row-major.
+ * fp32 accumulation; d is rounded to nearest even.
+ * Requires k % 64 == 0, n % 32 == 0.  workspace may be NULL when
+ * nvfp4_workspace_bytes() is 0. */
+nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, const uint8_t *b_fp4,
+                        const uint8_t *b_sf, const float *alpha, uint16_t *d, int64_t m, int64_t n,
+                        int64_t k, void *workspace, size_t ws_bytes, nvfp4_stream_t stream);
+nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, const uint8_t *b_fp4,
+                           const uint8_t *b_sf, const float *alpha, uint16_t *d, int64_t m,
+                           int64_t n, int64_t k, void *workspace, size_t ws_bytes,
+                           nvfp4_algo algo, nvfp4_stream_t stream);
+
+/* Fused gate_up GEMM + SwiGLU + NVFP4 requantize ([P2] "实现拆解" item 1 and
+ * deepseek_v2.py excerpt: nvfp4_gemm_swiglu_nvfp4_quant).
+ *   a_fp4/a_sf      activation, as nvfp4_gemm
+ *   w_int_fp4/_sf   gate_up weight [n = 2I, k/2] from
+ *                   nvfp4_prepare_gate_up_interleaved (rows interleaved)
+ *   alpha           fp32 [1] = 1/(gs_a * gs_w), one for gate and up
+ *   out_global_scale fp32 [1] = down_proj input global scale
+ *   out_fp4         uint8 [m, n/4]  (I/2 bytes per row)
+ *   out_sf          swizzled over m rows with I/16 columns
+ * g, u = alpha * acc (fp32); h = silu(g) * u in fp32 (no bf16 rounding); h is
+ * quantized as nvfp4_quantize.  W4A4 only ([P3] "实现拆解" item 5: the fused
+ * kernels are guarded to quant_mode "w4a4").  Requires n % 128 == 0,
+ * k % 64 == 0. */
+nvfp4_status nvfp4_gemm_swiglu_quant(const uint8_t *a_fp4, const uint8_t *a_sf,
+                                     const uint8_t *w_int_fp4, const uint8_t *w_int_sf,
+                                     const float *alpha, const float *out_global_scale,
+                                     uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
+                                     int64_t k, void *workspace, size_t ws_bytes,
+                                     nvfp4_stream_t stream);
+nvfp4_status nvfp4_gemm_swiglu_quant_ex(const uint8_t *a_fp4, const uint8_t *a_sf,
+                                        const uint8_t *w_int_fp4, const uint8_t *w_int_sf,
+                                        const float *alpha, const float *out_global_scale,
+                                        uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
+                                        int64_t k, void *workspace, size_t ws_bytes,
+                                        nvfp4_algo algo, nvfp4_stream_t stream);
+
+/* W4A16 GEMM ([P3] fp4_gemm, quant_mode "w4a16" -> mm_bf16_fp4):
+ *   d[m, n] = bf16( alpha * sum_k a[m, k] * (E2M1(b)*SF_b)[n, k] )
+ *   a bf16 [m, k];  b_fp4/b_sf as nvfp4_gemm;  alpha fp32 [1] = 1/gs_b only.
+ * Requires k % 64 == 0, n % 32 == 0. */
+nvfp4_status bf16_fp4_gemm(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
+                           const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
+                           void *workspace, size_t ws_bytes, nvfp4_stream_t stream);
+nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
+                              const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
+                              void *workspace, size_t ws_bytes, nvfp4_algo algo,
+                              nvfp4_stream_t stream);
+
+/* Weight prep, run once at load time ([P2] modelopt_quant.py excerpt:
+ * process_weights_after_loading; [P3] "实现拆解" item 2:
+ * prepare_bf16_fp4_weights).  Takes the LINEAR scales (the pages snapshot the
+ * raw scales before any swizzle) and writes:
+ *   w_out  uint8 [n, k/2]  copy of w_fp4 (w_out == w_fp4 is allowed: no copy)
+ *   sf_out swizzled, nvfp4_sf_bytes(n, k, SWIZZLED) bytes.
+ * The same prepared weight serves nvfp4_gemm and bf16_fp4_gemm.
+ * Requires k % 16 == 0. */
+nvfp4_status nvfp4_prepare_weights(const uint8_t *w_fp4, const uint8_t *sf_linear, int64_t n,
+                                   int64_t k, uint8_t *w_out, uint8_t *sf_out,
+                                   nvfp4_stream_t stream);
+
+/* Gate/up interleave for the fused kernel ([P2] modelopt_quant.py excerpt:
+ * interleave_linear_and_gate(cat(up, gate), group_size=64) on the weight and
+ * on the un-swizzled scales, then swizzle_blockscale_2d on the scales).
+ *   w_fp4     uint8 [n = 2I, k/2] rows [gate; up];  sf_linear uint8 [n, k/16]
+ *   w_out     uint8 [n, k/2]: output row 128b + j is up row 64b + j (j < 64),
+ *             gate row 64b + j - 64 (j >= 64);  must not alias w_fp4
+ *   sf_out    swizzled scales of the interleaved rows.
+ * Requires n % 128 == 0, k % 16 == 0. */
+nvfp4_status nvfp4_prepare_gate_up_interleaved(const uint8_t *w_fp4, const uint8_t *sf_linear,
+                                               int64_t n, int64_t k, uint8_t *w_out,
+                                               uint8_t *sf_out, nvfp4_stream_t stream);
+
+/* Synchronizes `stream`, then returns in *status_out (HOST pointer) the
+ * device status word of the current device -- NVFP4_OK, or
+ * NVFP4_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded pipeline wait since
+ * the last call -- and clears it.  The return value reports the call itself. */
+nvfp4_status nvfp4_get_device_status(int *status_out, nvfp4_stream_t stream);
+
+/* Testing hook for the bounded waits: sets the spin limit the tensor-core
+ * kernels use for every mbarrier wait (0 restores the default, about 2 s at
+ * full clock).  A limit of 1 makes a wait give up at once; the kernel then
+ * records NVFP4_ERR_DEVICE_TIMEOUT and returns without faulting. */
+nvfp4_status nvfp4_set_wait_limit(uint32_t spins);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4MLP_H */

@@ -1,0 +1,255 @@
+// C ABI of the NVFP4 dense-MLP library: host-side validation, the sm_103
+// check, M-based kernel selection and launch.  Nothing here allocates.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace nvfp4;
+
+namespace {
+
+constexpr int kVersion = (1 << 16) | 0;
+std::atomic<uint32_t> g_wait_limit{0};  // 0 = kernel default
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The current device must be a GB300-class part (compute capability 10.3).
+// Cached per device ordinal.
+nvfp4_status check_arch() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return NVFP4_ERR_ARCH;
+  int c = cache[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    c = (major == 10 && minor == 3) ? 1 : 2;
+    cache[dev].store(c, std::memory_order_relaxed);
+  }
+  return c == 1 ? NVFP4_OK : NVFP4_ERR_ARCH;
+}
+
+nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+// Largest M served by the weight-streaming kernels when AUTO is asked.
+constexpr int64_t kSmallM = 16;
+
+nvfp4_status check_gemm_shape(int64_t m, int64_t n, int64_t k) {
+  if (m < 0 || n <= 0 || k <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (k % 64 != 0 || n % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (m > (int64_t(1) << 31) || n > (int64_t(1) << 31) || k > (int64_t(1) << 31))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape or alignment";
+    case NVFP4_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case NVFP4_ERR_CUDA: return "CUDA runtime error";
+    case NVFP4_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+  }
+  return "unknown status";
+}
+
+int nvfp4_version(void) { return kVersion; }
+
+size_t nvfp4_sf_bytes(int64_t rows, int64_t k, nvfp4_sf_layout layout) {
+  if (rows < 0 || k <= 0 || k % 16 != 0) return 0;
+  if (layout == NVFP4_SF_LINEAR) return (size_t)(rows * (k / 16));
+  if (layout != NVFP4_SF_SWIZZLED_128x4) return 0;
+  return (size_t)((rows + 127) / 128 * 128) * (size_t)((k / 16 + 3) / 4 * 4);
+}
+
+size_t nvfp4_workspace_bytes(int64_t, int64_t, int64_t, nvfp4_algo) { return 0; }
+
+nvfp4_status nvfp4_quantize(const uint16_t *x, int64_t m, int64_t k, const float *global_scale,
+                            uint8_t *out_fp4, uint8_t *out_sf, nvfp4_sf_layout sf_layout,
+                            nvfp4_stream_t stream) {
+  if (!x || !global_scale || !out_fp4 || !out_sf || m < 0 || k <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (sf_layout != NVFP4_SF_LINEAR && sf_layout != NVFP4_SF_SWIZZLED_128x4)
+    return NVFP4_ERR_INVALID_ARG;
+  if (k % 16 != 0 || !aligned16(x) || !aligned16(out_fp4)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  return from_cuda(launch_quantize(x, m, k, global_scale, out_fp4, out_sf,
+                                   sf_layout == NVFP4_SF_SWIZZLED_128x4, (cudaStream_t)stream));
+}
+
+nvfp4_status silu_mul_nvfp4_quantize(const uint16_t *gate_up, int64_t m, int64_t i,
+                                     const float *global_scale, uint8_t *out_fp4, uint8_t *out_sf,
+                                     nvfp4_stream_t stream) {
+  if (!gate_up || !global_scale || !out_fp4 || !out_sf || m < 0 || i <= 0)
+    return NVFP4_ERR_INVALID_ARG;
+  if (i % 16 != 0 || !aligned16(gate_up) || !aligned16(out_fp4)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  return from_cuda(launch_silu_mul_quantize(gate_up, m, i, global_scale, out_fp4, out_sf,
+                                            (cudaStream_t)stream));
+}
+
+nvfp4_status silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
+                           nvfp4_stream_t stream) {
+  if (!gate_up || !out || m < 0 || i <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (i % 8 != 0 || !aligned16(gate_up) || !aligned16(out)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  return from_cuda(launch_silu_mul_bf16(gate_up, m, i, out, (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, const uint8_t *b_fp4,
+                           const uint8_t *b_sf, const float *alpha, uint16_t *d, int64_t m,
+                           int64_t n, int64_t k, void *, size_t, nvfp4_algo algo,
+                           nvfp4_stream_t stream) {
+  if (!a_fp4 || !a_sf || !b_fp4 || !b_sf || !alpha || !d) return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
+  if (!aligned16(a_fp4) || !aligned16(a_sf) || !aligned16(b_fp4) || !aligned16(b_sf) || !aligned16(d))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (algo == NVFP4_ALGO_AUTO) {
+    if (m > kSmallM && tc_supported(TC_W4A4, false, m, n, k)) algo = NVFP4_ALGO_TC;
+    else algo = NVFP4_ALGO_GEMV;
+  }
+  if (algo == NVFP4_ALGO_GEMV)
+    return from_cuda(launch_gemv(GEMV_W4A4, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
+                                 nullptr, m, n, k, st));
+  const bool swap = algo == NVFP4_ALGO_TC_SWAPAB;
+  if (!tc_supported(TC_W4A4, swap, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A4, swap, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
+                             nullptr, m, n, k, g_wait_limit.load(), st));
+}
+
+nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, const uint8_t *b_fp4,
+                        const uint8_t *b_sf, const float *alpha, uint16_t *d, int64_t m, int64_t n,
+                        int64_t k, void *workspace, size_t ws_bytes, nvfp4_stream_t stream) {
+  return nvfp4_gemm_ex(a_fp4, a_sf, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes,
+                       NVFP4_ALGO_AUTO, stream);
+}
+
+nvfp4_status nvfp4_gemm_swiglu_quant_ex(const uint8_t *a_fp4, const uint8_t *a_sf,
+                                        const uint8_t *w_int_fp4, const uint8_t *w_int_sf,
+                                        const float *alpha, const float *out_global_scale,
+                                        uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
+                                        int64_t k, void *, size_t, nvfp4_algo algo,
+                                        nvfp4_stream_t stream) {
+  if (!a_fp4 || !a_sf || !w_int_fp4 || !w_int_sf || !alpha || !out_global_scale || !out_fp4 || !out_sf)
+    return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
+  if (n % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a_fp4) || !aligned16(a_sf) || !aligned16(w_int_fp4) || !aligned16(w_int_sf) ||
+      !aligned16(out_fp4) || !aligned16(out_sf))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (algo == NVFP4_ALGO_AUTO) {
+    if (m > kSmallM && tc_supported(TC_W4A4_SWIGLU, false, m, n, k)) algo = NVFP4_ALGO_TC;
+    else algo = NVFP4_ALGO_GEMV;
+  }
+  if (algo == NVFP4_ALGO_GEMV)
+    return from_cuda(launch_gemv(GEMV_W4A4_SWIGLU, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
+                                 out_global_scale, nullptr, out_fp4, out_sf, m, n, k, st));
+  const bool swap = algo == NVFP4_ALGO_TC_SWAPAB;
+  if (!tc_supported(TC_W4A4_SWIGLU, swap, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A4_SWIGLU, swap, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
+                             out_global_scale, nullptr, out_fp4, out_sf, m, n, k,
+                             g_wait_limit.load(), st));
+}
+
+nvfp4_status nvfp4_gemm_swiglu_quant(const uint8_t *a_fp4, const uint8_t *a_sf,
+                                     const uint8_t *w_int_fp4, const uint8_t *w_int_sf,
+                                     const float *alpha, const float *out_global_scale,
+                                     uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
+                                     int64_t k, void *workspace, size_t ws_bytes,
+                                     nvfp4_stream_t stream) {
+  return nvfp4_gemm_swiglu_quant_ex(a_fp4, a_sf, w_int_fp4, w_int_sf, alpha, out_global_scale,
+                                    out_fp4, out_sf, m, n, k, workspace, ws_bytes,
+                                    NVFP4_ALGO_AUTO, stream);
+}
+
+nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
+                              const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
+                              void *, size_t, nvfp4_algo algo, nvfp4_stream_t stream) {
+  if (!a || !b_fp4 || !b_sf || !alpha || !d) return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
+  if (!aligned16(a) || !aligned16(b_fp4) || !aligned16(b_sf) || !aligned16(d))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (algo == NVFP4_ALGO_AUTO) {
+    if (m > kSmallM && tc_supported(TC_W4A16, false, m, n, k)) algo = NVFP4_ALGO_TC;
+    else algo = NVFP4_ALGO_GEMV;
+  }
+  if (algo == NVFP4_ALGO_GEMV)
+    return from_cuda(launch_gemv(GEMV_W4A16, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
+                                 nullptr, m, n, k, st));
+  const bool swap = algo == NVFP4_ALGO_TC_SWAPAB;
+  if (!tc_supported(TC_W4A16, swap, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A16, swap, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
+                             nullptr, m, n, k, g_wait_limit.load(), st));
+}
+
+nvfp4_status bf16_fp4_gemm(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
+                           const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
+                           void *workspace, size_t ws_bytes, nvfp4_stream_t stream) {
+  return bf16_fp4_gemm_ex(a, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes, NVFP4_ALGO_AUTO,
+                          stream);
+}
+
+nvfp4_status nvfp4_prepare_weights(const uint8_t *w_fp4, const uint8_t *sf_linear, int64_t n,
+                                   int64_t k, uint8_t *w_out, uint8_t *sf_out,
+                                   nvfp4_stream_t stream) {
+  if (!w_fp4 || !sf_linear || !w_out || !sf_out || n <= 0 || k <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (k % 16 != 0 || !aligned16(w_fp4) || !aligned16(w_out) || !aligned16(sf_out))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  return from_cuda(launch_prepare(w_fp4, sf_linear, n, k, w_out, sf_out, false,
+                                  (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_prepare_gate_up_interleaved(const uint8_t *w_fp4, const uint8_t *sf_linear,
+                                               int64_t n, int64_t k, uint8_t *w_out,
+                                               uint8_t *sf_out, nvfp4_stream_t stream) {
+  if (!w_fp4 || !sf_linear || !w_out || !sf_out || n <= 0 || k <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (w_out == w_fp4) return NVFP4_ERR_INVALID_ARG;
+  if (n % 128 != 0 || k % 16 != 0 || !aligned16(w_fp4) || !aligned16(w_out) || !aligned16(sf_out))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  return from_cuda(launch_prepare(w_fp4, sf_linear, n, k, w_out, sf_out, true,
+                                  (cudaStream_t)stream));
+}
+
+nvfp4_status nvfp4_get_device_status(int *status_out, nvfp4_stream_t stream) {
+  if (!status_out) return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_arch()) return s;
+  int v = 0;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (read_and_clear_device_status(&v) != cudaSuccess) return NVFP4_ERR_CUDA;
+  *status_out = v;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_set_wait_limit(uint32_t spins) {
+  g_wait_limit.store(spins);
+  return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,40 @@
+// Launchers shared between the C-ABI translation unit and the kernel units.
+// Arguments are validated by the caller (api.cu) before any launcher runs.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nvfp4mlp.h"
+
+namespace nvfp4 {
+
+cudaError_t launch_quantize(const uint16_t *x, int64_t m, int64_t k, const float *gs,
+                            uint8_t *out_fp4, uint8_t *out_sf, bool swizzled, cudaStream_t st);
+cudaError_t launch_silu_mul_quantize(const uint16_t *gate_up, int64_t m, int64_t i, const float *gs,
+                                     uint8_t *out_fp4, uint8_t *out_sf, cudaStream_t st);
+cudaError_t launch_silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
+                                 cudaStream_t st);
+cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf_lin, int64_t n, int64_t k,
+                           uint8_t *w_out, uint8_t *sf_out, bool interleave, cudaStream_t st);
+
+// CUDA-core GEMV family (any M; meant for decode-sized M).
+enum GemvMode { GEMV_W4A4 = 0, GEMV_W4A4_SWIGLU = 1, GEMV_W4A16 = 2 };
+cudaError_t launch_gemv(GemvMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,
+                        const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
+                        uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t st);
+
+// tcgen05 tensor-core family.
+enum TcMode { TC_W4A4 = 0, TC_W4A4_SWIGLU = 1, TC_W4A16 = 2 };
+cudaError_t launch_tc(TcMode mode, bool swap_ab, const void *a, const uint8_t *a_sf,
+                      const uint8_t *b, const uint8_t *b_sf, const float *alpha,
+                      const float *out_gs, uint16_t *d, uint8_t *out_fp4, uint8_t *out_sf,
+                      int64_t m, int64_t n, int64_t k, uint32_t wait_limit, cudaStream_t st);
+bool tc_supported(TcMode mode, bool swap_ab, int64_t m, int64_t n, int64_t k);
+
+// Device status word of the current device (set by kernels that give up a
+// bounded wait); reads it into *out and clears it.  Synchronous.
+cudaError_t read_and_clear_device_status(int *out);
+
+}  // namespace nvfp4

@@ -1,0 +1,197 @@
+// Elementwise kernels of the NVFP4 MLP: activation quantize, fused
+// SiLU*mul + quantize, SiLU*mul to bf16, and the load-time weight prep.
+// All HBM-bound: one pass over the input, vector loads, coalesced stores.
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+
+namespace {
+
+// One CTA covers one 512-byte tile of the swizzled scale layout: 128 rows x
+// 4 scale columns (64 elements of K).  Thread t owns the block (row, column)
+// whose scale byte sits at offset t of that tile, so the scale stores are one
+// contiguous 512-byte write per CTA, and each group of 4 threads reads 128
+// contiguous bytes of one input row.
+constexpr int kTileThreads = 512;
+
+__device__ __forceinline__ void tile_coords(int t, int64_t &row, int64_t &col) {
+  const int c4 = t & 3, r4 = (t >> 2) & 3, r32 = t >> 4;
+  row = (int64_t)blockIdx.y * 128 + r4 * 32 + r32;
+  col = (int64_t)blockIdx.x * 4 + c4;
+}
+
+__device__ __forceinline__ void load16_bf16(const uint16_t *p, float (&x)[16]) {
+  const uint4 *q = reinterpret_cast<const uint4 *>(p);
+  const uint4 v0 = __ldcs(q), v1 = __ldcs(q + 1);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = bf16_lo(w[i]);
+    x[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+// x [m, k] bf16 -> codes [m, k/2] + scales.  Grid (ceil(k/64), ceil(m/128)).
+__global__ void __launch_bounds__(kTileThreads) quantize_kernel(
+    const uint16_t *__restrict__ x, int64_t m, int64_t k, const float *__restrict__ gs_ptr,
+    uint8_t *__restrict__ out_fp4, uint8_t *__restrict__ out_sf, bool swizzled) {
+  int64_t row, col;
+  tile_coords(threadIdx.x, row, col);
+  const int64_t cols = k >> 4;
+  const int64_t cp4 = (cols + 3) >> 2;
+  const bool valid = row < m && col < cols;
+  uint32_t sf = 0;
+  if (valid) {
+    const float gs = __ldg(gs_ptr);
+    float v[16];
+    load16_bf16(x + row * k + col * 16, v);
+    uint32_t lo, hi;
+    sf = quantize_block16(v, gs, lo, hi);
+    *reinterpret_cast<uint2 *>(out_fp4 + row * (k >> 1) + col * 8) = make_uint2(lo, hi);
+  }
+  if (swizzled) {
+    out_sf[(((int64_t)blockIdx.y * cp4 + blockIdx.x) << 9) + threadIdx.x] = (uint8_t)sf;
+  } else if (valid) {
+    out_sf[row * cols + col] = (uint8_t)sf;
+  }
+}
+
+// gate_up [m, 2i] bf16 ([gate | up]) -> h = silu(gate)*up (fp32) -> NVFP4
+// with swizzled scales.  Same tiling as quantize_kernel over h [m, i].
+__global__ void __launch_bounds__(kTileThreads) silu_mul_quantize_kernel(
+    const uint16_t *__restrict__ gate_up, int64_t m, int64_t inter, const float *__restrict__ gs_ptr,
+    uint8_t *__restrict__ out_fp4, uint8_t *__restrict__ out_sf) {
+  int64_t row, col;
+  tile_coords(threadIdx.x, row, col);
+  const int64_t cols = inter >> 4;
+  const int64_t cp4 = (cols + 3) >> 2;
+  uint32_t sf = 0;
+  if (row < m && col < cols) {
+    const float gs = __ldg(gs_ptr);
+    float g[16], u[16], h[16];
+    load16_bf16(gate_up + row * 2 * inter + col * 16, g);
+    load16_bf16(gate_up + row * 2 * inter + inter + col * 16, u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) h[i] = silu_mul(g[i], u[i]);
+    uint32_t lo, hi;
+    sf = quantize_block16(h, gs, lo, hi);
+    *reinterpret_cast<uint2 *>(out_fp4 + row * (inter >> 1) + col * 8) = make_uint2(lo, hi);
+  }
+  out_sf[(((int64_t)blockIdx.y * cp4 + blockIdx.x) << 9) + threadIdx.x] = (uint8_t)sf;
+}
+
+// out [m, i] = bf16(silu(gate) * up); 8 outputs per thread, grid-stride.
+__global__ void __launch_bounds__(256) silu_mul_bf16_kernel(const uint16_t *__restrict__ gate_up,
+                                                            int64_t m, int64_t inter,
+                                                            uint16_t *__restrict__ out) {
+  const int64_t per_row = inter >> 3;
+  const int64_t total = m * per_row;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = idx / per_row, c8 = idx - row * per_row;
+    const uint4 g = __ldcs(reinterpret_cast<const uint4 *>(gate_up + row * 2 * inter + c8 * 8));
+    const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(gate_up + row * 2 * inter + inter + c8 * 8));
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float h0 = silu_mul(bf16_lo(gw[i]), bf16_lo(uw[i]));
+      const float h1 = silu_mul(bf16_hi(gw[i]), bf16_hi(uw[i]));
+      const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);  // .x = h0 -> low half
+      o[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    *reinterpret_cast<uint4 *>(out + row * inter + c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Output row -> source row of the gate/up interleave: blocks of 128 rows are
+// [up 64b..64b+63 ; gate 64b..64b+63], with [gate; up] source rows.
+__device__ __forceinline__ int64_t interleave_src(int64_t o, int64_t n) {
+  const int64_t b = o >> 7, j = o & 127;
+  return j < 64 ? (n >> 1) + 64 * b + j : 64 * b + (j - 64);
+}
+
+// Row copy (8 bytes per thread), with the optional interleave row map.
+__global__ void __launch_bounds__(256) prep_rows_kernel(const uint8_t *__restrict__ w, int64_t n,
+                                                        int64_t row_bytes, uint8_t *__restrict__ w_out,
+                                                        bool interleave) {
+  const int64_t per_row = row_bytes >> 3;
+  const int64_t total = n * per_row;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t o = idx / per_row, c = idx - o * per_row;
+    const int64_t src = interleave ? interleave_src(o, n) : o;
+    reinterpret_cast<uint2 *>(w_out + o * row_bytes)[c] =
+        reinterpret_cast<const uint2 *>(w + src * row_bytes)[c];
+  }
+}
+
+// Linear scales [n, cols] -> swizzled; 4 output bytes (one row, 4 scale
+// columns) per thread; padding rows and columns get 0.
+__global__ void __launch_bounds__(256) prep_sf_kernel(const uint8_t *__restrict__ sf_lin, int64_t n,
+                                                      int64_t cols, uint8_t *__restrict__ sf_out,
+                                                      bool interleave) {
+  const int64_t cp4 = (cols + 3) >> 2;
+  const int64_t rp = (n + 127) & ~(int64_t)127;
+  const int64_t words = rp * cp4;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < words;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = idx >> 7, within = idx & 127;  // 128 words per 512-byte tile
+    const int64_t rb = tile / cp4, kb = tile - rb * cp4;
+    const int64_t r = rb * 128 + ((within & 3) << 5) + (within >> 2);
+    uint32_t word = 0;
+    if (r < n) {
+      const int64_t src = interleave ? interleave_src(r, n) : r;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t j = kb * 4 + c;
+        if (j < cols) word |= (uint32_t)sf_lin[src * cols + j] << (8 * c);
+      }
+    }
+    reinterpret_cast<uint32_t *>(sf_out)[idx] = word;
+  }
+}
+
+inline unsigned grid_for(int64_t work, int threads) {
+  int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = 152 * 16;
+  return (unsigned)(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const uint16_t *x, int64_t m, int64_t k, const float *gs,
+                            uint8_t *out_fp4, uint8_t *out_sf, bool swizzled, cudaStream_t st) {
+  const dim3 grid((unsigned)((k / 16 + 3) / 4), (unsigned)((m + 127) / 128));
+  quantize_kernel<<<grid, kTileThreads, 0, st>>>(x, m, k, gs, out_fp4, out_sf, swizzled);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul_quantize(const uint16_t *gate_up, int64_t m, int64_t i, const float *gs,
+                                     uint8_t *out_fp4, uint8_t *out_sf, cudaStream_t st) {
+  const dim3 grid((unsigned)((i / 16 + 3) / 4), (unsigned)((m + 127) / 128));
+  silu_mul_quantize_kernel<<<grid, kTileThreads, 0, st>>>(gate_up, m, i, gs, out_fp4, out_sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
+                                 cudaStream_t st) {
+  silu_mul_bf16_kernel<<<grid_for(m * (i / 8), 256), 256, 0, st>>>(gate_up, m, i, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf_lin, int64_t n, int64_t k,
+                           uint8_t *w_out, uint8_t *sf_out, bool interleave, cudaStream_t st) {
+  if (w_out != w || interleave) {
+    prep_rows_kernel<<<grid_for(n * (k / 16), 256), 256, 0, st>>>(w, n, k / 2, w_out, interleave);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t cols = k / 16;
+  const int64_t words = ((n + 127) / 128 * 128) * ((cols + 3) / 4);
+  prep_sf_kernel<<<grid_for(words, 256), 256, 0, st>>>(sf_lin, n, cols, sf_out, interleave);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

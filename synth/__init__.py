@@ -45,6 +45,11 @@ WORKLOADS = {
 
 T_X, T_WGU, T_WDOWN, T_OUTLIER = 0, 1, 2, 3
 
+# Workloads with the same MLP shape draw the same weights: the prefill
+# workload reuses the DeepSeek-V3-shaped decode weights and the W4A16 workload
+# the H5120/I17408 ones.
+WEIGHT_SOURCE = {3: 2, 4: 1}
+
 
 def rng(wid, tensor_id, seed=SEED):
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, wid, tensor_id])))
@@ -71,6 +76,7 @@ def activations(wid, m, k=None, outliers=None, seed=SEED):
 
 def weight(wid, which, rows=None, cols=None, seed=SEED):
     """fp32 weights ~ N(0, 0.02): which='gate_up' -> [2I, H], 'down' -> [H, I]."""
+    wid = WEIGHT_SOURCE.get(wid, wid)
     w = WORKLOADS[wid]
     if which == "gate_up":
         shape, tid = (2 * w.inter, w.hidden), T_WGU

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+function declared in include/nvfp4mlp.h; argument validation answers before
+any launch.  No GPU needed (and no compute call is made)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import nvfp4_quantized_dense_gb300 as nv
+import oracle
+from nvfp4_quantized_dense_gb300 import build as nvbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "nvfp4mlp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nvbuild.build()
+    return nv.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z0-9_]+)\s*\(", text)) - {"sizeof"})
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _declared_functions()
+    assert "nvfp4_gemm_swiglu_quant" in names and len(names) >= 17
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in nvfp4mlp.h but not exported"
+    assert sorted(names) == sorted(nv.EXPORTS)
+
+
+def test_version_and_status_strings(lib):
+    assert nv.nvfp4_version() >> 16 == 1
+    for s in range(6):
+        assert nv.nvfp4_status_string(s)
+    assert "sm_103" in nv.nvfp4_status_string(nv.ERR_ARCH)
+
+
+@pytest.mark.parametrize("rows,k", [(1, 16), (4, 256), (130, 320), (8192, 7168), (0, 64)])
+def test_sf_bytes(lib, rows, k):
+    assert nv.nvfp4_sf_bytes(rows, k, nv.SF_SWIZZLED_128x4) == oracle.sf_swizzled_bytes(rows, k // 16)
+    assert nv.nvfp4_sf_bytes(rows, k, nv.SF_LINEAR) == rows * k // 16
+    assert nv.nvfp4_sf_bytes(rows, 24, nv.SF_LINEAR) == 0
+    assert nv.nvfp4_workspace_bytes(rows, 1024, k) == 0
+
+
+FAKE = 1 << 20   # 16-byte aligned address that is never dereferenced
+
+
+def test_null_pointers_rejected(lib):
+    assert lib.nvfp4_quantize(None, 4, 256, FAKE, FAKE, FAKE, 0, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_gemm(FAKE, FAKE, FAKE, None, FAKE, FAKE, 4, 256, 256, None, 0, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_swiglu_quant(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 4, 256, 256,
+                                       None, 0, None) == nv.ERR_INVALID_ARG
+    assert lib.bf16_fp4_gemm(None, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None, 0, None) == nv.ERR_INVALID_ARG
+    assert lib.silu_mul_nvfp4_quantize(FAKE, 4, 256, None, FAKE, FAKE, None) == nv.ERR_INVALID_ARG
+    assert lib.silu_mul_bf16(FAKE, 4, 256, None, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_prepare_weights(FAKE, None, 256, 256, FAKE, FAKE, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_get_device_status(None, None) == nv.ERR_INVALID_ARG
+
+
+def test_bad_sizes_rejected(lib):
+    assert lib.nvfp4_quantize(FAKE, -1, 256, FAKE, FAKE, FAKE, 0, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize(FAKE, 4, 250, FAKE, FAKE, FAKE, 0, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_quantize(FAKE, 4, 256, FAKE, FAKE, FAKE, 7, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize(FAKE + 8, 4, 256, FAKE, FAKE, FAKE, 0, None) == nv.ERR_UNSUPPORTED_SHAPE
+    # GEMMs: K % 64, N % 32, fused N % 128
+    assert lib.nvfp4_gemm(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 96, None, 0, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_gemm(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 256, None, 0, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_gemm(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, 256, None, 0, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_swiglu_quant(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 96, 256,
+                                       None, 0, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_gemm_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None, 0, 9, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_prepare_gate_up_interleaved(FAKE, FAKE, 192, 256, FAKE + 4096, FAKE, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_prepare_gate_up_interleaved(FAKE, FAKE, 256, 256, FAKE, FAKE, None) == nv.ERR_INVALID_ARG
+    assert lib.silu_mul_bf16(FAKE, 4, 12, FAKE, None) == nv.ERR_UNSUPPORTED_SHAPE
+
+
+def test_binding_raises_on_error(lib):
+    with pytest.raises(nv.Nvfp4Error) as e:
+        nv.nvfp4_quantize(FAKE, 4, 250, FAKE, FAKE, FAKE, stream=0)
+    assert e.value.status == nv.ERR_UNSUPPORTED_SHAPE
+
+
+def test_valid_call_without_a_gpu_launches_nothing(lib):
+    """On a machine without a usable GB300 a well-formed call must come back
+    with an error status (ARCH or CUDA), not crash or fall back."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = lib.nvfp4_quantize(FAKE, 4, 256, FAKE, FAKE, FAKE, 0, None)
+    assert st in (nv.ERR_ARCH, nv.ERR_CUDA)
+
+
+def test_missing_library_raises(tmp_path):
+    saved = nv._lib
+    nv._lib = None
+    try:
+        with pytest.raises(ImportError):
+            nv.load(str(tmp_path / "missing.so"))
+    finally:
+        nv._lib = saved

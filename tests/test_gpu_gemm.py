@@ -1,0 +1,210 @@
+"""GPU parity of the GEMM entry points against the CPU oracle.
+
+Each stage runs on oracle-made inputs (activation codes and scales from the
+oracle's quantize, weights quantized by the oracle and prepared by the
+library's prep call), so a GEMM's result is compared with the oracle's result
+for exactly the same operands:
+  * bf16 outputs: relative Frobenius error <= 1e-3 against the float64 result
+    rounded once to bf16;
+  * fused SwiGLU outputs: the requantize tolerance of tests/tolerance.py.
+Full-size workloads compare sampled output columns (whole 16-feature blocks
+for the fused kernel), computed by the oracle one weight row at a time.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import (bf16_dev, bf16_host, dev, host, quantized_activation, sample_rows, scalar,
+                      small_weights, weights)
+from tolerance import assert_gemm_close, check_requant
+
+pytestmark = pytest.mark.gpu
+
+GEMV, TC, TC_SWAPAB = 1, 2, 3
+
+
+def run_w4a4(nv, xq, xs, wdev, alpha, m, n, k, algo):
+    d = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemm_ex(dev(xq), dev(oracle.sf_swizzle_128x4(xs)), wdev[0], wdev[1], scalar(alpha), d,
+                     m, n, k, algo=algo)
+    torch.cuda.synchronize()
+    return bf16_host(d)
+
+
+def run_swiglu(nv, xq, xs, wdev, alpha, gs_h, m, n, k, algo):
+    inter = n // 2
+    q = torch.full((m, inter // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    s = torch.full((nv.nvfp4_sf_bytes(m, inter),), 0xAB, dtype=torch.uint8, device="cuda")
+    nv.nvfp4_gemm_swiglu_quant_ex(dev(xq), dev(oracle.sf_swizzle_128x4(xs)), wdev[0], wdev[1],
+                                  scalar(alpha), scalar(gs_h), q, s, m, n, k, algo=algo)
+    torch.cuda.synchronize()
+    s = host(s)
+    lin = oracle.sf_unswizzle_128x4(s, m, inter // 16)
+    assert np.array_equal(oracle.sf_swizzle_128x4(lin), s), "scale padding not zero"
+    return host(q), lin
+
+
+def run_w4a16(nv, xbits, wdev, alpha, m, n, k, algo):
+    d = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nv.bf16_fp4_gemm_ex(bf16_dev(xbits), wdev[0], wdev[1], scalar(alpha), d, m, n, k, algo=algo)
+    torch.cuda.synchronize()
+    return bf16_host(d)
+
+
+# ---------------------------------------------------------------- W4A4 GEMM
+SMALL_SHAPES = [(4, 1024, 256), (1, 256, 512), (3, 96, 320), (16, 512, 256), (17, 128, 128),
+                (130, 160, 320)]
+
+
+@pytest.mark.parametrize("algo", [GEMV])
+@pytest.mark.parametrize("m,n,k", SMALL_SHAPES)
+def test_w4a4_small_shapes(lib, m, n, k, algo):
+    ws = small_weights(n, k, 3)
+    _, _, gs_x, xq, xs = quantized_activation(0, m, k)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, algo)
+    ref = oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha)
+    err = assert_gemm_close(got, ref)
+    print(f"w4a4 algo={algo} m={m} n={n} k={k}: rel err {err:.2e}")
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 16])
+def test_w4a4_decode_full_size_sampled(lib, m, which):
+    """Decode workload H5120/I17408: gate_up 34816x5120 and down 5120x17408."""
+    ws = weights(1, which)
+    k = ws.k
+    if which == "gate_up":
+        _, _, gs_x, xq, xs = quantized_activation(1, m)
+    else:  # down_proj input: an NVFP4 h drawn by the oracle
+        hf = synth.random_matrix((m, k), (21, m), scale=0.05)
+        gs_x = oracle.global_scale(np.abs(hf).max())
+        xq, xs = oracle.quantize_nvfp4(hf, gs_x)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, ws.n, k, 0)
+    cols = sample_rows(ws.n, 512, seed=m)
+    ref = oracle.gemm_w4a4(xq, xs, ws.packed[cols], ws.sf[cols], alpha)
+    err = assert_gemm_close(got[:, cols], ref)
+    print(f"decode {which} m={m}: rel err {err:.2e}")
+
+
+def test_w4a4_is_deterministic(lib):
+    ws = small_weights(512, 512, 4)
+    _, _, gs_x, xq, xs = quantized_activation(0, 8, 512)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    a = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, 8, 512, 512, 0)
+    b = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, 8, 512, 512, 0)
+    assert np.array_equal(a, b)
+
+
+def test_gemm_m_zero_is_a_noop(lib):
+    ws = small_weights(256, 256, 5)
+    w = ws.device_prepared(lib)
+    d = torch.full((1, 256), 3.0, dtype=torch.bfloat16, device="cuda")
+    a = torch.zeros((1, 128), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((512,), dtype=torch.uint8, device="cuda")
+    lib.nvfp4_gemm(a, s, w[0], w[1], scalar(1.0), d, 0, 256, 256)
+    torch.cuda.synchronize()
+    assert float(d.float().min()) == 3.0
+
+
+# ------------------------------------------------------- fused gate_up SwiGLU
+def _swiglu_case(nv, wid, m, n, k, ws, algo, sampled_blocks=None, xq_xs_gs=None):
+    inter = n // 2
+    if xq_xs_gs is None:
+        _, _, gs_x, xq, xs = quantized_activation(wid, m, k)
+    else:
+        xq, xs, gs_x = xq_xs_gs
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    if sampled_blocks is None:
+        feats = np.arange(inter)
+    else:
+        feats = sample_rows(inter, sampled_blocks, seed=m + 7, block=16)
+    rows = np.concatenate([feats, inter + feats])           # gate rows, then up rows
+    d = oracle.gemm_w4a4(xq, xs, ws.packed[rows], ws.sf[rows], alpha, round_bf16=False)
+    h = oracle.swiglu_h(d)
+    gs_h = oracle.global_scale(np.abs(h).max())
+    q, s = run_swiglu(nv, xq, xs, ws.device_interleaved(nv), alpha, gs_h, m, n, k, algo)
+    codes = oracle.unpack_codes(q)[:, feats]
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    nflip, nsf = check_requant(packed, s[:, feats[::16] // 16], h, gs_h, what=f"swiglu m={m}")
+    print(f"swiglu algo={algo} m={m} n={n} k={k}: {nflip} boundary flips, {nsf} scale diffs")
+
+
+@pytest.mark.parametrize("algo", [GEMV])
+@pytest.mark.parametrize("m,n,k", [(4, 1024, 256), (1, 256, 512), (3, 128, 320), (16, 384, 256),
+                                   (130, 256, 128)])
+def test_swiglu_small_shapes(lib, m, n, k, algo):
+    _swiglu_case(lib, 0, m, n, k, small_weights(n, k, 6), algo)
+
+
+@pytest.mark.parametrize("m", [1, 8, 32, 64])
+def test_swiglu_deepseek_decode_full_size_sampled(lib, m):
+    """DeepSeek-V3-shaped decode, x with 1% outliers x20, interleaved
+    36864x7168 gate_up weight; 128 sampled 16-feature blocks."""
+    ws = weights(2, "gate_up")
+    _swiglu_case(lib, 2, m, ws.n, ws.k, ws, 0, sampled_blocks=128)
+
+
+# ------------------------------------------------------------------- W4A16
+@pytest.mark.parametrize("algo", [GEMV])
+@pytest.mark.parametrize("m,n,k", [(1, 256, 512), (16, 1024, 256), (5, 96, 320), (33, 128, 128)])
+def test_w4a16_small_shapes(lib, m, n, k, algo):
+    ws = small_weights(n, k, 8)
+    xbits, x = synth.activations(4, m, k)
+    alpha = np.float32(1.0) / ws.gs
+    got = run_w4a16(lib, xbits, ws.device_prepared(lib), alpha, m, n, k, algo)
+    ref = oracle.gemm_w4a16(x, ws.packed, ws.sf, alpha)
+    err = assert_gemm_close(got, ref)
+    print(f"w4a16 algo={algo} m={m} n={n} k={k}: rel err {err:.2e}")
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+@pytest.mark.parametrize("m", [1, 16])
+def test_w4a16_full_size_sampled(lib, m, which):
+    ws = weights(4, which)
+    if which == "gate_up":
+        xbits, x = synth.activations(4, m)
+    else:
+        xbits, x = synth.to_bf16_bits(synth.random_matrix((m, ws.k), (23, m), scale=0.1))
+    alpha = np.float32(1.0) / ws.gs
+    got = run_w4a16(lib, xbits, ws.device_prepared(lib), alpha, m, ws.n, ws.k, 0)
+    cols = sample_rows(ws.n, 512, seed=m + 3)
+    ref = oracle.gemm_w4a16(x, ws.packed[cols], ws.sf[cols], alpha)
+    err = assert_gemm_close(got[:, cols], ref)
+    print(f"w4a16 {which} m={m}: rel err {err:.2e}")
+
+
+# ------------------------------------------------------------- whole chains
+def test_tiny_mlp_chain_end_to_end(lib):
+    """H256/I512, M=4: quantize -> fused gate_up -> down, all on the GPU,
+    against the oracle's own chain (one tolerance for the end-to-end error,
+    since requant boundary flips may propagate)."""
+    m = 4
+    xbits, x = synth.activations(0, m)
+    wgu, wdn = weights(0, "gate_up"), weights(0, "down")
+    gs_x = oracle.global_scale(np.abs(x).max())
+    a_gu = np.float32(1.0) / (gs_x * wgu.gs)
+    xq, xs = oracle.quantize_nvfp4(x, gs_x)
+    h = oracle.swiglu_h(oracle.gemm_w4a4(xq, xs, wgu.packed, wgu.sf, a_gu, round_bf16=False))
+    gs_h = oracle.global_scale(np.abs(h).max())
+    a_dn = np.float32(1.0) / (gs_h * wdn.gs)
+    ref = oracle.mlp_w4a4_fused(x, gs_x, (wgu.packed, wgu.sf), a_gu, gs_h, (wdn.packed, wdn.sf), a_dn)
+
+    h_, i_ = 256, 512
+    xq_d = torch.empty((m, h_ // 2), dtype=torch.uint8, device="cuda")
+    xs_d = torch.empty((lib.nvfp4_sf_bytes(m, h_),), dtype=torch.uint8, device="cuda")
+    lib.nvfp4_quantize(bf16_dev(xbits), m, h_, scalar(gs_x), xq_d, xs_d)
+    hq_d = torch.empty((m, i_ // 2), dtype=torch.uint8, device="cuda")
+    hs_d = torch.empty((lib.nvfp4_sf_bytes(m, i_),), dtype=torch.uint8, device="cuda")
+    wi = wgu.device_interleaved(lib)
+    lib.nvfp4_gemm_swiglu_quant(xq_d, xs_d, wi[0], wi[1], scalar(a_gu), scalar(gs_h), hq_d, hs_d,
+                                m, 2 * i_, h_)
+    out = torch.empty((m, h_), dtype=torch.bfloat16, device="cuda")
+    wd = wdn.device_prepared(lib)
+    lib.nvfp4_gemm(hq_d, hs_d, wd[0], wd[1], scalar(a_dn), out, m, h_, i_)
+    torch.cuda.synchronize()
+    err = assert_gemm_close(bf16_host(out), ref, tol=5e-3, what="tiny MLP end to end")
+    print(f"tiny MLP end-to-end rel err {err:.2e}")
