@@ -1,6 +1,27 @@
-// tcgen05 tensor-core GEMMs (block-scaled NVFP4 MMA, accumulators in TMEM).
+// tcgen05 tensor-core GEMMs: NVFP4 block-scaled MMA (E2M1 x E2M1, UE4M3 per
+// 16 elements), accumulators in TMEM.
+//
+// Kernel shape (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A/B code tiles (2-D tensor maps, 128-byte
+//               swizzle) and the matching 512-byte tiles of the swizzled
+//               block scales (1-D bulk copies), one mbarrier per stage;
+//   warp 1      allocates TMEM; one elected thread copies each stage's
+//               scales into TMEM (tcgen05.cp) and issues the MMAs, then
+//               commits the stage back to the producer;
+//   warps 2..5  epilogue: TMEM -> registers (tcgen05.ld) -> bf16 output, or
+//               the fused SwiGLU + NVFP4 requantize of the gate_up GEMM.
+// Tile 128 (M) x 256 (N) x 256 (K); one MMA instruction covers K = 64, so a
+// stage holds four.  Every mbarrier wait is bounded: a wait that gives up
+// records NVFP4_ERR_DEVICE_TIMEOUT, every role leaves its loop, outstanding
+// copies and MMAs are drained with a second bounded wait, TMEM is freed and
+// the kernel returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace nvfp4 {
 
@@ -15,12 +36,364 @@ cudaError_t read_and_clear_device_status(int *out) {
   return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
 }
 
-bool tc_supported(TcMode, bool, int64_t, int64_t, int64_t) { return false; }
+namespace {
 
-cudaError_t launch_tc(TcMode, bool, const void *, const uint8_t *, const uint8_t *, const uint8_t *,
-                      const float *, const float *, uint16_t *, uint8_t *, uint8_t *, int64_t,
-                      int64_t, int64_t, uint32_t, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int BM = 128, BN = 256, BK = 256;
+constexpr int KSTEPS = BK / 64;                 // MMAs per stage
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK / 2;       // 16 KB
+constexpr uint32_t B_BYTES = BN * BK / 2;       // 32 KB
+constexpr uint32_t SFA_BYTES = (BM / 128) * KSTEPS * 512;
+constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kThreads = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COL = 0, SFA_COL = 256, SFB_COL = 256 + 4 * KSTEPS;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
+constexpr uint32_t kDrainPolls = 1u << 22;
+
+// Instruction descriptor, kind::mxf4nvf4: A/B format E2M1 (1) in bits 7-9 and
+// 10-12, K-major both, N >> 3 in bits 17-22, scale type UE4M3 (0) in bit 23,
+// M >> 4 in bits 24-28, scale-factor ids 0, dense K = 64.
+constexpr uint32_t idesc_nvfp4(int m, int n) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+struct TcArgs {
+  const uint8_t *sfa;     // swizzled scales of A (M rows)
+  const uint8_t *sfb;     // swizzled scales of B (N rows)
+  const float *alpha;
+  const float *out_gs;
+  uint16_t *d;            // bf16 [M, N]
+  uint8_t *out_fp4;       // fused: [M, N/4]
+  uint8_t *out_sf;        // fused: swizzled over M rows, N/32 columns
+  int32_t m, n, k;
+  int32_t num_m, num_n;
+  uint32_t wait_limit;
+};
+
+struct Smem {
+  uint8_t *base;
+  __device__ uint8_t *a(int s) const { return base + s * STAGE_BYTES; }
+  __device__ uint8_t *b(int s) const { return a(s) + A_BYTES; }
+  __device__ uint8_t *sfa(int s) const { return b(s) + B_BYTES; }
+  __device__ uint8_t *sfb(int s) const { return sfa(s) + SFA_BYTES; }
+  __device__ uint64_t *full() const { return reinterpret_cast<uint64_t *>(base + STAGES * STAGE_BYTES); }
+  __device__ uint64_t *empty() const { return full() + STAGES; }
+  __device__ uint64_t *tfull() const { return empty() + STAGES; }
+  __device__ uint64_t *tempty() const { return tfull() + 1; }
+  __device__ uint64_t *drain() const { return tempty() + 1; }
+  __device__ uint32_t *tslot() const { return reinterpret_cast<uint32_t *>(drain() + 1); }
+  __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(tslot() + 1); }
+};
+
+__device__ __forceinline__ void give_up(volatile int *abort_flag) {
+  *abort_flag = 1;
+  atomicCAS(&g_device_status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+template <int MODE>  // TC_W4A4: bf16 out; TC_W4A4_SWIGLU: fused SwiGLU + NVFP4 requant
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const TcArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem sm{reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int *abort_flag = sm.abort_flag();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&sm.full()[s], 1);
+      ptx::mbar_init(&sm.empty()[s], 1);
+    }
+    ptx::mbar_init(sm.tfull(), 1);
+    ptx::mbar_init(sm.tempty(), 128);
+    ptx::mbar_init(sm.drain(), 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tm_a);
+    ptx::prefetch_tensormap(&tm_b);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sm.tslot(), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *sm.tslot();
+
+  const int num_tiles = p.num_m * p.num_n;
+  const int ksteps_total = p.k >> 6;              // K / 64
+  const int num_kb = (ksteps_total + KSTEPS - 1) / KSTEPS;
+  const int cp4a = ksteps_total, cp4b = ksteps_total;   // 512-byte scale tiles per row block
+  const int nrb_b = (p.n + 127) >> 7;             // 128-row blocks of B
+  const uint32_t limit = p.wait_limit;
+
+  // producer bookkeeping for the drain: last issued phase parity per stage
+  uint32_t issued_mask = 0, issued_parity = 0;
+  bool mma_issued = false;
+
+  if (warp == 0) {
+    if (ptx::elect_one()) {
+      const uint64_t pol_a = ptx::l2_policy_evict_last();
+      const uint64_t pol_b = ptx::l2_policy_evict_first();
+      int s = 0;
+      uint32_t ph = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+        const int mt = tile % p.num_m, nt = tile / p.num_m;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait_bounded(&sm.empty()[s], ph ^ 1u, limit, kDefaultTimeoutNs, abort_flag)) {
+            give_up(abort_flag);
+            break;
+          }
+          const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
+          const int nbv = min(2, nrb_b - nt * 2);
+          const uint32_t bytes = A_BYTES + B_BYTES + (uint32_t)nk * 512u * (1u + (uint32_t)nbv);
+          ptx::mbar_arrive_expect_tx(&sm.full()[s], bytes);
+          ptx::tma_load_2d(sm.a(s), &tm_a, &sm.full()[s], kb * (BK / 2), mt * BM, pol_a);
+          ptx::tma_load_2d(sm.b(s), &tm_b, &sm.full()[s], kb * (BK / 2), nt * BN, pol_b);
+          ptx::bulk_load(sm.sfa(s), p.sfa + ((size_t)mt * cp4a + kb * KSTEPS) * 512, nk * 512u,
+                         &sm.full()[s], pol_a);
+          for (int rb = 0; rb < nbv; ++rb)
+            ptx::bulk_load(sm.sfb(s) + rb * (KSTEPS * 512),
+                           p.sfb + ((size_t)(nt * 2 + rb) * cp4b + kb * KSTEPS) * 512, nk * 512u,
+                           &sm.full()[s], pol_b);
+          issued_mask |= 1u << s;
+          issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (ptx::elect_one()) {
+      constexpr uint32_t idesc = idesc_nvfp4(BM, BN);
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+        if (!ptx::mbar_wait_bounded(sm.tempty(), (uint32_t)(it & 1) ^ 1u, limit, kDefaultTimeoutNs,
+                                    abort_flag)) {
+          give_up(abort_flag);
+          break;
+        }
+        ptx::tc_fence_after();
+        const int nt = tile / p.num_m;
+        const int nbv = min(2, nrb_b - nt * 2);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
+            give_up(abort_flag);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
+          const uint32_t sfa_s = ptx::smem_u32(sm.sfa(s)), sfb_s = ptx::smem_u32(sm.sfb(s));
+          for (int j = 0; j < nk; ++j) {
+            ptx::tmem_cp_32x128b_x4(tmem + SFA_COL + 4 * j, ptx::smem_desc(sfa_s + 512 * j, 0, 128, 0));
+            for (int rb = 0; rb < nbv; ++rb)
+              ptx::tmem_cp_32x128b_x4(tmem + SFB_COL + 8 * j + 4 * rb,
+                                      ptx::smem_desc(sfb_s + rb * (KSTEPS * 512) + 512 * j, 0, 128, 0));
+          }
+          const uint32_t a_s = ptx::smem_u32(sm.a(s)), b_s = ptx::smem_u32(sm.b(s));
+          for (int j = 0; j < nk; ++j) {
+            ptx::mma_nvfp4(tmem + ACC_COL, ptx::smem_desc(a_s + 32 * j, 16, 1024, 2),
+                           ptx::smem_desc(b_s + 32 * j, 16, 1024, 2), idesc, tmem + SFA_COL + 4 * j,
+                           tmem + SFB_COL + 8 * j, (kb | j) != 0);
+          }
+          mma_issued = true;
+          ptx::tc_commit(&sm.empty()[s]);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::tc_commit(sm.tfull());
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int row = q * 32 + lane;
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    const float alpha = __ldg(p.alpha);
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      if (!ptx::mbar_wait_bounded(sm.tfull(), (uint32_t)(it & 1), limit, kDefaultTimeoutNs, abort_flag)) {
+        give_up(abort_flag);
+        break;
+      }
+      ptx::tc_fence_after();
+      const int mt = tile % p.num_m, nt = tile / p.num_m;
+      const int m = mt * BM + row;
+      if constexpr (MODE == TC_W4A4) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          uint32_t r[16];
+          ptx::tmem_ld16(t_row + ACC_COL + c * 16, r);
+          ptx::tmem_wait_ld();
+          const int n = nt * BN + c * 16;
+          if (m < p.m && n < p.n) {
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[i] = pack_bf16x2(alpha * __uint_as_float(r[2 * i]), alpha * __uint_as_float(r[2 * i + 1]));
+            uint4 *dst = reinterpret_cast<uint4 *>(p.d + (size_t)m * p.n + n);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+      } else {
+        // accumulator columns: [up 64 | gate 64] for features nt*128 + 64g + (0..63), g = 0, 1
+        const float gs = __ldg(p.out_gs);
+        const int inter = p.n >> 1;
+        const int ocp4 = ((inter >> 4) + 3) >> 2;
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          const int f0 = nt * 128 + 64 * g;
+          if (f0 >= inter) break;
+          uint32_t sfw = 0;
+#pragma unroll 1
+          for (int qb = 0; qb < 4; ++qb) {
+            uint32_t up[16], gt[16];
+            ptx::tmem_ld16(t_row + ACC_COL + 128 * g + 16 * qb, up);
+            ptx::tmem_ld16(t_row + ACC_COL + 128 * g + 64 + 16 * qb, gt);
+            ptx::tmem_wait_ld();
+            if (m < p.m) {
+              float h[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                h[i] = silu_mul(alpha * __uint_as_float(gt[i]), alpha * __uint_as_float(up[i]));
+              uint32_t lo, hi;
+              const uint32_t sf = quantize_block16(h, gs, lo, hi);
+              *reinterpret_cast<uint2 *>(p.out_fp4 + (size_t)m * (inter >> 1) + (f0 + 16 * qb) / 2) =
+                  make_uint2(lo, hi);
+              sfw |= sf << (8 * qb);
+            }
+          }
+          // 4 consecutive scale columns (f0/16 .. +3) of this row in one word; rows
+          // past M (the 128-row padding) get zeros
+          *reinterpret_cast<uint32_t *>(p.out_sf + sf_swizzled_offset(m, f0 >> 4, ocp4)) = sfw;
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sm.tempty());
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // Drain: wait (bounded) for this CTA's copies still in flight and for
+    // every MMA it issued, so nothing lands in shared memory or TMEM after
+    // the CTA is gone.
+    if (warp == 0 && issued_mask) {
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_mask & (1u << s)) {
+          volatile int no_abort = 0;
+          ptx::mbar_wait_bounded(&sm.full()[s], (issued_parity >> s) & 1u, kDrainPolls, 0, &no_abort);
+        }
+    }
+    if (warp == 1 && mma_issued) {
+      volatile int no_abort = 0;
+      ptx::tc_commit(sm.drain());
+      ptx::mbar_wait_bounded(sm.drain(), 0, kDrainPolls, 0, &no_abort);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D map over packed NVFP4 codes [rows, k/2] bytes; box 128 bytes x box_rows,
+// 128-byte swizzle; out-of-range rows and columns read as zero.
+bool make_code_map(CUtensorMap *tm, const uint8_t *ptr, int64_t rows, int64_t k, uint32_t box_rows) {
+  auto encode = get_encode();
+  if (!encode) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(ptr), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = v > 0 ? v : 148;
+  }
+  return cache[dev];
+}
+
+template <int MODE>
+cudaError_t launch_mode(const uint8_t *a, const uint8_t *a_sf, const uint8_t *b, const uint8_t *b_sf,
+                        const float *alpha, const float *out_gs, uint16_t *d, uint8_t *out_fp4,
+                        uint8_t *out_sf, int64_t m, int64_t n, int64_t k, uint32_t wait_limit,
+                        cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap tm_a, tm_b;
+  if (!make_code_map(&tm_a, a, m, k, BM) || !make_code_map(&tm_b, b, n, k, BN)) return cudaErrorInvalidValue;
+  TcArgs args{a_sf, b_sf, alpha, out_gs, d, out_fp4, out_sf, (int32_t)m, (int32_t)n, (int32_t)k,
+              (int32_t)((m + BM - 1) / BM), (int32_t)((n + BN - 1) / BN), wait_limit};
+  const int tiles = args.num_m * args.num_n;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  tc_gemm_kernel<MODE><<<grid, kThreads, SMEM_BYTES, st>>>(tm_a, tm_b, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(TcMode mode, bool swap_ab, int64_t m, int64_t n, int64_t k) {
+  if (swap_ab || mode == TC_W4A16) return false;
+  if (k % 64 != 0 || n % 32 != 0 || m <= 0) return false;
+  if (mode == TC_W4A4_SWIGLU && n % 128 != 0) return false;
+  if (m > (1 << 30) || n > (1 << 30) || k > (1 << 30)) return false;
+  return get_encode() != nullptr;
+}
+
+cudaError_t launch_tc(TcMode mode, bool swap_ab, const void *a, const uint8_t *a_sf, const uint8_t *b,
+                      const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
+                      uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
+                      uint32_t wait_limit, cudaStream_t st) {
+  if (!tc_supported(mode, swap_ab, m, n, k)) return cudaErrorNotSupported;
+  const uint8_t *a8 = static_cast<const uint8_t *>(a);
+  if (mode == TC_W4A4)
+    return launch_mode<TC_W4A4>(a8, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, wait_limit, st);
+  return launch_mode<TC_W4A4_SWIGLU>(a8, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k,
+                                     wait_limit, st);
 }
 
 }  // namespace nvfp4

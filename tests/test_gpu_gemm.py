@@ -56,10 +56,14 @@ def run_w4a16(nv, xbits, wdev, alpha, m, n, k, algo):
 # ---------------------------------------------------------------- W4A4 GEMM
 SMALL_SHAPES = [(4, 1024, 256), (1, 256, 512), (3, 96, 320), (16, 512, 256), (17, 128, 128),
                 (130, 160, 320)]
+# tensor-core tiles are 128 x 256 x 256: cover exact tiles, ragged M / N / K
+# tails, several k-blocks and more tiles than SMs (persistent loop)
+TC_SHAPES = [(128, 256, 256), (1, 256, 256), (130, 160, 320), (256, 512, 1024), (200, 96, 576),
+             (384, 1024, 2048), (1000, 2304, 512), (4096, 4096, 256)]
 
 
-@pytest.mark.parametrize("algo", [GEMV])
-@pytest.mark.parametrize("m,n,k", SMALL_SHAPES)
+@pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SMALL_SHAPES] +
+                         [(m, n, k, TC) for m, n, k in TC_SHAPES])
 def test_w4a4_small_shapes(lib, m, n, k, algo):
     ws = small_weights(n, k, 3)
     _, _, gs_x, xq, xs = quantized_activation(0, m, k)
@@ -111,31 +115,30 @@ def test_gemm_m_zero_is_a_noop(lib):
 
 
 # ------------------------------------------------------- fused gate_up SwiGLU
-def _swiglu_case(nv, wid, m, n, k, ws, algo, sampled_blocks=None, xq_xs_gs=None):
+def _swiglu_case(nv, wid, m, n, k, ws, algo, sampled_blocks=None, sampled_tokens=None):
     inter = n // 2
-    if xq_xs_gs is None:
-        _, _, gs_x, xq, xs = quantized_activation(wid, m, k)
-    else:
-        xq, xs, gs_x = xq_xs_gs
+    _, _, gs_x, xq, xs = quantized_activation(wid, m, k)
     alpha = np.float32(1.0) / (gs_x * ws.gs)
-    if sampled_blocks is None:
-        feats = np.arange(inter)
-    else:
-        feats = sample_rows(inter, sampled_blocks, seed=m + 7, block=16)
+    feats = np.arange(inter) if sampled_blocks is None else \
+        sample_rows(inter, sampled_blocks, seed=m + 7, block=16)
+    toks = np.arange(m) if sampled_tokens is None else sample_rows(m, sampled_tokens, seed=m + 9)
     rows = np.concatenate([feats, inter + feats])           # gate rows, then up rows
-    d = oracle.gemm_w4a4(xq, xs, ws.packed[rows], ws.sf[rows], alpha, round_bf16=False)
+    d = oracle.gemm_w4a4(xq[toks], xs[toks], ws.packed[rows], ws.sf[rows], alpha, round_bf16=False)
     h = oracle.swiglu_h(d)
     gs_h = oracle.global_scale(np.abs(h).max())
     q, s = run_swiglu(nv, xq, xs, ws.device_interleaved(nv), alpha, gs_h, m, n, k, algo)
-    codes = oracle.unpack_codes(q)[:, feats]
+    codes = oracle.unpack_codes(q[toks])[:, feats]
     packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
-    nflip, nsf = check_requant(packed, s[:, feats[::16] // 16], h, gs_h, what=f"swiglu m={m}")
+    nflip, nsf = check_requant(packed, s[toks][:, feats[::16] // 16], h, gs_h, what=f"swiglu m={m}")
     print(f"swiglu algo={algo} m={m} n={n} k={k}: {nflip} boundary flips, {nsf} scale diffs")
 
 
-@pytest.mark.parametrize("algo", [GEMV])
-@pytest.mark.parametrize("m,n,k", [(4, 1024, 256), (1, 256, 512), (3, 128, 320), (16, 384, 256),
-                                   (130, 256, 128)])
+SWIGLU_GEMV = [(4, 1024, 256), (1, 256, 512), (3, 128, 320), (16, 384, 256), (130, 256, 128)]
+SWIGLU_TC = [(128, 256, 256), (4, 1024, 256), (130, 384, 320), (256, 1024, 1024), (700, 2304, 512)]
+
+
+@pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SWIGLU_GEMV] +
+                         [(m, n, k, TC) for m, n, k in SWIGLU_TC])
 def test_swiglu_small_shapes(lib, m, n, k, algo):
     _swiglu_case(lib, 0, m, n, k, small_weights(n, k, 6), algo)
 
@@ -146,6 +149,68 @@ def test_swiglu_deepseek_decode_full_size_sampled(lib, m):
     36864x7168 gate_up weight; 128 sampled 16-feature blocks."""
     ws = weights(2, "gate_up")
     _swiglu_case(lib, 2, m, ws.n, ws.k, ws, 0, sampled_blocks=128)
+
+
+@pytest.mark.parametrize("m", [1024, 4096, 8192])
+def test_swiglu_prefill_full_size_sampled(lib, m):
+    """Prefill H7168/I18432, M up to 8192, the launch the prefill chain uses:
+    256 sampled tokens x 32 sampled 16-feature blocks."""
+    ws = weights(3, "gate_up")
+    _swiglu_case(lib, 3, m, ws.n, ws.k, ws, 0, sampled_blocks=32, sampled_tokens=256)
+
+
+@pytest.mark.parametrize("m", [1024, 8192])
+def test_down_prefill_full_size_sampled(lib, m):
+    """Prefill down_proj 7168 x 18432 on an oracle-made NVFP4 h: 256 sampled
+    tokens x 512 sampled output columns."""
+    ws = weights(3, "down")
+    hf = synth.random_matrix((m, ws.k), (24, m), scale=0.05)
+    gs_h = oracle.global_scale(np.abs(hf).max())
+    hq, hs = quantize_rows(hf, gs_h)
+    alpha = np.float32(1.0) / (gs_h * ws.gs)
+    got = run_w4a4(lib, hq, hs, ws.device_prepared(lib), alpha, m, ws.n, ws.k, 0)
+    toks, cols = sample_rows(m, 256, seed=5), sample_rows(ws.n, 512, seed=6)
+    ref = oracle.gemm_w4a4(hq[toks], hs[toks], ws.packed[cols], ws.sf[cols], alpha)
+    err = assert_gemm_close(got[np.ix_(toks, cols)], ref)
+    print(f"prefill down m={m}: rel err {err:.2e}")
+
+
+def quantize_rows(x, gs):
+    from gpu_util import quantize_big
+    return quantize_big(x, gs)
+
+
+def test_tc_bounded_wait_gives_up_cleanly(lib):
+    """A wait limit of one poll makes the pipeline waits run out: the kernel
+    must record NVFP4_ERR_DEVICE_TIMEOUT and return, leaving the context
+    usable for the next (normal) call."""
+    m, n, k = 256, 512, 1024
+    ws = small_weights(n, k, 9)
+    _, _, gs_x, xq, xs = quantized_activation(0, m, k)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    assert lib.nvfp4_get_device_status() == 0
+    lib.nvfp4_set_wait_limit(1)
+    try:
+        run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, TC)
+    finally:
+        lib.nvfp4_set_wait_limit(0)
+    assert lib.nvfp4_get_device_status() == lib.ERR_DEVICE_TIMEOUT
+    assert lib.nvfp4_get_device_status() == 0          # read clears it
+    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, TC)
+    assert_gemm_close(got, oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha))
+
+
+def test_auto_dispatch_matches_forced_paths(lib):
+    """AUTO picks GEMV for decode-sized M and the tensor cores above; both
+    give the same result within tolerance at the crossover."""
+    n, k = 512, 512
+    ws = small_weights(n, k, 10)
+    for m in (16, 17):
+        _, _, gs_x, xq, xs = quantized_activation(0, m, k)
+        alpha = np.float32(1.0) / (gs_x * ws.gs)
+        ref = oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha)
+        for algo in (0, GEMV, TC):
+            assert_gemm_close(run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, algo), ref)
 
 
 # ------------------------------------------------------------------- W4A16
