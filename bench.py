@@ -41,6 +41,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", default="decode", choices=["decode", "prefill", "w4a16"],
+                   help="decode (default line) | prefill H7168/I18432 | w4a16 H5120/I17408")
+    p.add_argument("--m", type=int, default=None, help="single M for prefill / w4a16")
     return p.parse_args()
 
 
@@ -193,51 +196,127 @@ def run_ours(args, world, rank, local):
     def gscale(t):
         return np.float32(np.float32(448.0 * 6.0) / np.float32(t.abs().max().float().item()))
 
-    def make_weight(rows, cols):
+    def make_weight(rows, cols, interleave=False):
         w = (torch.randn(rows, cols, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
         gs = gscale(w)
         q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
         s_lin = torch.empty((rows * cols // 16,), dtype=torch.uint8, device=dev)
         nv.nvfp4_quantize(w, rows, cols, scalar(gs), q, s_lin, nv.SF_LINEAR)
         s = torch.empty((nv.nvfp4_sf_bytes(rows, cols),), dtype=torch.uint8, device=dev)
-        nv.nvfp4_prepare_weights(q, s_lin, rows, cols, q, s)
+        if interleave:
+            qi = torch.empty_like(q)
+            nv.nvfp4_prepare_gate_up_interleaved(q, s_lin, rows, cols, qi, s)
+            q = qi
+        else:
+            nv.nvfp4_prepare_weights(q, s_lin, rows, cols, q, s)
         del w, s_lin
         return q, s, gs
 
-    wgu0 = make_weight(2 * I, H)
-    wdn0 = make_weight(H, I)
-    copies = [(wgu0, wdn0)]
-    for _ in range(NCOPY - 1):
-        copies.append(((wgu0[0].clone(), wgu0[1].clone(), wgu0[2]), (wdn0[0].clone(), wdn0[1].clone(), wdn0[2])))
-    weight_bytes = sum(t.numel() for t in (wgu0[0], wgu0[1], wdn0[0], wdn0[1]))
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    bf16_peak = pk["bf16_tflops"] if pk else 1900.0
+    fp4_peak = bf16_peak * 6.0        # dense FP4 : dense BF16 = 13.5 : 2.25 (nominal)
 
-    mmax = max(MS)
-    x = torch.randn(mmax, H, generator=gen, device=dev).to(torch.bfloat16)
+    wl = args.workload
+    if wl == "decode":
+        hid, inter, ms, ncopy = H, I, MS, NCOPY
+        metric, workload = METRIC, WORKLOAD
+    elif wl == "prefill":
+        hid, inter = 7168, 18432
+        ms = (args.m or 8192,)
+        ncopy = 2
+        metric = f"NVFP4 MLP tokens/s (prefill H7168 I18432, M={ms[0]})"
+        workload = f"prefill dense MLP W4A4 NVFP4 (fused gate_up+SwiGLU+requant), hidden 7168, intermediate 18432, M={ms[0]}"
+    else:
+        hid, inter = H, I
+        ms = (args.m,) if args.m else (1, 16, 128, 1024)
+        ncopy = NCOPY
+        metric = f"W4A16 MLP tokens/s (H5120 I17408, M in {','.join(map(str, ms))})"
+        workload = f"W4A16 dense MLP (bf16 x NVFP4), hidden 5120, intermediate 17408, M in {ms}"
+    tokens_per_step = sum(ms)
+    mmax = max(ms)
+
+    w_gu0 = make_weight(2 * inter, hid, interleave=(wl == "prefill"))
+    w_dn0 = make_weight(hid, inter)
+    copies = [(w_gu0, w_dn0)]
+    for _ in range(ncopy - 1):
+        copies.append(((w_gu0[0].clone(), w_gu0[1].clone(), w_gu0[2]),
+                       (w_dn0[0].clone(), w_dn0[1].clone(), w_dn0[2])))
+    weight_bytes = sum(t.numel() for t in (w_gu0[0], w_gu0[1], w_dn0[0], w_dn0[1]))
+
+    x = torch.randn(mmax, hid, generator=gen, device=dev).to(torch.bfloat16)
     gs_x = gscale(x)
-    # calibrate the static down_proj input scale once from the gate_up output
-    gu_tmp = torch.empty((mmax, 2 * I), dtype=torch.bfloat16, device=dev)
-    xq = torch.empty((mmax, H // 2), dtype=torch.uint8, device=dev)
-    xs = torch.empty((nv.nvfp4_sf_bytes(mmax, H),), dtype=torch.uint8, device=dev)
-    nv.nvfp4_quantize(x, mmax, H, scalar(gs_x), xq, xs)
-    a_gu = scalar(np.float32(1.0) / (gs_x * wgu0[2]))
-    nv.nvfp4_gemm(xq, xs, wgu0[0], wgu0[1], a_gu, gu_tmp, mmax, 2 * I, H)
-    g, u = gu_tmp.float()[:, :I], gu_tmp.float()[:, I:]
-    gs_h = gscale(g * torch.sigmoid(g) * u)
-    a_dn = scalar(np.float32(1.0) / (gs_h * wdn0[2]))
-    gs_x_d, gs_h_d = scalar(gs_x), scalar(gs_h)
+    # calibrate the static down_proj input scale once from one gate_up pass
+    mc = min(mmax, 1024)
+    gu_tmp = torch.empty((mc, 2 * inter), dtype=torch.bfloat16, device=dev)
+    if wl == "w4a16":
+        nv.bf16_fp4_gemm(x[:mc].contiguous(), w_gu0[0], w_gu0[1], scalar(np.float32(1.0) / w_gu0[2]),
+                         gu_tmp, mc, 2 * inter, hid)
+        gs_h, a_gu = None, scalar(np.float32(1.0) / w_gu0[2])
+        a_dn = scalar(np.float32(1.0) / w_dn0[2])
+    else:
+        xq = torch.empty((mc, hid // 2), dtype=torch.uint8, device=dev)
+        xs = torch.empty((nv.nvfp4_sf_bytes(mc, hid),), dtype=torch.uint8, device=dev)
+        nv.nvfp4_quantize(x[:mc].contiguous(), mc, hid, scalar(gs_x), xq, xs)
+        a_gu = scalar(np.float32(1.0) / (gs_x * w_gu0[2]))
+        nv.nvfp4_gemm(xq, xs, w_gu0[0], w_gu0[1], a_gu, gu_tmp, mc, 2 * inter, hid)
+        gf = gu_tmp.float()
+        if wl == "prefill":   # interleaved rows: blocks of 128 = [64 up ; 64 gate]
+            gf = gf.view(mc, 2 * inter // 128, 2, 64)
+            u, g = gf[:, :, 0, :].reshape(mc, inter), gf[:, :, 1, :].reshape(mc, inter)
+        else:
+            g, u = gf[:, :inter], gf[:, inter:]
+        gs_h = gscale(g * torch.sigmoid(g) * u)
+        a_dn = scalar(np.float32(1.0) / (gs_h * w_dn0[2]))
+    gs_x_d = scalar(gs_x)
+    gs_h_d = scalar(gs_h) if gs_h is not None else None
     del gu_tmp
 
-    # per-M buffers
     bufs = {}
-    for m in MS:
+    for m in ms:
         bufs[m] = dict(
-            xq=torch.empty((m, H // 2), dtype=torch.uint8, device=dev),
-            xs=torch.empty((nv.nvfp4_sf_bytes(m, H),), dtype=torch.uint8, device=dev),
-            gu=torch.empty((m, 2 * I), dtype=torch.bfloat16, device=dev),
-            hq=torch.empty((m, I // 2), dtype=torch.uint8, device=dev),
-            hs=torch.empty((nv.nvfp4_sf_bytes(m, I),), dtype=torch.uint8, device=dev),
-            out=torch.empty((m, H), dtype=torch.bfloat16, device=dev))
-    x_in = {m: x[:m].contiguous() for m in MS}
+            xq=torch.empty((m, hid // 2), dtype=torch.uint8, device=dev),
+            xs=torch.empty((nv.nvfp4_sf_bytes(m, hid),), dtype=torch.uint8, device=dev),
+            gu=torch.empty((m, 2 * inter), dtype=torch.bfloat16, device=dev),
+            h16=torch.empty((m, inter), dtype=torch.bfloat16, device=dev),
+            hq=torch.empty((m, inter // 2), dtype=torch.uint8, device=dev),
+            hs=torch.empty((nv.nvfp4_sf_bytes(m, inter),), dtype=torch.uint8, device=dev),
+            out=torch.empty((m, hid), dtype=torch.bfloat16, device=dev))
+    x_in = {m: x[:m].contiguous() for m in ms}
+    # one zero-filled scratch buffer (split-K partials + arrival counters),
+    # sized for the largest GEMM of the chain and shared by its sequential calls
+    ws_bytes = max([nv.nvfp4_workspace_bytes(m, 2 * inter, hid) for m in ms] +
+                   [nv.nvfp4_workspace_bytes(m, hid, inter) for m in ms] + [0])
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def forward(m, wc, ev=None):
+        """One MLP forward; ev = (start, end) events around the dominant kernel."""
+        b = bufs[m]
+        (gq, gsf, _), (dq, dsf, _) = wc
+        if wl == "w4a16":
+            if ev is not None:
+                ev[0].record()
+            nv.bf16_fp4_gemm(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid)
+            if ev is not None:
+                ev[1].record()
+            nv.silu_mul_bf16(b["gu"], m, inter, b["h16"])
+            nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter)
+            return
+        nv.nvfp4_quantize(x_in[m], m, hid, gs_x_d, b["xq"], b["xs"])
+        if ev is not None:
+            ev[0].record()
+        if wl == "prefill":
+            nv.nvfp4_gemm_swiglu_quant(b["xq"], b["xs"], gq, gsf, a_gu, gs_h_d, b["hq"], b["hs"], m,
+                                       2 * inter, hid, ws, ws_bytes)
+        else:
+            nv.nvfp4_gemm(b["xq"], b["xs"], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes)
+        if ev is not None:
+            ev[1].record()
+        if wl == "decode":
+            nv.silu_mul_nvfp4_quantize(b["gu"], m, inter, gs_h_d, b["hq"], b["hs"])
+        nv.nvfp4_gemm(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
+
+    launches_per_step = sum({"decode": 4, "prefill": 3, "w4a16": 3}[wl] for _ in ms)
 
     try:
         torch.cuda.Event(enable_timing=True, external=True)
@@ -245,33 +324,18 @@ def run_ours(args, world, rank, local):
     except TypeError:
         ext_ok = False
 
-    def forward(m, wc, ev=None):
-        b = bufs[m]
-        (gq, gsf, _), (dq, dsf, _) = wc
-        nv.nvfp4_quantize(x_in[m], m, H, gs_x_d, b["xq"], b["xs"])
-        if ev is not None:
-            ev[0].record()
-        nv.nvfp4_gemm(b["xq"], b["xs"], gq, gsf, a_gu, b["gu"], m, 2 * I, H)
-        if ev is not None:
-            ev[1].record()
-        nv.silu_mul_nvfp4_quantize(b["gu"], m, I, gs_h_d, b["hq"], b["hs"])
-        nv.nvfp4_gemm(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, H, I)
-
-    launches_per_step = 4 * len(MS)
-
-    # capture one graph per weight copy, with timing events around gate_up
     stream = torch.cuda.Stream(device=dev)
     graphs, events = [], []
     with torch.cuda.stream(stream):
-        for m in MS:                      # warm the kernels outside capture
+        for m in ms:                      # warm the kernels outside capture
             forward(m, copies[0])
         torch.cuda.synchronize()
-        for c in range(NCOPY):
+        for c in range(ncopy):
             evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                    torch.cuda.Event(enable_timing=True, external=True)) for _ in MS] if ext_ok else None
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in ms] if ext_ok else None
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=stream):
-                for j, m in enumerate(MS):
+                for j, m in enumerate(ms):
                     forward(m, copies[c], evs[j] if evs else None)
             graphs.append(gr)
             events.append(evs)
@@ -283,7 +347,7 @@ def run_ours(args, world, rank, local):
 
     for i in range(args.warmup):
         with torch.cuda.stream(stream):
-            graphs[i % NCOPY].replay()
+            graphs[i % ncopy].replay()
     torch.cuda.synchronize()
 
     clocks = Clocks(local)
@@ -292,71 +356,78 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    gate_ms = []
     with torch.cuda.stream(stream):
         t_start.record()
         for i in range(args.steps):
-            graphs[i % NCOPY].replay()
+            graphs[i % ncopy].replay()
         t_end.record()
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     step_ms = t_start.elapsed_time(t_end) / args.steps
+    dom_ms = None
     if ext_ok:
-        for c in range(min(NCOPY, args.steps)):
-            gate_ms.append([events[c][j][0].elapsed_time(events[c][j][1]) for j in range(len(MS))])
+        # each graph's event nodes hold the times of its last replay in the timed region
+        rows = [[events[c][j][0].elapsed_time(events[c][j][1]) for j in range(len(ms))]
+                for c in range(min(ncopy, args.steps))]
+        dom_ms = [statistics.mean(col) for col in zip(*rows)]
 
     if world > 1:
         t = torch.tensor([step_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         step_ms = float(t.item())
-    value = world * TOKENS_PER_STEP / (step_ms / 1000.0)
+    value = world * tokens_per_step / (step_ms / 1000.0)
 
-    # dominant kernel: the gate_up GEMM (weight stream 34816 x 5120 NVFP4)
-    gu_bytes = lambda m: 2 * I * H // 2 + (2 * I) * H // 16 + m * H // 2 + m * H // 16 + m * 2 * I * 2
-    if gate_ms:
-        per_m = [statistics.mean(col) for col in zip(*gate_ms)]
-    else:
-        per_m = None
-    pk = peaks()
-    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
     roofline = None
-    if per_m:
-        tot_bytes = sum(gu_bytes(m) for m in MS)
-        tot_ms = sum(per_m)
-        achieved = tot_bytes / (tot_ms / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "kernel": "nvfp4_gemm gate_up (34816x5120), M=1..16",
-                    "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": None,
-                    "peak_source": "measured" if pk else "fallback",
-                    "per_m_us": {str(m): 1000.0 * t for m, t in zip(MS, per_m)}}
+    if dom_ms:
+        per_m_us = {str(m): 1000.0 * t for m, t in zip(ms, dom_ms)}
+        tot_s = sum(dom_ms) / 1000.0
+        if wl == "decode":
+            nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 9 // 16 + m * 2 * inter * 2 for m in ms)
+            achieved = nbytes / tot_s / 1e9
+            roofline = {"bound": "hbm", "kernel": "nvfp4_gemm gate_up 34816x5120 (GEMV, M=1..16)",
+                        "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                        "traffic": None, "algorithmic_bytes_per_step": nbytes}
+        elif wl == "prefill":
+            flops = sum(4.0 * m * hid * inter for m in ms)
+            achieved = flops / tot_s / 1e12
+            roofline = {"bound": "tensor", "kernel": "nvfp4_gemm_swiglu_quant gate_up 36864x7168 (tcgen05)",
+                        "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
+                        "traffic": None, "peak_note": "measured bf16 burst x 6 (nominal fp4:bf16)"}
+        else:
+            nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 2 + m * 2 * inter * 2 for m in ms)
+            achieved = nbytes / tot_s / 1e9
+            roofline = {"bound": "hbm", "kernel": "bf16_fp4_gemm gate_up 34816x5120",
+                        "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                        "traffic": None}
+        roofline["per_m_us"] = per_m_us
+        roofline["peak_source"] = "measured" if pk else "fallback"
 
     # end to end through the API: pinned host x in, host result out, per step
     x_host = x.cpu().pin_memory()
-    outs_host = {m: torch.empty((m, H), dtype=torch.bfloat16).pin_memory() for m in MS}
-    h2d = sum(m * H * 2 for m in MS)
-    d2h = sum(m * H * 2 for m in MS)
+    outs_host = {m: torch.empty((m, hid), dtype=torch.bfloat16).pin_memory() for m in ms}
+    h2d = sum(m * hid * 2 for m in ms)
+    d2h = sum(m * hid * 2 for m in ms)
     e2e_steps = max(3, min(args.steps, 20))
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for i in range(2):
-            for m in MS:
+        def e2e_step(i):
+            for m in ms:
                 x_in[m].copy_(x_host[:m], non_blocking=True)
-                forward(m, copies[i % NCOPY])
+                forward(m, copies[i % ncopy])
                 outs_host[m].copy_(bufs[m]["out"], non_blocking=True)
-        torch.cuda.synchronize()
+        for i in range(2):
+            e2e_step(i)
+        stream.synchronize()
         w0 = time.perf_counter()
         for i in range(e2e_steps):
-            for m in MS:
-                x_in[m].copy_(x_host[:m], non_blocking=True)
-                forward(m, copies[i % NCOPY])
-                outs_host[m].copy_(bufs[m]["out"], non_blocking=True)
+            e2e_step(i)
         stream.synchronize()
         e2e_s = (time.perf_counter() - w0) / e2e_steps
-    e2e_value = world * TOKENS_PER_STEP / e2e_s
+    e2e_value = world * tokens_per_step / e2e_s
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and wl == "decode" and not args.no_cpu_baseline:
         tokens, secs, threads = oracle_sample((1, 16))
         cpu = {"value": tokens / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": "CPU oracle (NumPy float64) decode MLP forward at M=1 and M=16, "
@@ -364,11 +435,13 @@ def run_ours(args, world, rank, local):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "nvfp4 (e2m1 x ue4m3, fp32 accumulate)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "tokens_per_step": TOKENS_PER_STEP,
-                       "l2": f"{NCOPY} rotating weight copies, {NCOPY * weight_bytes / 1e6:.0f} MB > L2",
+            "vs_baseline": None,
+            "dtype": "bf16 x nvfp4 (fp32 accumulate)" if wl == "w4a16" else "nvfp4 (e2m1 x ue4m3, fp32 accumulate)",
+            "data": "synthetic",
+            "config": {"workload": workload, "tokens_per_step": tokens_per_step,
+                       "l2": f"{ncopy} rotating weight copies, {ncopy * weight_bytes / 1e6:.0f} MB > L2",
                        "graph": "one CUDA graph per step", "parallelism": f"replicas{world}"},
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

@@ -37,8 +37,14 @@ nvfp4_status check_arch() {
 
 nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
-// Largest M served by the weight-streaming kernels when AUTO is asked.
-constexpr int64_t kSmallM = 16;
+// AUTO kernel choice: the weight-streaming tensor-core kernel (weights as
+// the MMA's M operand) for decode-sized M, the prefill tensor-core kernel
+// above, the CUDA-core GEMV where neither applies.
+nvfp4_algo pick_algo(TcMode mode, int64_t m, int64_t n, int64_t k) {
+  if (m <= 64 && swapab_supported(mode, m, n, k)) return NVFP4_ALGO_TC_SWAPAB;
+  if (m > 16 && tc_supported(mode, false, m, n, k)) return NVFP4_ALGO_TC;
+  return NVFP4_ALGO_GEMV;
+}
 
 nvfp4_status check_gemm_shape(int64_t m, int64_t n, int64_t k) {
   if (m < 0 || n <= 0 || k <= 0) return NVFP4_ERR_INVALID_ARG;
@@ -73,7 +79,12 @@ size_t nvfp4_sf_bytes(int64_t rows, int64_t k, nvfp4_sf_layout layout) {
   return (size_t)((rows + 127) / 128 * 128) * (size_t)((k / 16 + 3) / 4 * 4);
 }
 
-size_t nvfp4_workspace_bytes(int64_t, int64_t, int64_t, nvfp4_algo) { return 0; }
+size_t nvfp4_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo) {
+  if (m <= 0 || n <= 0 || k <= 0) return 0;
+  if (algo == NVFP4_ALGO_AUTO) algo = pick_algo(TC_W4A4, m, n, k);
+  if (algo != NVFP4_ALGO_TC_SWAPAB) return 0;
+  return swapab_workspace_bytes(TC_W4A4, m, n, k);
+}
 
 nvfp4_status nvfp4_quantize(const uint16_t *x, int64_t m, int64_t k, const float *global_scale,
                             uint8_t *out_fp4, uint8_t *out_sf, nvfp4_sf_layout sf_layout,
@@ -111,7 +122,7 @@ nvfp4_status silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16
 
 nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, const uint8_t *b_fp4,
                            const uint8_t *b_sf, const float *alpha, uint16_t *d, int64_t m,
-                           int64_t n, int64_t k, void *, size_t, nvfp4_algo algo,
+                           int64_t n, int64_t k, void *workspace, size_t ws_bytes, nvfp4_algo algo,
                            nvfp4_stream_t stream) {
   if (!a_fp4 || !a_sf || !b_fp4 || !b_sf || !alpha || !d) return NVFP4_ERR_INVALID_ARG;
   if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
@@ -121,16 +132,17 @@ nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, const uint
   if (nvfp4_status s = check_arch()) return s;
   if (m == 0) return NVFP4_OK;
   const cudaStream_t st = (cudaStream_t)stream;
-  if (algo == NVFP4_ALGO_AUTO) {
-    if (m > kSmallM && tc_supported(TC_W4A4, false, m, n, k)) algo = NVFP4_ALGO_TC;
-    else algo = NVFP4_ALGO_GEMV;
-  }
+  if (algo == NVFP4_ALGO_AUTO) algo = pick_algo(TC_W4A4, m, n, k);
   if (algo == NVFP4_ALGO_GEMV)
     return from_cuda(launch_gemv(GEMV_W4A4, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
                                  nullptr, m, n, k, st));
-  const bool swap = algo == NVFP4_ALGO_TC_SWAPAB;
-  if (!tc_supported(TC_W4A4, swap, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  return from_cuda(launch_tc(TC_W4A4, swap, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
+  if (algo == NVFP4_ALGO_TC_SWAPAB) {
+    if (!swapab_supported(TC_W4A4, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    return from_cuda(launch_swapab(TC_W4A4, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
+                                   nullptr, m, n, k, workspace, ws_bytes, g_wait_limit.load(), st));
+  }
+  if (!tc_supported(TC_W4A4, false, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A4, false, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
                              nullptr, m, n, k, g_wait_limit.load(), st));
 }
 
@@ -145,7 +157,7 @@ nvfp4_status nvfp4_gemm_swiglu_quant_ex(const uint8_t *a_fp4, const uint8_t *a_s
                                         const uint8_t *w_int_fp4, const uint8_t *w_int_sf,
                                         const float *alpha, const float *out_global_scale,
                                         uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
-                                        int64_t k, void *, size_t, nvfp4_algo algo,
+                                        int64_t k, void *workspace, size_t ws_bytes, nvfp4_algo algo,
                                         nvfp4_stream_t stream) {
   if (!a_fp4 || !a_sf || !w_int_fp4 || !w_int_sf || !alpha || !out_global_scale || !out_fp4 || !out_sf)
     return NVFP4_ERR_INVALID_ARG;
@@ -158,16 +170,18 @@ nvfp4_status nvfp4_gemm_swiglu_quant_ex(const uint8_t *a_fp4, const uint8_t *a_s
   if (nvfp4_status s = check_arch()) return s;
   if (m == 0) return NVFP4_OK;
   const cudaStream_t st = (cudaStream_t)stream;
-  if (algo == NVFP4_ALGO_AUTO) {
-    if (m > kSmallM && tc_supported(TC_W4A4_SWIGLU, false, m, n, k)) algo = NVFP4_ALGO_TC;
-    else algo = NVFP4_ALGO_GEMV;
-  }
+  if (algo == NVFP4_ALGO_AUTO) algo = pick_algo(TC_W4A4_SWIGLU, m, n, k);
   if (algo == NVFP4_ALGO_GEMV)
     return from_cuda(launch_gemv(GEMV_W4A4_SWIGLU, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
                                  out_global_scale, nullptr, out_fp4, out_sf, m, n, k, st));
-  const bool swap = algo == NVFP4_ALGO_TC_SWAPAB;
-  if (!tc_supported(TC_W4A4_SWIGLU, swap, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  return from_cuda(launch_tc(TC_W4A4_SWIGLU, swap, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
+  if (algo == NVFP4_ALGO_TC_SWAPAB) {
+    if (!swapab_supported(TC_W4A4_SWIGLU, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    return from_cuda(launch_swapab(TC_W4A4_SWIGLU, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
+                                   out_global_scale, nullptr, out_fp4, out_sf, m, n, k, workspace,
+                                   ws_bytes, g_wait_limit.load(), st));
+  }
+  if (!tc_supported(TC_W4A4_SWIGLU, false, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A4_SWIGLU, false, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
                              out_global_scale, nullptr, out_fp4, out_sf, m, n, k,
                              g_wait_limit.load(), st));
 }
@@ -194,16 +208,13 @@ nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uin
   if (nvfp4_status s = check_arch()) return s;
   if (m == 0) return NVFP4_OK;
   const cudaStream_t st = (cudaStream_t)stream;
-  if (algo == NVFP4_ALGO_AUTO) {
-    if (m > kSmallM && tc_supported(TC_W4A16, false, m, n, k)) algo = NVFP4_ALGO_TC;
-    else algo = NVFP4_ALGO_GEMV;
-  }
+  if (algo == NVFP4_ALGO_AUTO) algo = pick_algo(TC_W4A16, m, n, k);
   if (algo == NVFP4_ALGO_GEMV)
     return from_cuda(launch_gemv(GEMV_W4A16, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
                                  nullptr, m, n, k, st));
-  const bool swap = algo == NVFP4_ALGO_TC_SWAPAB;
-  if (!tc_supported(TC_W4A16, swap, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  return from_cuda(launch_tc(TC_W4A16, swap, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
+  if (algo == NVFP4_ALGO_TC_SWAPAB || !tc_supported(TC_W4A16, false, m, n, k))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A16, false, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
                              nullptr, m, n, k, g_wait_limit.load(), st));
 }
 

@@ -1,0 +1,434 @@
+// Decode-sized NVFP4 GEMMs on the tensor cores with the weight as the MMA's
+// 128-row operand ("swap AB"): D^T[n, t] = sum_k W[n, k] * X[t, k], with the
+// tokens (M <= 64) as the MMA's N = 16, 32 or 64.  The weight stream is the
+// roofline, so the kernel is a deep TMA pipeline (6-8 stages of 16 KB weight
+// tiles per SM) feeding one MMA issuer.
+//
+// Work is split into units = (128-row weight tile, K range).  When a tile's K
+// is split over several units, each unit writes its fp32 partial tile to the
+// caller's workspace and bumps the tile's arrival counter; the unit that
+// arrives last sums the partials in split order (so the result does not
+// depend on which CTA finishes last), resets the counter to 0 and runs the
+// epilogue.  The workspace must be zero-filled once before its first use; the
+// kernel leaves its counters at zero after every complete call.
+//
+// Roles per CTA (192 threads, persistent over units): warp 0 TMA producer,
+// warp 1 TMEM owner + MMA issuer (double-buffered accumulators), warps 2..5
+// epilogue (TMEM lane = weight row).  Bounded waits as in gemm_tc.cu.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int BK = 256, KSTEPS = 4;
+constexpr uint32_t W_BYTES = 128 * BK / 2;
+constexpr uint32_t SFW_BYTES = KSTEPS * 512, SFX_BYTES = KSTEPS * 512;
+constexpr int kThreads = 192;
+constexpr int ACC_BUFS = 2;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint32_t kDrainPolls = 1u << 22;
+
+template <int NT>
+struct Cfg {
+  static constexpr uint32_t X_BYTES = NT * BK / 2;
+  static constexpr uint32_t STAGE_BYTES = W_BYTES + X_BYTES + SFW_BYTES + SFX_BYTES;
+  static constexpr int STAGES = NT == 64 ? 6 : 8;
+  static constexpr int PITCH = NT + 1;                      // floats per staged row
+  static constexpr uint32_t OUT_BYTES = 128 * PITCH * 4;
+  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 256;
+  static constexpr uint32_t SFW_COL = ACC_BUFS * NT;
+  static constexpr uint32_t SFX_COL = SFW_COL + 4 * KSTEPS;
+  static constexpr uint32_t USED_COLS = SFX_COL + 4 * KSTEPS;
+  static constexpr uint32_t TMEM_COLS = USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128 : 256;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct SwapArgs {
+  const uint8_t *sfw;   // weight scales, swizzled over N rows
+  const uint8_t *sfx;   // activation scales, swizzled over M rows (one 128-row block)
+  const float *alpha;
+  const float *out_gs;
+  uint16_t *d;          // bf16 [M, N]
+  uint8_t *out_fp4;     // fused: [M, N/4]
+  uint8_t *out_sf;      // fused: swizzled over M rows, N/32 columns
+  float *partials;      // [units][NT][128] fp32 when splits > 1
+  int *counters;        // [tiles] arrival counters when splits > 1
+  int32_t m, n, k;
+  int32_t tiles, splits, kbps, kb_total;
+  uint32_t wait_limit;
+  int *status;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int MODE, int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    swapab_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                  const SwapArgs p) {
+  using C = Cfg<NT>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float *s_out = reinterpret_cast<float *>(base + STAGES * C::STAGE_BYTES);
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + STAGES * C::STAGE_BYTES + C::OUT_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + ACC_BUFS;
+  uint64_t *drain = tempty + ACC_BUFS;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
+  volatile int *last_flag = abort_flag + 1;
+  auto st_w = [&](int s) { return base + s * C::STAGE_BYTES; };
+  auto st_x = [&](int s) { return st_w(s) + W_BYTES; };
+  auto st_sfw = [&](int s) { return st_x(s) + C::X_BYTES; };
+  auto st_sfx = [&](int s) { return st_sfw(s) + SFW_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < ACC_BUFS; ++b) {
+      ptx::mbar_init(&tfull[b], 1);
+      ptx::mbar_init(&tempty[b], 128);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tm_w);
+    ptx::prefetch_tensormap(&tm_x);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tslot, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  const int units = p.tiles * p.splits;
+  const int ksteps_total = p.k >> 6;
+  const int cp4 = ksteps_total;          // 512-byte scale tiles per 128-row block
+  const uint32_t limit = p.wait_limit;
+  uint32_t issued_mask = 0, issued_parity = 0;
+  bool mma_issued = false;
+
+  if (warp == 0) {
+    if (ptx::elect_one()) {
+      const uint64_t pol_w = ptx::l2_policy_evict_first();
+      const uint64_t pol_x = ptx::l2_policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0;
+      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+        const int tile = u / p.splits, sp = u % p.splits;
+        const int kb0 = sp * p.kbps, kb1 = min(kb0 + p.kbps, p.kb_total);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+            break;
+          }
+          const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
+          ptx::mbar_arrive_expect_tx(&full[s], W_BYTES + C::X_BYTES + 2u * (uint32_t)nk * 512u);
+          ptx::tma_load_2d(st_w(s), &tm_w, &full[s], kb * (BK / 2), tile * 128, pol_w);
+          ptx::tma_load_2d(st_x(s), &tm_x, &full[s], kb * (BK / 2), 0, pol_x);
+          ptx::bulk_load(st_sfw(s), p.sfw + ((size_t)tile * cp4 + kb * KSTEPS) * 512, nk * 512u, &full[s],
+                         pol_w);
+          ptx::bulk_load(st_sfx(s), p.sfx + (size_t)kb * KSTEPS * 512, nk * 512u, &full[s], pol_x);
+          issued_mask |= 1u << s;
+          issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (ptx::elect_one()) {
+      // kind::mxf4nvf4, E2M1 x E2M1, UE4M3 scales, M = 128 (weights), N = NT (tokens)
+      constexpr uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) | (8u << 24);
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x, ++it) {
+        const int ab = it & 1;
+        if (!ptx::mbar_wait_bounded(&tempty[ab], (uint32_t)((it >> 1) & 1) ^ 1u, limit, kTimeoutNs, abort_flag)) {
+          *abort_flag = 1;
+          atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+        ptx::tc_fence_after();
+        const int sp = u % p.splits;
+        const int kb0 = sp * p.kbps, kb1 = min(kb0 + p.kbps, p.kb_total);
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_bounded(&full[s], ph, limit, kTimeoutNs, abort_flag)) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
+          const uint32_t sfw_s = ptx::smem_u32(st_sfw(s)), sfx_s = ptx::smem_u32(st_sfx(s));
+          for (int j = 0; j < nk; ++j) {
+            ptx::tmem_cp_32x128b_x4(tmem + C::SFW_COL + 4 * j, ptx::smem_desc(sfw_s + 512 * j, 0, 128, 0));
+            ptx::tmem_cp_32x128b_x4(tmem + C::SFX_COL + 4 * j, ptx::smem_desc(sfx_s + 512 * j, 0, 128, 0));
+          }
+          const uint32_t w_s = ptx::smem_u32(st_w(s)), x_s = ptx::smem_u32(st_x(s));
+          for (int j = 0; j < nk; ++j)
+            ptx::mma_nvfp4(tmem + ab * NT, ptx::smem_desc(w_s + 32 * j, 16, 1024, 2),
+                           ptx::smem_desc(x_s + 32 * j, 16, 1024, 2), idesc, tmem + C::SFW_COL + 4 * j,
+                           tmem + C::SFX_COL + 4 * j, (kb != kb0) || (j != 0));
+          mma_issued = true;
+          ptx::tc_commit(&empty[s]);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::tc_commit(&tfull[ab]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;                 // weight row within the tile
+    const int et = threadIdx.x - 64;             // 0..127 across the epilogue warps
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    const float alpha = __ldg(p.alpha);
+    const int mt = min(p.m, NT);
+    int it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+      const int ab = it & 1;
+      if (!ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag)) {
+        *abort_flag = 1;
+        atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      ptx::tc_fence_after();
+      float v[NT];
+#pragma unroll
+      for (int c = 0; c < NT / 16; ++c) {
+        uint32_t raw[16];
+        ptx::tmem_ld16(t_row + ab * NT + 16 * c, raw);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[16 * c + i] = __uint_as_float(raw[i]);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[ab]);              // accumulator buffer free again
+
+      const int tile = u / p.splits;
+      if (p.splits > 1) {
+        float *part = p.partials + (size_t)u * NT * 128;
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          if (t < mt) part[t * 128 + r] = v[t];
+        __threadfence();
+        epi_bar();
+        if (et == 0) *last_flag = (atomicAdd(&p.counters[tile], 1) == p.splits - 1);
+        epi_bar();
+        if (!*last_flag) continue;
+        __threadfence();
+        const float *tp = p.partials + (size_t)tile * p.splits * NT * 128;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          float acc = 0.0f;
+          if (t < mt)
+            for (int s2 = 0; s2 < p.splits; ++s2) acc += __ldcg(tp + ((size_t)s2 * NT + t) * 128 + r);
+          v[t] = acc;
+        }
+        if (et == 0) p.counters[tile] = 0;
+      }
+
+      const int n = tile * 128 + r;
+      if constexpr (MODE == TC_W4A4) {
+        if (n < p.n) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            if (t < mt) {
+              const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v[t]);
+              p.d[(size_t)t * p.n + n] = *reinterpret_cast<const uint16_t *>(&o);
+            }
+        }
+      } else {
+        // rows 0..63 of the tile are up, 64..127 gate, for features 64*tile + (0..63)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) s_out[r * C::PITCH + t] = alpha * v[t];
+        epi_bar();
+        const int inter = p.n >> 1;
+        const int ocp4 = ((inter >> 4) + 3) >> 2;
+        const float gs = __ldg(p.out_gs);
+        for (int idx = et; idx < mt * 4; idx += 128) {
+          const int t = idx >> 2, qb = idx & 3;
+          float h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            h[i] = silu_mul(s_out[(64 + 16 * qb + i) * C::PITCH + t], s_out[(16 * qb + i) * C::PITCH + t]);
+          uint32_t lo, hi;
+          const uint32_t sf = quantize_block16(h, gs, lo, hi);
+          const int f = 64 * tile + 16 * qb;
+          *reinterpret_cast<uint2 *>(p.out_fp4 + (size_t)t * (inter >> 1) + f / 2) = make_uint2(lo, hi);
+          p.out_sf[sf_swizzled_offset(t, f >> 4, ocp4)] = (uint8_t)sf;
+        }
+        // padding rows of the 128-row scale block: zero this tile's 4 columns
+        const int mpad = (p.m + 127) & ~127;
+        for (int t = p.m + et; t < mpad; t += 128)
+          *reinterpret_cast<uint32_t *>(p.out_sf + sf_swizzled_offset(t, tile * 4, ocp4)) = 0u;
+        epi_bar();
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 0 && issued_mask) {
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_mask & (1u << s)) {
+          volatile int no_abort = 0;
+          ptx::mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, kDrainPolls, 0, &no_abort);
+        }
+    }
+    if (warp == 1 && mma_issued) {
+      volatile int no_abort = 0;
+      ptx::tc_commit(drain);
+      ptx::mbar_wait_bounded(drain, 0, kDrainPolls, 0, &no_abort);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+struct Plan {
+  int nt, tiles, splits, kbps, kb_total;
+  size_t ws_bytes;
+};
+
+// Choose the K split so that units spread evenly over the SMs: minimise
+// (units per SM, rounded up) x (k-blocks per unit + per-unit overhead).
+Plan make_plan(int64_t m, int64_t n, int64_t k) {
+  Plan pl{};
+  pl.nt = m <= 16 ? 16 : m <= 32 ? 32 : 64;
+  pl.tiles = (int)((n + 127) / 128);
+  pl.kb_total = (int)((k + BK - 1) / BK);
+  const int sms = num_sms();
+  double best = 1e30;
+  for (int kbps = pl.kb_total; kbps >= 1; --kbps) {
+    const int splits = (pl.kb_total + kbps - 1) / kbps;
+    if (splits > 64) break;
+    const int units = pl.tiles * splits;
+    const int waves = (units + sms - 1) / sms;
+    const double cost = waves * (kbps + 0.5);
+    if (cost < best - 1e-9) {
+      best = cost;
+      pl.kbps = kbps;
+      pl.splits = splits;
+    }
+  }
+  pl.ws_bytes = pl.splits > 1 ? ((size_t)pl.tiles * 4 + 255) / 256 * 256 +
+                                    (size_t)pl.tiles * pl.splits * pl.nt * 128 * 4
+                              : 0;
+  return pl;
+}
+
+template <int MODE, int NT>
+cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, const uint8_t *w,
+                      const uint8_t *w_sf, const float *alpha, const float *out_gs, uint16_t *d,
+                      uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k, void *ws,
+                      uint32_t wait_limit, cudaStream_t st) {
+  using C = Cfg<NT>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(swapab_kernel<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap tm_w, tm_x;
+  if (!make_byte_map(&tm_w, w, n, k / 2, 128, 128, true) || !make_byte_map(&tm_x, x, m, k / 2, 128, NT, true))
+    return cudaErrorInvalidValue;
+  SwapArgs a{};
+  a.sfw = w_sf;
+  a.sfx = x_sf;
+  a.alpha = alpha;
+  a.out_gs = out_gs;
+  a.d = d;
+  a.out_fp4 = out_fp4;
+  a.out_sf = out_sf;
+  if (pl.splits > 1) {
+    a.counters = static_cast<int *>(ws);
+    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)pl.tiles * 4 + 255) / 256 * 256);
+  }
+  a.m = (int32_t)m;
+  a.n = (int32_t)n;
+  a.k = (int32_t)k;
+  a.tiles = pl.tiles;
+  a.splits = pl.splits;
+  a.kbps = pl.kbps;
+  a.kb_total = pl.kb_total;
+  a.wait_limit = wait_limit;
+  a.status = device_status_ptr();
+  if (!a.status) return cudaErrorInvalidValue;
+  const int units = pl.tiles * pl.splits;
+  const int grid = units < num_sms() ? units : num_sms();
+  swapab_kernel<MODE, NT><<<grid, kThreads, C::SMEM_BYTES, st>>>(tm_w, tm_x, a);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, const uint8_t *w,
+                        const uint8_t *w_sf, const float *alpha, const float *out_gs, uint16_t *d,
+                        uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k, void *ws,
+                        uint32_t wait_limit, cudaStream_t st) {
+  switch (pl.nt) {
+    case 16:
+      return launch_nt<MODE, 16>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
+                                 wait_limit, st);
+    case 32:
+      return launch_nt<MODE, 32>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
+                                 wait_limit, st);
+    default:
+      return launch_nt<MODE, 64>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
+                                 wait_limit, st);
+  }
+}
+
+}  // namespace
+
+bool swapab_supported(TcMode mode, int64_t m, int64_t n, int64_t k) {
+  if (mode == TC_W4A16) return false;
+  if (m <= 0 || m > 64 || k % 64 != 0 || n % 32 != 0) return false;
+  if (mode == TC_W4A4_SWIGLU && n % 128 != 0) return false;
+  return n < (1 << 30) && k < (1 << 30);
+}
+
+size_t swapab_workspace_bytes(TcMode mode, int64_t m, int64_t n, int64_t k) {
+  if (!swapab_supported(mode, m, n, k)) return 0;
+  return make_plan(m, n, k).ws_bytes;
+}
+
+cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,
+                          const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
+                          uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
+                          void *workspace, size_t ws_bytes, uint32_t wait_limit, cudaStream_t st) {
+  if (!swapab_supported(mode, m, n, k)) return cudaErrorNotSupported;
+  Plan pl = make_plan(m, n, k);
+  if (pl.splits > 1 && (workspace == nullptr || ws_bytes < pl.ws_bytes)) {
+    // not enough scratch for the balanced split: one unit per weight tile
+    pl.splits = 1;
+    pl.kbps = pl.kb_total;
+    pl.ws_bytes = 0;
+  }
+  const uint8_t *x = static_cast<const uint8_t *>(a);
+  if (mode == TC_W4A4)
+    return launch_mode<TC_W4A4>(pl, x, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, workspace,
+                                wait_limit, st);
+  return launch_mode<TC_W4A4_SWIGLU>(pl, x, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k,
+                                     workspace, wait_limit, st);
+}
+
+}  // namespace nvfp4

@@ -36,6 +36,17 @@ cudaError_t read_and_clear_device_status(int *out) {
   return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
 }
 
+int *device_status_ptr() {
+  static int *cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) cache[dev] = static_cast<int *>(p);
+  }
+  return cache[dev];
+}
+
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 256;
@@ -71,6 +82,7 @@ struct TcArgs {
   int32_t m, n, k;
   int32_t num_m, num_n;
   uint32_t wait_limit;
+  int *status;            // device status word
 };
 
 struct Smem {
@@ -88,9 +100,9 @@ struct Smem {
   __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(tslot() + 1); }
 };
 
-__device__ __forceinline__ void give_up(volatile int *abort_flag) {
+__device__ __forceinline__ void give_up(volatile int *abort_flag, int *status) {
   *abort_flag = 1;
-  atomicCAS(&g_device_status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+  atomicCAS(status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -150,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mt = tile % p.num_m, nt = tile / p.num_m;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!ptx::mbar_wait_bounded(&sm.empty()[s], ph ^ 1u, limit, kDefaultTimeoutNs, abort_flag)) {
-            give_up(abort_flag);
+            give_up(abort_flag, p.status);
             break;
           }
           const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
         if (!ptx::mbar_wait_bounded(sm.tempty(), (uint32_t)(it & 1) ^ 1u, limit, kDefaultTimeoutNs,
                                     abort_flag)) {
-          give_up(abort_flag);
+          give_up(abort_flag, p.status);
           break;
         }
         ptx::tc_fence_after();
@@ -189,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
-            give_up(abort_flag);
+            give_up(abort_flag, p.status);
             ok = false;
             break;
           }
@@ -225,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
       if (!ptx::mbar_wait_bounded(sm.tfull(), (uint32_t)(it & 1), limit, kDefaultTimeoutNs, abort_flag)) {
-        give_up(abort_flag);
+        give_up(abort_flag, p.status);
         break;
       }
       ptx::tc_fence_after();
@@ -325,18 +337,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2-D map over packed NVFP4 codes [rows, k/2] bytes; box 128 bytes x box_rows,
-// 128-byte swizzle; out-of-range rows and columns read as zero.
-bool make_code_map(CUtensorMap *tm, const uint8_t *ptr, int64_t rows, int64_t k, uint32_t box_rows) {
+}  // namespace
+
+bool make_byte_map(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t row_bytes, uint32_t box_bytes,
+                   uint32_t box_rows, bool swizzle128) {
   auto encode = get_encode();
   if (!encode) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
-  cuuint32_t box[2] = {128u, box_rows};
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {box_bytes, box_rows};
   cuuint32_t estr[2] = {1u, 1u};
-  return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(ptr), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int num_sms() {
@@ -352,6 +366,8 @@ int num_sms() {
   return cache[dev];
 }
 
+namespace {
+
 template <int MODE>
 cudaError_t launch_mode(const uint8_t *a, const uint8_t *a_sf, const uint8_t *b, const uint8_t *b_sf,
                         const float *alpha, const float *out_gs, uint16_t *d, uint8_t *out_fp4,
@@ -365,9 +381,12 @@ cudaError_t launch_mode(const uint8_t *a, const uint8_t *a_sf, const uint8_t *b,
     attr_set = true;
   }
   CUtensorMap tm_a, tm_b;
-  if (!make_code_map(&tm_a, a, m, k, BM) || !make_code_map(&tm_b, b, n, k, BN)) return cudaErrorInvalidValue;
+  // codes [rows, k/2] bytes; box 128 bytes of K x tile rows, 128-byte swizzle
+  if (!make_byte_map(&tm_a, a, m, k / 2, 128, BM, true) || !make_byte_map(&tm_b, b, n, k / 2, 128, BN, true))
+    return cudaErrorInvalidValue;
   TcArgs args{a_sf, b_sf, alpha, out_gs, d, out_fp4, out_sf, (int32_t)m, (int32_t)n, (int32_t)k,
-              (int32_t)((m + BM - 1) / BM), (int32_t)((n + BN - 1) / BN), wait_limit};
+              (int32_t)((m + BM - 1) / BM), (int32_t)((n + BN - 1) / BN), wait_limit, device_status_ptr()};
+  if (!args.status) return cudaErrorInvalidValue;
   const int tiles = args.num_m * args.num_n;
   const int grid = tiles < num_sms() ? tiles : num_sms();
   tc_gemm_kernel<MODE><<<grid, kThreads, SMEM_BYTES, st>>>(tm_a, tm_b, args);

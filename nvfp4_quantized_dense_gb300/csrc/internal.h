@@ -2,6 +2,7 @@
 // Arguments are validated by the caller (api.cu) before any launcher runs.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,5 +37,23 @@ bool tc_supported(TcMode mode, bool swap_ab, int64_t m, int64_t n, int64_t k);
 // Device status word of the current device (set by kernels that give up a
 // bounded wait); reads it into *out and clears it.  Synchronous.
 cudaError_t read_and_clear_device_status(int *out);
+// Device address of that word, for kernels in any translation unit.
+int *device_status_ptr();
+
+// Host helpers shared by the tensor-core units.
+int num_sms();
+// 2-D TMA map over a row-major byte matrix [rows, row_bytes] (row stride
+// row_bytes), box box_bytes x box_rows, 128-byte swizzle when swizzle128.
+bool make_byte_map(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t row_bytes,
+                   uint32_t box_bytes, uint32_t box_rows, bool swizzle128);
+
+// Decode-sized tensor-core path (weights as the MMA M operand).
+size_t swapab_workspace_bytes(TcMode mode, int64_t m, int64_t n, int64_t k);
+bool swapab_supported(TcMode mode, int64_t m, int64_t n, int64_t k);
+cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,
+                          const uint8_t *b_sf, const float *alpha, const float *out_gs,
+                          uint16_t *d, uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
+                          int64_t k, void *workspace, size_t ws_bytes, uint32_t wait_limit,
+                          cudaStream_t st);
 
 }  // namespace nvfp4

@@ -25,10 +25,17 @@ pytestmark = pytest.mark.gpu
 GEMV, TC, TC_SWAPAB = 1, 2, 3
 
 
-def run_w4a4(nv, xq, xs, wdev, alpha, m, n, k, algo):
+def workspace(nv, m, n, k, algo):
+    """Zero-filled scratch of the size the library asks for (None if none)."""
+    nbytes = nv.nvfp4_workspace_bytes(m, n, k, algo)
+    return (torch.zeros(nbytes, dtype=torch.uint8, device="cuda"), nbytes) if nbytes else (None, 0)
+
+
+def run_w4a4(nv, xq, xs, wdev, alpha, m, n, k, algo, ws=None):
     d = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    w, nbytes = ws if ws is not None else workspace(nv, m, n, k, algo)
     nv.nvfp4_gemm_ex(dev(xq), dev(oracle.sf_swizzle_128x4(xs)), wdev[0], wdev[1], scalar(alpha), d,
-                     m, n, k, algo=algo)
+                     m, n, k, w, nbytes, algo=algo)
     torch.cuda.synchronize()
     return bf16_host(d)
 
@@ -37,8 +44,9 @@ def run_swiglu(nv, xq, xs, wdev, alpha, gs_h, m, n, k, algo):
     inter = n // 2
     q = torch.full((m, inter // 2), 0xAB, dtype=torch.uint8, device="cuda")
     s = torch.full((nv.nvfp4_sf_bytes(m, inter),), 0xAB, dtype=torch.uint8, device="cuda")
+    w, nbytes = workspace(nv, m, n, k, algo)
     nv.nvfp4_gemm_swiglu_quant_ex(dev(xq), dev(oracle.sf_swizzle_128x4(xs)), wdev[0], wdev[1],
-                                  scalar(alpha), scalar(gs_h), q, s, m, n, k, algo=algo)
+                                  scalar(alpha), scalar(gs_h), q, s, m, n, k, w, nbytes, algo=algo)
     torch.cuda.synchronize()
     s = host(s)
     lin = oracle.sf_unswizzle_128x4(s, m, inter // 16)
@@ -62,8 +70,14 @@ TC_SHAPES = [(128, 256, 256), (1, 256, 256), (130, 160, 320), (256, 512, 1024), 
              (384, 1024, 2048), (1000, 2304, 512), (4096, 4096, 256)]
 
 
+# swap-AB (weights as the MMA M operand): tokens padded to 16/32/64, split-K
+SWAP_SHAPES = [(1, 256, 256), (4, 1024, 256), (3, 96, 320), (16, 512, 2048), (17, 128, 128),
+               (33, 384, 1024), (64, 256, 512), (8, 2048, 8192)]
+
+
 @pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SMALL_SHAPES] +
-                         [(m, n, k, TC) for m, n, k in TC_SHAPES])
+                         [(m, n, k, TC) for m, n, k in TC_SHAPES] +
+                         [(m, n, k, TC_SWAPAB) for m, n, k in SWAP_SHAPES])
 def test_w4a4_small_shapes(lib, m, n, k, algo):
     ws = small_weights(n, k, 3)
     _, _, gs_x, xq, xs = quantized_activation(0, m, k)
@@ -74,9 +88,10 @@ def test_w4a4_small_shapes(lib, m, n, k, algo):
     print(f"w4a4 algo={algo} m={m} n={n} k={k}: rel err {err:.2e}")
 
 
+@pytest.mark.parametrize("algo", [GEMV, TC_SWAPAB])
 @pytest.mark.parametrize("which", ["gate_up", "down"])
 @pytest.mark.parametrize("m", [1, 2, 4, 8, 16])
-def test_w4a4_decode_full_size_sampled(lib, m, which):
+def test_w4a4_decode_full_size_sampled(lib, m, which, algo):
     """Decode workload H5120/I17408: gate_up 34816x5120 and down 5120x17408."""
     ws = weights(1, which)
     k = ws.k
@@ -87,20 +102,36 @@ def test_w4a4_decode_full_size_sampled(lib, m, which):
         gs_x = oracle.global_scale(np.abs(hf).max())
         xq, xs = oracle.quantize_nvfp4(hf, gs_x)
     alpha = np.float32(1.0) / (gs_x * ws.gs)
-    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, ws.n, k, 0)
+    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, ws.n, k, algo)
     cols = sample_rows(ws.n, 512, seed=m)
     ref = oracle.gemm_w4a4(xq, xs, ws.packed[cols], ws.sf[cols], alpha)
     err = assert_gemm_close(got[:, cols], ref)
-    print(f"decode {which} m={m}: rel err {err:.2e}")
+    print(f"decode {which} m={m} algo={algo}: rel err {err:.2e}")
 
 
-def test_w4a4_is_deterministic(lib):
-    ws = small_weights(512, 512, 4)
-    _, _, gs_x, xq, xs = quantized_activation(0, 8, 512)
+@pytest.mark.parametrize("algo", [GEMV, TC, TC_SWAPAB])
+def test_w4a4_is_deterministic(lib, algo):
+    m, n, k = 16, 1024, 4096
+    ws = small_weights(n, k, 4)
+    _, _, gs_x, xq, xs = quantized_activation(0, m, k)
     alpha = np.float32(1.0) / (gs_x * ws.gs)
-    a = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, 8, 512, 512, 0)
-    b = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, 8, 512, 512, 0)
+    scratch = workspace(lib, m, n, k, algo)
+    a = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, algo, scratch)
+    b = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, algo, scratch)
     assert np.array_equal(a, b)
+    if scratch[0] is not None:   # split-K arrival counters are back at zero
+        ntiles = (n + 127) // 128
+        assert int(scratch[0][: 4 * ntiles].view(torch.int32).abs().sum()) == 0
+
+
+def test_swapab_without_workspace_still_correct(lib):
+    """Too little scratch: the kernel runs one unit per weight tile instead."""
+    m, n, k = 4, 512, 4096
+    ws = small_weights(n, k, 11)
+    _, _, gs_x, xq, xs = quantized_activation(0, m, k)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, TC_SWAPAB, (None, 0))
+    assert_gemm_close(got, oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha))
 
 
 def test_gemm_m_zero_is_a_noop(lib):
@@ -137,18 +168,24 @@ SWIGLU_GEMV = [(4, 1024, 256), (1, 256, 512), (3, 128, 320), (16, 384, 256), (13
 SWIGLU_TC = [(128, 256, 256), (4, 1024, 256), (130, 384, 320), (256, 1024, 1024), (700, 2304, 512)]
 
 
+SWIGLU_SWAP = [(1, 256, 256), (4, 1024, 256), (3, 128, 320), (16, 384, 4096), (40, 256, 512),
+               (64, 1024, 1024)]
+
+
 @pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SWIGLU_GEMV] +
-                         [(m, n, k, TC) for m, n, k in SWIGLU_TC])
+                         [(m, n, k, TC) for m, n, k in SWIGLU_TC] +
+                         [(m, n, k, TC_SWAPAB) for m, n, k in SWIGLU_SWAP])
 def test_swiglu_small_shapes(lib, m, n, k, algo):
     _swiglu_case(lib, 0, m, n, k, small_weights(n, k, 6), algo)
 
 
+@pytest.mark.parametrize("algo", [GEMV, TC_SWAPAB])
 @pytest.mark.parametrize("m", [1, 8, 32, 64])
-def test_swiglu_deepseek_decode_full_size_sampled(lib, m):
+def test_swiglu_deepseek_decode_full_size_sampled(lib, m, algo):
     """DeepSeek-V3-shaped decode, x with 1% outliers x20, interleaved
     36864x7168 gate_up weight; 128 sampled 16-feature blocks."""
     ws = weights(2, "gate_up")
-    _swiglu_case(lib, 2, m, ws.n, ws.k, ws, 0, sampled_blocks=128)
+    _swiglu_case(lib, 2, m, ws.n, ws.k, ws, algo, sampled_blocks=128)
 
 
 @pytest.mark.parametrize("m", [1024, 4096, 8192])
@@ -205,11 +242,11 @@ def test_auto_dispatch_matches_forced_paths(lib):
     give the same result within tolerance at the crossover."""
     n, k = 512, 512
     ws = small_weights(n, k, 10)
-    for m in (16, 17):
+    for m in (16, 17, 64, 65):
         _, _, gs_x, xq, xs = quantized_activation(0, m, k)
         alpha = np.float32(1.0) / (gs_x * ws.gs)
         ref = oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha)
-        for algo in (0, GEMV, TC):
+        for algo in (0, GEMV, TC) + ((TC_SWAPAB,) if m <= 64 else ()):
             assert_gemm_close(run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, algo), ref)
 
 
@@ -265,11 +302,13 @@ def test_tiny_mlp_chain_end_to_end(lib):
     hq_d = torch.empty((m, i_ // 2), dtype=torch.uint8, device="cuda")
     hs_d = torch.empty((lib.nvfp4_sf_bytes(m, i_),), dtype=torch.uint8, device="cuda")
     wi = wgu.device_interleaved(lib)
+    w1, n1 = workspace(lib, m, 2 * i_, h_, 0)
     lib.nvfp4_gemm_swiglu_quant(xq_d, xs_d, wi[0], wi[1], scalar(a_gu), scalar(gs_h), hq_d, hs_d,
-                                m, 2 * i_, h_)
+                                m, 2 * i_, h_, w1, n1)
     out = torch.empty((m, h_), dtype=torch.bfloat16, device="cuda")
     wd = wdn.device_prepared(lib)
-    lib.nvfp4_gemm(hq_d, hs_d, wd[0], wd[1], scalar(a_dn), out, m, h_, i_)
+    w2, n2 = workspace(lib, m, h_, i_, 0)
+    lib.nvfp4_gemm(hq_d, hs_d, wd[0], wd[1], scalar(a_dn), out, m, h_, i_, w2, n2)
     torch.cuda.synchronize()
     err = assert_gemm_close(bf16_host(out), ref, tol=5e-3, what="tiny MLP end to end")
     print(f"tiny MLP end-to-end rel err {err:.2e}")
