@@ -24,7 +24,8 @@
  *  - Every pointer argument except status_out is a DEVICE pointer to memory
  *    the caller owns (allocated by the caller, e.g. through PyTorch).  The
  *    library never allocates, frees or logs, and holds no state between calls
- *    other than the device status word (nvfp4_get_device_status).
+ *    other than the device status word (nvfp4_get_device_status) and the
+ *    fixed scratch array of nvfp4_gemm_decode_noalloc.
  *  - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
  *  - Scalars (global_scale, alpha, out_global_scale) are 1-element fp32
  *    DEVICE buffers, so a call sequence can be captured in a CUDA graph.
@@ -96,8 +97,16 @@ int nvfp4_version(void);
  * Returns 0 for invalid arguments. */
 size_t nvfp4_sf_bytes(int64_t rows, int64_t k, nvfp4_sf_layout layout);
 
-/* Scratch bytes the GEMM entry points need for (m, n, k) with `algo`.  All
- * current kernels return 0 (no scratch); pass workspace = NULL, ws_bytes = 0. */
+/* Scratch bytes the GEMM entry points want for (m, n, k) with `algo` (AUTO
+ * resolves as the GEMM would).  Non-zero only for the weight-streaming
+ * tensor-core kernel (NVFP4_ALGO_TC_SWAPAB, AUTO for m <= 64), which splits K
+ * across CTAs: fp32 partial tiles plus one arrival counter per 128-row weight
+ * tile.  The workspace must be zero-filled once before its first use; every
+ * complete call leaves the counters at zero again, so one buffer serves a
+ * whole sequence of calls on one stream (not concurrent calls).  After a call
+ * that reported NVFP4_ERR_DEVICE_TIMEOUT, zero it again.  A smaller or NULL
+ * workspace is not an error: the kernel then runs one CTA per weight tile
+ * without splitting K. */
 size_t nvfp4_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo);
 
 /* NVFP4 quantize of bf16 activations ([P2] deepseek_v2.py excerpt:
@@ -208,6 +217,26 @@ nvfp4_status nvfp4_prepare_weights(const uint8_t *w_fp4, const uint8_t *sf_linea
 nvfp4_status nvfp4_prepare_gate_up_interleaved(const uint8_t *w_fp4, const uint8_t *sf_linear,
                                                int64_t n, int64_t k, uint8_t *w_out,
                                                uint8_t *sf_out, nvfp4_stream_t stream);
+
+/* Decode W4A4 GEMM that allocates nothing (the source pages have no
+ * counterpart to this call).  Same operands, result and tolerance as
+ * nvfp4_gemm_ex with NVFP4_ALGO_TC_SWAPAB, for callers that cannot hand the
+ * library a workspace: the split-K scratch comes from an 8 MiB array inside
+ * the library (one per GPU that loads it, held until the process exits).
+ *   Requires 1 <= m <= 64 (m == 0 is a no-op), k % 64 == 0, n % 32 == 0, and
+ *   that the split plan for (m, n, k) fits in the 8 MiB; otherwise
+ *   NVFP4_ERR_UNSUPPORTED_SHAPE and nothing runs.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Each call zeroes the array's arrival counters on `stream` before its
+ *   kernel, and the array keeps the last call's partial sums afterwards.  All
+ *   calls on a device share the one array, so calls that can run on the GPU
+ *   at the same time (for instance on two streams) race on it: serialize
+ *   them.  Calls no cudaMalloc/cudaFree or other allocating routine. */
+nvfp4_status nvfp4_gemm_decode_noalloc(const uint8_t *a_fp4, const uint8_t *a_sf,
+                                       const uint8_t *b_fp4, const uint8_t *b_sf,
+                                       const float *alpha, uint16_t *d, int64_t m, int64_t n,
+                                       int64_t k, nvfp4_stream_t stream);
 
 /* Synchronizes `stream`, then returns in *status_out (HOST pointer) the
  * device status word of the current device -- NVFP4_OK, or

@@ -39,6 +39,7 @@ _SIGS = {
     "bf16_fp4_gemm_ex": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
     "nvfp4_prepare_weights": [_P, _P, _I64, _I64, _P, _P, _P],
     "nvfp4_prepare_gate_up_interleaved": [_P, _P, _I64, _I64, _P, _P, _P],
+    "nvfp4_gemm_decode_noalloc": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
     "nvfp4_get_device_status": [ctypes.POINTER(_I), _P],
     "nvfp4_set_wait_limit": [ctypes.c_uint32],
 }
@@ -164,6 +165,13 @@ def nvfp4_prepare_weights(w_fp4, sf_linear, n, k, w_out, sf_out, stream=None):
 def nvfp4_prepare_gate_up_interleaved(w_fp4, sf_linear, n, k, w_out, sf_out, stream=None):
     _call("nvfp4_prepare_gate_up_interleaved", _ptr(w_fp4), _ptr(sf_linear), n, k, _ptr(w_out),
           _ptr(sf_out), _stream(stream))
+
+
+def nvfp4_gemm_decode_noalloc(a_fp4, a_sf, b_fp4, b_sf, alpha, d, m, n, k, stream=None):
+    """Decode GEMM whose split-K scratch lives inside the library (for
+    callers that cannot provide a workspace)."""
+    _call("nvfp4_gemm_decode_noalloc", _ptr(a_fp4), _ptr(a_sf), _ptr(b_fp4), _ptr(b_sf), _ptr(alpha),
+          _ptr(d), m, n, k, _stream(stream))
 
 
 def nvfp4_get_device_status(stream=None):
