@@ -208,14 +208,15 @@ nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uin
   if (nvfp4_status s = check_arch()) return s;
   if (m == 0) return NVFP4_OK;
   const cudaStream_t st = (cudaStream_t)stream;
-  if (algo == NVFP4_ALGO_AUTO) algo = pick_algo(TC_W4A16, m, n, k);
+  // The W4A16 tensor-core kernel always has the weight as the MMA's 128-row
+  // operand, so NVFP4_ALGO_TC and NVFP4_ALGO_TC_SWAPAB name the same kernel.
+  if (algo == NVFP4_ALGO_AUTO)
+    algo = w4a16_tc_supported(m, n, k) ? NVFP4_ALGO_TC : NVFP4_ALGO_GEMV;
   if (algo == NVFP4_ALGO_GEMV)
     return from_cuda(launch_gemv(GEMV_W4A16, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
                                  nullptr, m, n, k, st));
-  if (algo == NVFP4_ALGO_TC_SWAPAB || !tc_supported(TC_W4A16, false, m, n, k))
-    return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  return from_cuda(launch_tc(TC_W4A16, false, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
-                             nullptr, m, n, k, g_wait_limit.load(), st));
+  if (!w4a16_tc_supported(m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_w4a16_tc(a, b_fp4, b_sf, alpha, d, m, n, k, g_wait_limit.load(), st));
 }
 
 nvfp4_status bf16_fp4_gemm(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,

@@ -11,17 +11,25 @@
 namespace nvfp4 {
 
 // ---------------------------------------------------------------------------
-// E2M1 encode, round to nearest even with saturation at 6.  The magnitude
-// code is the number of decision thresholds |v| lies above: a threshold is a
-// midpoint between neighbouring magnitudes {0,.5,1,1.5,2,3,4,6}; at an exact
-// midpoint the even code wins, which is ">" for midpoints whose lower
-// neighbour has an even code and ">=" for the others.  Bit 3 copies the sign
-// bit of v (so -0.1 encodes as 0x8).
-__device__ __forceinline__ uint32_t e2m1_encode(float v) {
-  const float a = fabsf(v);
-  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-               (a >= 3.5f) + (a > 5.0f);
-  return c | ((__float_as_uint(v) >> 28) & 8u);
+// E2M1 encode of eight floats into one word (element i in nibble i), with the
+// PTX conversion cvt.rn.satfinite.e2m1x2.f32: round to nearest even, magnitudes
+// past 6 saturate to 6, the sign bit is kept (a negative value that rounds to
+// zero gives code 0x8).  The instruction puts its first source operand in the
+// high nibble.
+__device__ __forceinline__ uint32_t e2m1_pack8(float v0, float v1, float v2, float v3, float v4, float v5,
+                                               float v6, float v7) {
+  uint32_t w;
+  asm("{\n"
+      ".reg .b8 b0, b1, b2, b3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      "mov.b32 %0, {b0, b1, b2, b3};\n"
+      "}"
+      : "=r"(w)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return w;
 }
 
 // E4M3 (e4m3fn) encode of a non-negative float, round to nearest even,
@@ -55,12 +63,11 @@ __device__ __forceinline__ uint32_t quantize_block16(const float (&x)[16], float
   const float s = __fmul_rn(__fdiv_rn(amax, 6.0f), gs);
   const uint32_t sf = e4m3_encode_satfinite(s);
   const float r = (sf == 0u) ? 0.0f : __fdiv_rn(gs, e4m3_decode(sf));
-  lo = 0u;
-  hi = 0u;
+  float v[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) lo |= e2m1_encode(__fmul_rn(x[i], r)) << (4 * i);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) hi |= e2m1_encode(__fmul_rn(x[8 + i], r)) << (4 * i);
+  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(x[i], r);
+  lo = e2m1_pack8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+  hi = e2m1_pack8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
   return sf;
 }
 
@@ -68,6 +75,12 @@ __device__ __forceinline__ uint32_t quantize_block16(const float (&x)[16], float
 // layout with cp4 = padded scale columns / 4.
 __host__ __device__ __forceinline__ int64_t sf_swizzled_offset(int64_t r, int64_t j, int64_t cp4) {
   return (((r >> 7) * cp4 + (j >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (j & 3);
+}
+
+// silu(g) * u with the fast exponential and division (relative error about
+// 1e-6; h feeds a quantizer whose steps are ~1e-1 apart).
+__device__ __forceinline__ float silu_mul_fast(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // silu(g) * u in fp32 with an IEEE division.

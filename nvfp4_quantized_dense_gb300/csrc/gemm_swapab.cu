@@ -4,15 +4,19 @@
 // roofline, so the kernel is a deep TMA pipeline (6-8 stages of 16 KB weight
 // tiles per SM) feeding one MMA issuer.
 //
-// Work is split into units = (128-row weight tile, K range).  When a tile's K
-// is split over several units, each unit writes its fp32 partial tile to the
-// caller's workspace and bumps the tile's arrival counter; the unit that
-// arrives last sums the partials in split order (so the result does not
-// depend on which CTA finishes last), resets the counter to 0 and runs the
-// epilogue.  The workspace must be zero-filled once before its first use; the
-// kernel leaves its counters at zero after every complete call.
+// Work split: the (128-row weight tile, 256-wide k-block) pairs are laid out
+// tile-major and cut into one contiguous, equal run per CTA, so every SM
+// streams the same number of weight bytes.  A CTA's run crosses tile
+// boundaries; each piece of a tile it covers is a fragment.  A tile covered by
+// one CTA is finished in place.  Otherwise each fragment writes its fp32
+// partial tile to the caller's workspace and bumps the tile's arrival
+// counter; the fragment that arrives last sums the partials in K order (so
+// the result does not depend on which CTA finishes last), resets the counter
+// to 0 and runs the epilogue.  The workspace must be zero-filled once before
+// its first use; the kernel leaves its counters at zero after every complete
+// call.
 //
-// Roles per CTA (192 threads, persistent over units): warp 0 TMA producer,
+// Roles per CTA (192 threads, one CTA per SM): warp 0 TMA producer,
 // warp 1 TMEM owner + MMA issuer (double-buffered accumulators), warps 2..5
 // epilogue (TMEM lane = weight row).  Bounded waits as in gemm_tc.cu.
 #include "common.cuh"
@@ -54,15 +58,52 @@ struct SwapArgs {
   uint16_t *d;          // bf16 [M, N]
   uint8_t *out_fp4;     // fused: [M, N/4]
   uint8_t *out_sf;      // fused: swizzled over M rows, N/32 columns
-  float *partials;      // [units][NT][128] fp32 when splits > 1
-  int *counters;        // [tiles] arrival counters when splits > 1
+  float *partials;      // [grid][maxfrag][NT][128] fp32 (tiles shared by CTAs)
+  int *counters;        // [tiles] arrival counters
   int32_t m, n, k;
-  int32_t tiles, splits, kbps, kb_total;
+  int32_t tiles, kb_total;   // weight tiles, k-blocks per tile
+  int32_t grid, maxfrag;     // CTAs, fragment slots per CTA
+  int32_t split_ok;          // 0: no workspace, every CTA owns whole tiles
   uint32_t wait_limit;
   int *status;
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Contiguous partition of W = tiles * kb_total k-blocks over `grid` CTAs:
+// CTA j owns [start(j), start(j+1)), start(j) = floor(j * W / grid).  Without
+// a workspace the cut points are rounded to whole tiles instead.
+struct Partition {
+  int64_t w, grid, kbt;
+  bool whole_tiles;
+  int64_t tiles;
+  __device__ __forceinline__ int64_t start(int64_t j) const {
+    if (whole_tiles) return (j * tiles / grid) * kbt;
+    return j * w / grid;
+  }
+  // CTA owning global k-block x (inverse of start)
+  __device__ __forceinline__ int64_t cta_of(int64_t x) const {
+    if (whole_tiles) {
+      const int64_t t = x / kbt;
+      return ((t + 1) * grid - 1) / tiles;
+    }
+    return ((x + 1) * grid - 1) / w;
+  }
+};
+
+// Iterates the fragments of one CTA: tile, [kb0, kb1) within the tile.
+struct FragIter {
+  int64_t x, end, kbt;
+  __device__ __forceinline__ bool next(int &tile, int &kb0, int &kb1) {
+    if (x >= end) return false;
+    tile = (int)(x / kbt);
+    kb0 = (int)(x - (int64_t)tile * kbt);
+    const int64_t room = end - x;
+    kb1 = (int)min((int64_t)kbt, kb0 + room);
+    x += kb1 - kb0;
+    return true;
+  }
+};
 
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -111,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  const int units = p.tiles * p.splits;
+  const Partition part{(int64_t)p.tiles * p.kb_total, p.grid, p.kb_total, p.split_ok == 0, p.tiles};
+  const int64_t my_start = part.start(blockIdx.x), my_end = part.start(blockIdx.x + 1);
   const int ksteps_total = p.k >> 6;
   const int cp4 = ksteps_total;          // 512-byte scale tiles per 128-row block
   const uint32_t limit = p.wait_limit;
@@ -124,9 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = ptx::l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0;
-      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
-        const int tile = u / p.splits, sp = u % p.splits;
-        const int kb0 = sp * p.kbps, kb1 = min(kb0 + p.kbps, p.kb_total);
+      FragIter fi{my_start, my_end, p.kb_total};
+      int tile, kb0, kb1;
+      while (!*abort_flag && fi.next(tile, kb0, kb1)) {
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
             *abort_flag = 1;
@@ -153,7 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
-      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x, ++it) {
+      FragIter fi{my_start, my_end, p.kb_total};
+      int tile, kb0, kb1;
+      for (; !*abort_flag && fi.next(tile, kb0, kb1); ++it) {
         const int ab = it & 1;
         if (!ptx::mbar_wait_bounded(&tempty[ab], (uint32_t)((it >> 1) & 1) ^ 1u, limit, kTimeoutNs, abort_flag)) {
           *abort_flag = 1;
@@ -161,8 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const int sp = u % p.splits;
-        const int kb0 = sp * p.kbps, kb1 = min(kb0 + p.kbps, p.kb_total);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(&full[s], ph, limit, kTimeoutNs, abort_flag)) {
@@ -200,7 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float alpha = __ldg(p.alpha);
     const int mt = min(p.m, NT);
     int it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+    FragIter fi{my_start, my_end, p.kb_total};
+    int tile, kb0, kb1;
+    for (; fi.next(tile, kb0, kb1); ++it) {
       const int ab = it & 1;
       if (!ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag)) {
         *abort_flag = 1;
@@ -220,25 +264,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tempty[ab]);              // accumulator buffer free again
 
-      const int tile = u / p.splits;
-      if (p.splits > 1) {
-        float *part = p.partials + (size_t)u * NT * 128;
+      // CTAs sharing this tile: the owners of its first and last k-block
+      const int64_t c_first = part.cta_of((int64_t)tile * p.kb_total);
+      const int64_t c_last = part.cta_of((int64_t)tile * p.kb_total + p.kb_total - 1);
+      if (c_last > c_first) {
+        auto slot = [&](int64_t c) {
+          return p.partials + ((size_t)c * p.maxfrag + (size_t)(tile - part.start(c) / p.kb_total)) * NT * 128;
+        };
+        float *mine = slot(blockIdx.x);
 #pragma unroll
         for (int t = 0; t < NT; ++t)
-          if (t < mt) part[t * 128 + r] = v[t];
-        __threadfence();
-        epi_bar();
-        if (et == 0) *last_flag = (atomicAdd(&p.counters[tile], 1) == p.splits - 1);
+          if (t < mt) mine[t * 128 + r] = v[t];
+        epi_bar();                    // every partial write of the CTA precedes the release below
+        if (et == 0) {
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          const int old = atomicAdd(&p.counters[tile], 1);
+          const int last = old == (int)(c_last - c_first);
+          if (last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          *last_flag = last;
+        }
         epi_bar();
         if (!*last_flag) continue;
-        __threadfence();
-        const float *tp = p.partials + (size_t)tile * p.splits * NT * 128;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          float acc = 0.0f;
-          if (t < mt)
-            for (int s2 = 0; s2 < p.splits; ++s2) acc += __ldcg(tp + ((size_t)s2 * NT + t) * 128 + r);
-          v[t] = acc;
+        for (int t = 0; t < NT; ++t) v[t] = 0.0f;
+        for (int64_t c = c_first; c <= c_last; ++c) {      // K order
+          const float *pc = slot(c);
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            if (t < mt) v[t] += __ldcg(pc + t * 128 + r);
         }
         if (et == 0) p.counters[tile] = 0;
       }
@@ -266,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float h[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            h[i] = silu_mul(s_out[(64 + 16 * qb + i) * C::PITCH + t], s_out[(16 * qb + i) * C::PITCH + t]);
+            h[i] = silu_mul_fast(s_out[(64 + 16 * qb + i) * C::PITCH + t], s_out[(16 * qb + i) * C::PITCH + t]);
           uint32_t lo, hi;
           const uint32_t sf = quantize_block16(h, gs, lo, hi);
           const int f = 64 * tile + 16 * qb;
@@ -304,34 +357,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct Plan {
-  int nt, tiles, splits, kbps, kb_total;
+  int nt, tiles, kb_total, grid, maxfrag;
   size_t ws_bytes;
 };
 
-// Choose the K split so that units spread evenly over the SMs: minimise
-// (units per SM, rounded up) x (k-blocks per unit + per-unit overhead).
+size_t counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) / 256 * 256; }
+
 Plan make_plan(int64_t m, int64_t n, int64_t k) {
   Plan pl{};
   pl.nt = m <= 16 ? 16 : m <= 32 ? 32 : 64;
   pl.tiles = (int)((n + 127) / 128);
   pl.kb_total = (int)((k + BK - 1) / BK);
-  const int sms = num_sms();
-  double best = 1e30;
-  for (int kbps = pl.kb_total; kbps >= 1; --kbps) {
-    const int splits = (pl.kb_total + kbps - 1) / kbps;
-    if (splits > 64) break;
-    const int units = pl.tiles * splits;
-    const int waves = (units + sms - 1) / sms;
-    const double cost = waves * (kbps + 0.5);
-    if (cost < best - 1e-9) {
-      best = cost;
-      pl.kbps = kbps;
-      pl.splits = splits;
-    }
-  }
-  pl.ws_bytes = pl.splits > 1 ? ((size_t)pl.tiles * 4 + 255) / 256 * 256 +
-                                    (size_t)pl.tiles * pl.splits * pl.nt * 128 * 4
-                              : 0;
+  const int64_t w = (int64_t)pl.tiles * pl.kb_total;
+  pl.grid = (int)(w < num_sms() ? w : num_sms());
+  const int64_t per = (w + pl.grid - 1) / pl.grid;           // k-blocks per CTA, rounded up
+  pl.maxfrag = (int)((per + pl.kb_total - 1) / pl.kb_total + 1);
+  const bool shared_tiles = (w % pl.grid != 0) || ((w / pl.grid) % pl.kb_total != 0);
+  pl.ws_bytes = shared_tiles ? counter_bytes(pl.tiles) + (size_t)pl.grid * pl.maxfrag * pl.nt * 128 * 4 : 0;
   return pl;
 }
 
@@ -359,23 +401,24 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   a.d = d;
   a.out_fp4 = out_fp4;
   a.out_sf = out_sf;
-  if (pl.splits > 1) {
+  const bool split = pl.ws_bytes > 0 && ws != nullptr;
+  if (split) {
     a.counters = static_cast<int *>(ws);
-    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((size_t)pl.tiles * 4 + 255) / 256 * 256);
+    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + counter_bytes(pl.tiles));
   }
   a.m = (int32_t)m;
   a.n = (int32_t)n;
   a.k = (int32_t)k;
   a.tiles = pl.tiles;
-  a.splits = pl.splits;
-  a.kbps = pl.kbps;
   a.kb_total = pl.kb_total;
+  a.maxfrag = pl.maxfrag;
+  a.split_ok = split ? 1 : 0;
+  // without a workspace each CTA owns whole tiles (at most one CTA per tile)
+  a.grid = split ? pl.grid : (pl.tiles < num_sms() ? pl.tiles : num_sms());
   a.wait_limit = wait_limit;
   a.status = device_status_ptr();
   if (!a.status) return cudaErrorInvalidValue;
-  const int units = pl.tiles * pl.splits;
-  const int grid = units < num_sms() ? units : num_sms();
-  swapab_kernel<MODE, NT><<<grid, kThreads, C::SMEM_BYTES, st>>>(tm_w, tm_x, a);
+  swapab_kernel<MODE, NT><<<a.grid, kThreads, C::SMEM_BYTES, st>>>(tm_w, tm_x, a);
   return cudaGetLastError();
 }
 
@@ -417,11 +460,10 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
                           void *workspace, size_t ws_bytes, uint32_t wait_limit, cudaStream_t st) {
   if (!swapab_supported(mode, m, n, k)) return cudaErrorNotSupported;
   Plan pl = make_plan(m, n, k);
-  if (pl.splits > 1 && (workspace == nullptr || ws_bytes < pl.ws_bytes)) {
-    // not enough scratch for the balanced split: one unit per weight tile
-    pl.splits = 1;
-    pl.kbps = pl.kb_total;
+  if (pl.ws_bytes > 0 && (workspace == nullptr || ws_bytes < pl.ws_bytes)) {
+    // not enough scratch to share tiles between CTAs: whole tiles per CTA
     pl.ws_bytes = 0;
+    workspace = nullptr;
   }
   const uint8_t *x = static_cast<const uint8_t *>(a);
   if (mode == TC_W4A4)

@@ -8,8 +8,9 @@
 //   warp 1      allocates TMEM; one elected thread copies each stage's
 //               scales into TMEM (tcgen05.cp) and issues the MMAs, then
 //               commits the stage back to the producer;
-//   warps 2..5  epilogue: TMEM -> registers (tcgen05.ld) -> bf16 output, or
-//               the fused SwiGLU + NVFP4 requantize of the gate_up GEMM.
+//   warps 2..9  epilogue: TMEM -> registers (tcgen05.ld), TMEM released at
+//               once, then bf16 output or the fused SwiGLU + NVFP4 requantize
+//               of the gate_up GEMM while the next tile's MMAs run.
 // Tile 128 (M) x 256 (N) x 256 (K); one MMA instruction covers K = 64, so a
 // stage holds four.  Every mbarrier wait is bounded: a wait that gives up
 // records NVFP4_ERR_DEVICE_TIMEOUT, every role leaves its loop, outstanding
@@ -58,7 +59,7 @@ constexpr uint32_t SFA_BYTES = (BM / 128) * KSTEPS * 512;
 constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;           // producer, MMA, 8 epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0, SFA_COL = 256, SFB_COL = 256 + 4 * KSTEPS;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&sm.empty()[s], 1);
     }
     ptx::mbar_init(sm.tfull(), 1);
-    ptx::mbar_init(sm.tempty(), 128);
+    ptx::mbar_init(sm.tempty(), 256);
     ptx::mbar_init(sm.drain(), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -230,9 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    // Eight warps: warp w reads TMEM lane quarter w % 4 (the hardware lets a
+    // warp reach only its own quarter) and column half (w - 2) / 4, i.e. 128
+    // accumulator columns of its 32 rows.  It holds them in registers and
+    // releases TMEM before any math or store, so the MMAs of the next tile run
+    // while this tile's epilogue finishes.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
-    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t t_base = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL + 128 * half;
     const float alpha = __ldg(p.alpha);
     int it = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
@@ -241,60 +248,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
+      uint32_t acc[128];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ptx::tmem_ld16(t_base + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&acc[16 * c]));
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sm.tempty());            // accumulator free for the next tile
+
       const int mt = tile % p.num_m, nt = tile / p.num_m;
       const int m = mt * BM + row;
       if constexpr (MODE == TC_W4A4) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          uint32_t r[16];
-          ptx::tmem_ld16(t_row + ACC_COL + c * 16, r);
-          ptx::tmem_wait_ld();
-          const int n = nt * BN + c * 16;
-          if (m < p.m && n < p.n) {
-            uint32_t o[8];
+        const int n0 = nt * BN + 128 * half;
+        if (m < p.m) {
+          uint16_t *drow = p.d + (size_t)m * p.n;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = pack_bf16x2(alpha * __uint_as_float(r[2 * i]), alpha * __uint_as_float(r[2 * i + 1]));
-            uint4 *dst = reinterpret_cast<uint4 *>(p.d + (size_t)m * p.n + n);
-            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          for (int c = 0; c < 16; ++c) {
+            const int n = n0 + 8 * c;
+            if (n < p.n) {
+              uint4 o;
+              o.x = pack_bf16x2(alpha * __uint_as_float(acc[8 * c + 0]), alpha * __uint_as_float(acc[8 * c + 1]));
+              o.y = pack_bf16x2(alpha * __uint_as_float(acc[8 * c + 2]), alpha * __uint_as_float(acc[8 * c + 3]));
+              o.z = pack_bf16x2(alpha * __uint_as_float(acc[8 * c + 4]), alpha * __uint_as_float(acc[8 * c + 5]));
+              o.w = pack_bf16x2(alpha * __uint_as_float(acc[8 * c + 6]), alpha * __uint_as_float(acc[8 * c + 7]));
+              *reinterpret_cast<uint4 *>(drow + n) = o;
+            }
           }
         }
       } else {
-        // accumulator columns: [up 64 | gate 64] for features nt*128 + 64g + (0..63), g = 0, 1
-        const float gs = __ldg(p.out_gs);
+        // this half's columns: [up 64 | gate 64] for features nt*128 + 64*half + (0..63)
         const int inter = p.n >> 1;
-        const int ocp4 = ((inter >> 4) + 3) >> 2;
-#pragma unroll 1
-        for (int g = 0; g < 2; ++g) {
-          const int f0 = nt * 128 + 64 * g;
-          if (f0 >= inter) break;
+        const int f0 = nt * 128 + 64 * half;
+        if (f0 < inter) {
+          const float gs = __ldg(p.out_gs);
+          const int ocp4 = ((inter >> 4) + 3) >> 2;
           uint32_t sfw = 0;
-#pragma unroll 1
-          for (int qb = 0; qb < 4; ++qb) {
-            uint32_t up[16], gt[16];
-            ptx::tmem_ld16(t_row + ACC_COL + 128 * g + 16 * qb, up);
-            ptx::tmem_ld16(t_row + ACC_COL + 128 * g + 64 + 16 * qb, gt);
-            ptx::tmem_wait_ld();
-            if (m < p.m) {
-              float h[16];
+          if (m < p.m) {
+            uint32_t codes[8];
+#pragma unroll
+            for (int qb = 0; qb < 4; ++qb) {
+              float hv[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                h[i] = silu_mul(alpha * __uint_as_float(gt[i]), alpha * __uint_as_float(up[i]));
-              uint32_t lo, hi;
-              const uint32_t sf = quantize_block16(h, gs, lo, hi);
-              *reinterpret_cast<uint2 *>(p.out_fp4 + (size_t)m * (inter >> 1) + (f0 + 16 * qb) / 2) =
-                  make_uint2(lo, hi);
-              sfw |= sf << (8 * qb);
+                hv[i] = silu_mul_fast(alpha * __uint_as_float(acc[64 + 16 * qb + i]),
+                                      alpha * __uint_as_float(acc[16 * qb + i]));
+              sfw |= quantize_block16(hv, gs, codes[2 * qb], codes[2 * qb + 1]) << (8 * qb);
             }
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out_fp4 + (size_t)m * (inter >> 1) + f0 / 2);
+            dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
           }
-          // 4 consecutive scale columns (f0/16 .. +3) of this row in one word; rows
-          // past M (the 128-row padding) get zeros
+          // scale columns f0/16 .. +3 of this row in one word; padding rows past M get 0
           *reinterpret_cast<uint32_t *>(p.out_sf + sf_swizzled_offset(m, f0 >> 4, ocp4)) = sfw;
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(sm.tempty());
     }
   }
 

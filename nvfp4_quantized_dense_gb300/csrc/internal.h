@@ -56,4 +56,10 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
                           int64_t k, void *workspace, size_t ws_bytes, uint32_t wait_limit,
                           cudaStream_t st);
 
+// W4A16 on the tensor cores (weights dequantized to bf16 in shared memory).
+bool w4a16_tc_supported(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_w4a16_tc(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, const float *alpha,
+                            uint16_t *d, int64_t m, int64_t n, int64_t k, uint32_t wait_limit,
+                            cudaStream_t st);
+
 }  // namespace nvfp4

@@ -251,8 +251,14 @@ def test_auto_dispatch_matches_forced_paths(lib):
 
 
 # ------------------------------------------------------------------- W4A16
-@pytest.mark.parametrize("algo", [GEMV])
-@pytest.mark.parametrize("m,n,k", [(1, 256, 512), (16, 1024, 256), (5, 96, 320), (33, 128, 128)])
+W4A16_GEMV = [(1, 256, 512), (16, 1024, 256), (5, 96, 320), (33, 128, 128)]
+# tensor cores: token tiles of 16/32/64/128/256, ragged tokens, N and K tails
+W4A16_TC = [(1, 256, 512), (16, 1024, 256), (5, 96, 320), (33, 128, 128), (64, 384, 1024),
+            (100, 256, 640), (128, 512, 2048), (300, 1024, 512), (1024, 2048, 1024)]
+
+
+@pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in W4A16_GEMV] +
+                         [(m, n, k, TC) for m, n, k in W4A16_TC])
 def test_w4a16_small_shapes(lib, m, n, k, algo):
     ws = small_weights(n, k, 8)
     xbits, x = synth.activations(4, m, k)
@@ -264,19 +270,20 @@ def test_w4a16_small_shapes(lib, m, n, k, algo):
 
 
 @pytest.mark.parametrize("which", ["gate_up", "down"])
-@pytest.mark.parametrize("m", [1, 16])
-def test_w4a16_full_size_sampled(lib, m, which):
+@pytest.mark.parametrize("m,algo", [(1, GEMV), (16, GEMV), (1, TC), (16, TC), (128, TC), (1024, TC)])
+def test_w4a16_full_size_sampled(lib, m, which, algo):
     ws = weights(4, which)
     if which == "gate_up":
         xbits, x = synth.activations(4, m)
     else:
         xbits, x = synth.to_bf16_bits(synth.random_matrix((m, ws.k), (23, m), scale=0.1))
     alpha = np.float32(1.0) / ws.gs
-    got = run_w4a16(lib, xbits, ws.device_prepared(lib), alpha, m, ws.n, ws.k, 0)
+    got = run_w4a16(lib, xbits, ws.device_prepared(lib), alpha, m, ws.n, ws.k, algo)
     cols = sample_rows(ws.n, 512, seed=m + 3)
-    ref = oracle.gemm_w4a16(x, ws.packed[cols], ws.sf[cols], alpha)
-    err = assert_gemm_close(got[:, cols], ref)
-    print(f"w4a16 {which} m={m}: rel err {err:.2e}")
+    toks = sample_rows(m, 128, seed=m + 4)
+    ref = oracle.gemm_w4a16(x[toks], ws.packed[cols], ws.sf[cols], alpha)
+    err = assert_gemm_close(got[np.ix_(toks, cols)], ref)
+    print(f"w4a16 {which} m={m} algo={algo}: rel err {err:.2e}")
 
 
 # ------------------------------------------------------------- whole chains
