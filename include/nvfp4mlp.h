@@ -31,6 +31,12 @@
  *    DEVICE buffers, so a call sequence can be captured in a CUDA graph.
  *  - Calls are asynchronous and ordered on `stream` (NULL = legacy default
  *    stream); they do not synchronize, except nvfp4_get_device_status.
+ *  - Kernels are launched with programmatic dependent launch ([P2]
+ *    deepseek_v2.py excerpt passes enable_pdl=True to both fused-path kernels):
+ *    a kernel may start while the previous kernel on the stream is finishing
+ *    and stream its weights meanwhile, but it reads the previous kernel's
+ *    results and writes any global memory only after that kernel completed,
+ *    so stream order semantics are unchanged.
  *  - Pointers must be 16-byte aligned.  Outputs must not alias inputs.
  *  - Validation happens on the host before any launch; a call that returns
  *    anything but NVFP4_OK launched nothing and wrote nothing.
@@ -134,6 +140,25 @@ nvfp4_status nvfp4_quantize(const uint16_t *x, int64_t m, int64_t k, const float
 nvfp4_status silu_mul_nvfp4_quantize(const uint16_t *gate_up, int64_t m, int64_t i,
                                      const float *global_scale, uint8_t *out_fp4, uint8_t *out_sf,
                                      nvfp4_stream_t stream);
+
+/* Masked multi-group form of silu_mul_nvfp4_quantize: the call the pages
+ * make ([P1] qwen2_moe.py excerpt: silu_and_mul_scaled_nvfp4_experts_quantize
+ * (gate_up[G, M, 2I], masked_m, scale), whose scale comes back as a 6-D
+ * expert-grouped tensor that is permuted to the dense swizzled layout).
+ *   gate_up      bf16 [g, m_max, 2*i]: per row [gate | up]
+ *   masked_m     int32 [g] DEVICE: valid rows of each group (clamped to
+ *                [0, m_max]); rows past it are not computed
+ *   global_scale fp32 [1]: one global scale for every group
+ *   out_fp4      uint8 [g, m_max, i/2]; invalid rows are left untouched
+ *   out_sf       g consecutive blocks of nvfp4_sf_bytes(m_max, i, SWIZZLED)
+ *                bytes: group e's scales in the dense swizzled layout over its
+ *                m_max rows (the pages' permuted view, expert by expert);
+ *                invalid and padding rows get 0x00.
+ * Per valid row the arithmetic is exactly silu_mul_nvfp4_quantize.
+ * Requires i % 16 == 0, g <= 65535. */
+nvfp4_status silu_mul_nvfp4_quantize_masked(const uint16_t *gate_up, const int32_t *masked_m, int64_t g,
+                                            int64_t m_max, int64_t i, const float *global_scale,
+                                            uint8_t *out_fp4, uint8_t *out_sf, nvfp4_stream_t stream);
 
 /* Unfused activation of the W4A16 chain: out = bf16(silu(gate) * up).
  *   gate_up bf16 [m, 2*i] ([gate | up]);  out bf16 [m, i].  Requires i % 8 == 0. */

@@ -30,6 +30,7 @@ _P, _I64, _SZ, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_i
 _SIGS = {
     "nvfp4_quantize": [_P, _I64, _I64, _P, _P, _P, _I, _P],
     "silu_mul_nvfp4_quantize": [_P, _I64, _I64, _P, _P, _P, _P],
+    "silu_mul_nvfp4_quantize_masked": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "silu_mul_bf16": [_P, _I64, _I64, _P, _P],
     "nvfp4_gemm": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
     "nvfp4_gemm_ex": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
@@ -114,6 +115,12 @@ def nvfp4_quantize(x, m, k, global_scale, out_fp4, out_sf, sf_layout=SF_SWIZZLED
 def silu_mul_nvfp4_quantize(gate_up, m, i, global_scale, out_fp4, out_sf, stream=None):
     _call("silu_mul_nvfp4_quantize", _ptr(gate_up), m, i, _ptr(global_scale), _ptr(out_fp4),
           _ptr(out_sf), _stream(stream))
+
+
+def silu_mul_nvfp4_quantize_masked(gate_up, masked_m, g, m_max, i, global_scale, out_fp4, out_sf,
+                                   stream=None):
+    _call("silu_mul_nvfp4_quantize_masked", _ptr(gate_up), _ptr(masked_m), g, m_max, i, _ptr(global_scale),
+          _ptr(out_fp4), _ptr(out_sf), _stream(stream))
 
 
 def silu_mul_bf16(gate_up, m, i, out, stream=None):

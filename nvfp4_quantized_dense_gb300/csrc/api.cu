@@ -111,6 +111,19 @@ nvfp4_status silu_mul_nvfp4_quantize(const uint16_t *gate_up, int64_t m, int64_t
                                             (cudaStream_t)stream));
 }
 
+nvfp4_status silu_mul_nvfp4_quantize_masked(const uint16_t *gate_up, const int32_t *masked_m, int64_t g,
+                                            int64_t m_max, int64_t i, const float *global_scale,
+                                            uint8_t *out_fp4, uint8_t *out_sf, nvfp4_stream_t stream) {
+  if (!gate_up || !masked_m || !global_scale || !out_fp4 || !out_sf || g < 0 || m_max < 0 || i <= 0)
+    return NVFP4_ERR_INVALID_ARG;
+  if (i % 16 != 0 || !aligned16(gate_up) || !aligned16(out_fp4) || g > 65535)
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  if (g == 0 || m_max == 0) return NVFP4_OK;
+  return from_cuda(launch_silu_mul_quantize_masked(gate_up, masked_m, g, m_max, i, global_scale, out_fp4,
+                                                   out_sf, (cudaStream_t)stream));
+}
+
 nvfp4_status silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
                            nvfp4_stream_t stream) {
   if (!gate_up || !out || m < 0 || i <= 0) return NVFP4_ERR_INVALID_ARG;

@@ -11,6 +11,16 @@
 namespace nvfp4 {
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel here is launched so that it may
+// start while the previous kernel on the stream is still finishing:
+// pdl_trigger() lets the next kernel's CTAs launch, pdl_wait() blocks until
+// the previous kernel has completed and its memory is visible.  A kernel
+// reads the previous kernel's results, and writes any global memory, only
+// after pdl_wait(); without the launch attribute pdl_wait() returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // E2M1 encode of eight floats into one word (element i in nibble i), with the
 // PTX conversion cvt.rn.satfinite.e2m1x2.f32: round to nearest even, magnitudes
 // past 6 saturate to 6, the sign bit is kept (a negative value that rounds to

@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto st_sfx = [&](int s) { return st_sfw(s) + SFW_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -168,8 +169,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       FragIter fi{my_start, my_end, p.kb_total};
       int tile, kb0, kb1;
+      // The first STAGES stages get their weight tiles before the previous
+      // kernel on the stream has finished; their activation tiles (that
+      // kernel's output) follow once it has.
+      int pend_s[STAGES], pend_kb[STAGES];
+      int npend = 0, c = 0;
+      bool flushed = false;
+      auto issue_x = [&](int st, int kb) {
+        const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
+        ptx::tma_load_2d(st_x(st), &tm_x, &full[st], kb * (BK / 2), 0, pol_x);
+        ptx::bulk_load(st_sfx(st), p.sfx + (size_t)kb * KSTEPS * 512, nk * 512u, &full[st], pol_x);
+      };
+      auto flush = [&]() {
+        pdl_wait();
+        for (int i = 0; i < npend; ++i) issue_x(pend_s[i], pend_kb[i]);
+        flushed = true;
+      };
       while (!*abort_flag && fi.next(tile, kb0, kb1)) {
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb, ++c) {
+          if (c == STAGES && !flushed) flush();
           if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
             *abort_flag = 1;
             atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
@@ -178,17 +196,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
           ptx::mbar_arrive_expect_tx(&full[s], W_BYTES + C::X_BYTES + 2u * (uint32_t)nk * 512u);
           ptx::tma_load_2d(st_w(s), &tm_w, &full[s], kb * (BK / 2), tile * 128, pol_w);
-          ptx::tma_load_2d(st_x(s), &tm_x, &full[s], kb * (BK / 2), 0, pol_x);
           ptx::bulk_load(st_sfw(s), p.sfw + ((size_t)tile * cp4 + kb * KSTEPS) * 512, nk * 512u, &full[s],
                          pol_w);
-          ptx::bulk_load(st_sfx(s), p.sfx + (size_t)kb * KSTEPS * 512, nk * 512u, &full[s], pol_x);
+          if (c < STAGES) {
+            pend_s[npend] = s;
+            pend_kb[npend] = kb;
+            ++npend;
+          } else {
+            issue_x(s, kb);
+          }
           issued_mask |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
+      if (!flushed) flush();
     }
   } else if (warp == 1) {
+    pdl_wait();
     if (ptx::elect_one()) {
       // kind::mxf4nvf4, E2M1 x E2M1, UE4M3 scales, M = 128 (weights), N = NT (tokens)
       constexpr uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) | (8u << 24);
@@ -235,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;                 // weight row within the tile
     const int et = threadIdx.x - 64;             // 0..127 across the epilogue warps
@@ -418,8 +444,7 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   a.wait_limit = wait_limit;
   a.status = device_status_ptr();
   if (!a.status) return cudaErrorInvalidValue;
-  swapab_kernel<MODE, NT><<<a.grid, kThreads, C::SMEM_BYTES, st>>>(tm_w, tm_x, a);
-  return cudaGetLastError();
+  return launch_pdl(swapab_kernel<MODE, NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_w, tm_x, a);
 }
 
 template <int MODE>

@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem sm{reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int *abort_flag = sm.abort_flag();
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -159,9 +160,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_b = ptx::l2_policy_evict_first();
       int s = 0;
       uint32_t ph = 0;
+      // The first STAGES stages get their weight (B) tiles before the previous
+      // kernel on the stream has finished; their activation (A) tiles follow
+      // once it has.
+      int pend_s[STAGES], pend_kb[STAGES], pend_mt[STAGES];
+      int npend = 0, c = 0;
+      bool flushed = false;
+      auto issue_a = [&](int st, int mt, int kb) {
+        const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
+        ptx::tma_load_2d(sm.a(st), &tm_a, &sm.full()[st], kb * (BK / 2), mt * BM, pol_a);
+        ptx::bulk_load(sm.sfa(st), p.sfa + ((size_t)mt * cp4a + kb * KSTEPS) * 512, nk * 512u, &sm.full()[st],
+                       pol_a);
+      };
+      auto flush = [&]() {
+        pdl_wait();
+        for (int i = 0; i < npend; ++i) issue_a(pend_s[i], pend_mt[i], pend_kb[i]);
+        flushed = true;
+      };
       for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
         const int mt = tile % p.num_m, nt = tile / p.num_m;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < num_kb; ++kb, ++c) {
+          if (c == STAGES && !flushed) flush();
           if (!ptx::mbar_wait_bounded(&sm.empty()[s], ph ^ 1u, limit, kDefaultTimeoutNs, abort_flag)) {
             give_up(abort_flag, p.status);
             break;
@@ -170,21 +189,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nbv = min(2, nrb_b - nt * 2);
           const uint32_t bytes = A_BYTES + B_BYTES + (uint32_t)nk * 512u * (1u + (uint32_t)nbv);
           ptx::mbar_arrive_expect_tx(&sm.full()[s], bytes);
-          ptx::tma_load_2d(sm.a(s), &tm_a, &sm.full()[s], kb * (BK / 2), mt * BM, pol_a);
           ptx::tma_load_2d(sm.b(s), &tm_b, &sm.full()[s], kb * (BK / 2), nt * BN, pol_b);
-          ptx::bulk_load(sm.sfa(s), p.sfa + ((size_t)mt * cp4a + kb * KSTEPS) * 512, nk * 512u,
-                         &sm.full()[s], pol_a);
           for (int rb = 0; rb < nbv; ++rb)
             ptx::bulk_load(sm.sfb(s) + rb * (KSTEPS * 512),
                            p.sfb + ((size_t)(nt * 2 + rb) * cp4b + kb * KSTEPS) * 512, nk * 512u,
                            &sm.full()[s], pol_b);
+          if (c < STAGES) {
+            pend_s[npend] = s;
+            pend_kb[npend] = kb;
+            pend_mt[npend] = mt;
+            ++npend;
+          } else {
+            issue_a(s, mt, kb);
+          }
           issued_mask |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
+      if (!flushed) flush();
     }
   } else if (warp == 1) {
+    pdl_wait();
     if (ptx::elect_one()) {
       constexpr uint32_t idesc = idesc_nvfp4(BM, BN);
       int s = 0;
@@ -236,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // accumulator columns of its 32 rows.  It holds them in registers and
     // releases TMEM before any math or store, so the MMAs of the next tile run
     // while this tile's epilogue finishes.
+    pdl_wait();
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
@@ -395,8 +422,7 @@ cudaError_t launch_mode(const uint8_t *a, const uint8_t *a_sf, const uint8_t *b,
   if (!args.status) return cudaErrorInvalidValue;
   const int tiles = args.num_m * args.num_n;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  tc_gemm_kernel<MODE><<<grid, kThreads, SMEM_BYTES, st>>>(tm_a, tm_b, args);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<MODE>, dim3(grid), dim3(kThreads), SMEM_BYTES, st, tm_a, tm_b, args);
 }
 
 }  // namespace

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto st_ws = [&](int s) { return st_wc(s) + WC_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -159,24 +160,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = ptx::l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0;
+      // The first STAGES stages get their weight codes and scales before the
+      // previous kernel on the stream has finished; their activation tiles
+      // follow once it has.
+      int pend_s[STAGES], pend_kb[STAGES], pend_tt[STAGES];
+      int npend = 0, c = 0;
+      bool flushed = false;
+      auto flush = [&]() {
+        pdl_wait();
+        for (int i = 0; i < npend; ++i)
+          ptx::tma_load_2d(st_x(pend_s[i]), &tm_x, &full[pend_s[i]], pend_kb[i] * (BK * 2), pend_tt[i] * NT,
+                           pol_x);
+        flushed = true;
+      };
       for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
         const int wt = tile / p.ttiles, tt = tile % p.ttiles;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb, ++c) {
+          if (c == STAGES && !flushed) flush();
           if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
             give_up();
             break;
           }
           ptx::mbar_arrive_expect_tx(&full[s], C::X_BYTES + WC_BYTES + WS_BYTES);
-          ptx::tma_load_2d(st_x(s), &tm_x, &full[s], kb * (BK * 2), tt * NT, pol_x);
           ptx::tma_load_2d(st_wc(s), &tm_w, &full[s], kb * (BK / 2), wt * 128, pol_w);
           ptx::bulk_load(st_ws(s), p.wsf + ((size_t)wt * cp4 + kb) * 512, WS_BYTES, &full[s], pol_w);
+          if (c < STAGES) {
+            pend_s[npend] = s;
+            pend_kb[npend] = kb;
+            pend_tt[npend] = tt;
+            ++npend;
+          } else {
+            ptx::tma_load_2d(st_x(s), &tm_x, &full[s], kb * (BK * 2), tt * NT, pol_x);
+          }
           issued_mask |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
+      if (!flushed) flush();
     }
   } else if (warp == 1) {
+    pdl_wait();
     if (ptx::elect_one()) {
       // kind::f16: F32 accumulator (bits 4-5 = 1), A = B = BF16 (1), K-major,
       // N >> 3 in bits 17-22, M = 128 >> 4 in bits 24-28
@@ -215,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 6) {
     // ---------------------------------------------------------- converters
+    pdl_wait();
     const int r = threadIdx.x - 64;             // weight row of the tile, 0..127
     const int swz = r & 7;
     int s = 0;
@@ -247,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait();
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
@@ -335,8 +361,7 @@ cudaError_t launch_nt(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, c
   if (!a.status) return cudaErrorInvalidValue;
   const int tiles = a.wtiles * a.ttiles;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  w4a16_kernel<NT><<<grid, kThreads, C::SMEM_BYTES, st>>>(tm_x, tm_w, a);
-  return cudaGetLastError();
+  return launch_pdl(w4a16_kernel<NT>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, st, tm_x, tm_w, a);
 }
 
 }  // namespace

@@ -166,6 +166,8 @@ __device__ __forceinline__ void swiglu_epilogue(const GemvArgs &p, float (&acc)[
 
 template <int MT, int R, bool SWIGLU>
 __global__ void __launch_bounds__(kWarps * 32) gemv_w4a4_kernel(GemvArgs p) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t cta = blockIdx.x;
   const int64_t kb = p.k >> 1;                  // bytes per row
@@ -240,6 +242,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_w4a4_kernel(GemvArgs p) {
 
 template <int MT>
 __global__ void __launch_bounds__(kWarps * 32) gemv_w4a16_kernel(GemvArgs p) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
   const int64_t kb = p.k >> 1;
@@ -304,16 +308,13 @@ cudaError_t launch_mt(GemvMode mode, const GemvArgs &a, cudaStream_t st) {
   const dim3 block(kWarps * 32);
   switch (mode) {
     case GEMV_W4A4:
-      gemv_w4a4_kernel<MT, 2, false><<<(unsigned)(a.n / (kWarps * 2)), block, 0, st>>>(a);
-      break;
+      return launch_pdl(gemv_w4a4_kernel<MT, 2, false>, dim3((unsigned)(a.n / (kWarps * 2))), block, 0, st, a);
     case GEMV_W4A4_SWIGLU:
-      gemv_w4a4_kernel<MT, 4, true><<<(unsigned)(a.n / 32), block, 0, st>>>(a);
-      break;
+      return launch_pdl(gemv_w4a4_kernel<MT, 4, true>, dim3((unsigned)(a.n / 32)), block, 0, st, a);
     case GEMV_W4A16:
-      gemv_w4a16_kernel<MT><<<(unsigned)(a.n / kWarps), block, 0, st>>>(a);
-      break;
+      return launch_pdl(gemv_w4a16_kernel<MT>, dim3((unsigned)(a.n / kWarps)), block, 0, st, a);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace

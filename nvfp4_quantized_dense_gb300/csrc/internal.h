@@ -10,10 +10,30 @@
 
 namespace nvfp4 {
 
+// Launch with programmatic stream serialization (see pdl_wait in common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_quantize(const uint16_t *x, int64_t m, int64_t k, const float *gs,
                             uint8_t *out_fp4, uint8_t *out_sf, bool swizzled, cudaStream_t st);
 cudaError_t launch_silu_mul_quantize(const uint16_t *gate_up, int64_t m, int64_t i, const float *gs,
                                      uint8_t *out_fp4, uint8_t *out_sf, cudaStream_t st);
+cudaError_t launch_silu_mul_quantize_masked(const uint16_t *gate_up, const int32_t *masked_m, int64_t g,
+                                            int64_t m_max, int64_t i, const float *gs, uint8_t *out_fp4,
+                                            uint8_t *out_sf, cudaStream_t st);
 cudaError_t launch_silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
                                  cudaStream_t st);
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf_lin, int64_t n, int64_t k,

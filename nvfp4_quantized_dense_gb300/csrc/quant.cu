@@ -36,6 +36,8 @@ __device__ __forceinline__ void load16_bf16(const uint16_t *p, float (&x)[16]) {
 __global__ void __launch_bounds__(kTileThreads) quantize_kernel(
     const uint16_t *__restrict__ x, int64_t m, int64_t k, const float *__restrict__ gs_ptr,
     uint8_t *__restrict__ out_fp4, uint8_t *__restrict__ out_sf, bool swizzled) {
+  pdl_trigger();
+  pdl_wait();
   int64_t row, col;
   tile_coords(threadIdx.x, row, col);
   const int64_t cols = k >> 4;
@@ -58,16 +60,27 @@ __global__ void __launch_bounds__(kTileThreads) quantize_kernel(
 }
 
 // gate_up [m, 2i] bf16 ([gate | up]) -> h = silu(gate)*up (fp32) -> NVFP4
-// with swizzled scales.  Same tiling as quantize_kernel over h [m, i].
+// with swizzled scales.  Same tiling as quantize_kernel over h [m, i].  With
+// groups (blockIdx.z), group e's rows start at e * m rows of every tensor, its
+// scales at e * sf_group bytes, and only its first masked_m[e] rows are valid
+// (the rest get zero scales and untouched codes).
 __global__ void __launch_bounds__(kTileThreads) silu_mul_quantize_kernel(
     const uint16_t *__restrict__ gate_up, int64_t m, int64_t inter, const float *__restrict__ gs_ptr,
-    uint8_t *__restrict__ out_fp4, uint8_t *__restrict__ out_sf) {
+    uint8_t *__restrict__ out_fp4, uint8_t *__restrict__ out_sf, const int32_t *__restrict__ masked_m,
+    int64_t sf_group) {
+  pdl_trigger();
+  pdl_wait();
   int64_t row, col;
   tile_coords(threadIdx.x, row, col);
+  const int64_t e = blockIdx.z;
+  const int64_t rows_valid = masked_m ? min((int64_t)max(masked_m[e], 0), m) : m;
+  gate_up += e * m * 2 * inter;
+  out_fp4 += e * m * (inter >> 1);
+  out_sf += e * sf_group;
   const int64_t cols = inter >> 4;
   const int64_t cp4 = (cols + 3) >> 2;
   uint32_t sf = 0;
-  if (row < m && col < cols) {
+  if (row < rows_valid && col < cols) {
     const float gs = __ldg(gs_ptr);
     float g[16], u[16], h[16];
     load16_bf16(gate_up + row * 2 * inter + col * 16, g);
@@ -85,6 +98,8 @@ __global__ void __launch_bounds__(kTileThreads) silu_mul_quantize_kernel(
 __global__ void __launch_bounds__(256) silu_mul_bf16_kernel(const uint16_t *__restrict__ gate_up,
                                                             int64_t m, int64_t inter,
                                                             uint16_t *__restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t per_row = inter >> 3;
   const int64_t total = m * per_row;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -164,21 +179,29 @@ inline unsigned grid_for(int64_t work, int threads) {
 cudaError_t launch_quantize(const uint16_t *x, int64_t m, int64_t k, const float *gs,
                             uint8_t *out_fp4, uint8_t *out_sf, bool swizzled, cudaStream_t st) {
   const dim3 grid((unsigned)((k / 16 + 3) / 4), (unsigned)((m + 127) / 128));
-  quantize_kernel<<<grid, kTileThreads, 0, st>>>(x, m, k, gs, out_fp4, out_sf, swizzled);
-  return cudaGetLastError();
+  return launch_pdl(quantize_kernel, grid, dim3(kTileThreads), 0, st, x, m, k, gs, out_fp4, out_sf, swizzled);
 }
 
 cudaError_t launch_silu_mul_quantize(const uint16_t *gate_up, int64_t m, int64_t i, const float *gs,
                                      uint8_t *out_fp4, uint8_t *out_sf, cudaStream_t st) {
   const dim3 grid((unsigned)((i / 16 + 3) / 4), (unsigned)((m + 127) / 128));
-  silu_mul_quantize_kernel<<<grid, kTileThreads, 0, st>>>(gate_up, m, i, gs, out_fp4, out_sf);
-  return cudaGetLastError();
+  return launch_pdl(silu_mul_quantize_kernel, grid, dim3(kTileThreads), 0, st, gate_up, m, i, gs, out_fp4,
+                    out_sf, (const int32_t *)nullptr, (int64_t)0);
+}
+
+cudaError_t launch_silu_mul_quantize_masked(const uint16_t *gate_up, const int32_t *masked_m, int64_t g,
+                                            int64_t m_max, int64_t i, const float *gs, uint8_t *out_fp4,
+                                            uint8_t *out_sf, cudaStream_t st) {
+  const int64_t sf_group = ((m_max + 127) / 128 * 128) * ((i / 16 + 3) / 4 * 4);
+  const dim3 grid((unsigned)((i / 16 + 3) / 4), (unsigned)((m_max + 127) / 128), (unsigned)g);
+  return launch_pdl(silu_mul_quantize_kernel, grid, dim3(kTileThreads), 0, st, gate_up, m_max, i, gs, out_fp4,
+                    out_sf, masked_m, sf_group);
 }
 
 cudaError_t launch_silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
                                  cudaStream_t st) {
-  silu_mul_bf16_kernel<<<grid_for(m * (i / 8), 256), 256, 0, st>>>(gate_up, m, i, out);
-  return cudaGetLastError();
+  return launch_pdl(silu_mul_bf16_kernel, dim3(grid_for(m * (i / 8), 256)), dim3(256), 0, st, gate_up, m, i,
+                    out);
 }
 
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf_lin, int64_t n, int64_t k,

@@ -69,6 +69,19 @@ def silu_mul_quant(gate_up_bf16, gs_h, detail=False):
     return quantize_nvfp4(swiglu_h(gate_up_bf16), gs_h, detail=detail)
 
 
+def silu_mul_quant_masked(gate_up_groups, masked_m, gs_h):
+    """Masked multi-group form ([P1] "关键源码片段", qwen2_moe.py excerpt:
+    silu_and_mul_scaled_nvfp4_experts_quantize(gate_up[G, M, 2I], masked_m)):
+    group e quantizes only its first masked_m[e] rows.  Returns per group
+    (packed [valid, I/2], linear SF [valid, I/16]); the rows past masked_m[e]
+    carry no data and zero scales."""
+    out = []
+    for e, g in enumerate(np.asarray(gate_up_groups)):
+        valid = int(min(max(int(masked_m[e]), 0), g.shape[0]))
+        out.append(silu_mul_quant(g[:valid], gs_h))
+    return out
+
+
 def silu_mul_bf16(gate_up_bf16):
     gate_up = np.asarray(gate_up_bf16, dtype=np.float64)
     i = gate_up.shape[1] // 2

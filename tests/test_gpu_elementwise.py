@@ -151,3 +151,30 @@ def test_prepare_is_deterministic(lib):
         lib.nvfp4_prepare_gate_up_interleaved(dev(ws.packed), dev(ws.sf), 256, 512, w_out, s)
         outs.append((host(w_out), host(s)))
     assert all(np.array_equal(a, b) for a, b in zip(*outs))
+
+
+def test_silu_mul_quantize_masked_groups(lib):
+    """Three groups of up to 40 rows, masked to 40, 17 and 0 valid rows."""
+    groups, m_max, inter = 3, 40, 512
+    masked = np.array([40, 17, 0], dtype=np.int32)
+    bits, gu = _gate_up_input(groups * m_max, inter, 5)
+    gu3 = gu.reshape(groups, m_max, 2 * inter)
+    h_all = oracle.swiglu_h(gu)
+    gs = oracle.global_scale(np.abs(h_all).max())
+    q = torch.full((groups, m_max, inter // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    sfb = lib.nvfp4_sf_bytes(m_max, inter)
+    s = torch.full((groups * sfb,), 0xAB, dtype=torch.uint8, device="cuda")
+    lib.silu_mul_nvfp4_quantize_masked(bf16_dev(bits), dev(masked), groups, m_max, inter, scalar(gs), q, s)
+    torch.cuda.synchronize()
+    q, s = host(q), host(s)
+    ref = oracle.silu_mul_quant_masked(gu3, masked, gs)
+    for e in range(groups):
+        v = int(masked[e])
+        lin = oracle.sf_unswizzle_128x4(s[e * sfb:(e + 1) * sfb], m_max, inter // 16)
+        assert np.all(lin[v:] == 0), "scales of masked rows must be zero"
+        pad = oracle.sf_swizzle_128x4(lin)
+        assert np.array_equal(pad, s[e * sfb:(e + 1) * sfb]), "padding of the scale block is not zero"
+        assert np.all(q[e, v:] == 0xAB), "codes of masked rows must be untouched"
+        if v:
+            check_requant(q[e, :v], lin[:v], oracle.swiglu_h(gu3[e, :v]), gs, what=f"masked group {e}")
+            assert ref[e][0].shape == q[e, :v].shape

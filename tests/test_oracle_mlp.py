@@ -127,3 +127,15 @@ def test_fused_and_unfused_requant_agree_within_tolerance():
     # bf16 rounding of gate_up moves h by up to ~2^-8 relative: widen the window accordingly
     check_requant(uq, us, h, gs_h, max_frac=0.05, what="fused vs unfused", window=2.0 ** -7)
     assert h.shape == (4, w.inter)
+
+
+def test_masked_groups_reduce_to_dense_calls():
+    """Each group of the masked form is the dense SiLU*mul quantize of its
+    valid rows; a group with masked_m = 0 produces nothing."""
+    g = np.random.default_rng(21)
+    gu = (g.standard_normal((3, 10, 64)) * 1.5).astype(np.float32)
+    out = oracle.silu_mul_quant_masked(gu, [10, 4, 0], np.float32(20.0))
+    for e, valid in enumerate([10, 4, 0]):
+        ref = oracle.silu_mul_quant(gu[e, :valid], np.float32(20.0))
+        assert np.array_equal(out[e][0], ref[0]) and np.array_equal(out[e][1], ref[1])
+    assert out[2][0].shape == (0, 16)
