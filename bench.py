@@ -47,6 +47,19 @@ def parse():
     return p.parse_args()
 
 
+def aggregate(step_ms, tokens_per_step, world, device=None):
+    """Whole-job throughput of N independent replicas: every rank processed
+    `tokens_per_step` tokens per step; the job's step time is the slowest
+    rank's (max over ranks).  Returns (max step ms, tokens/s)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(step_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    return step_ms, world * tokens_per_step / (step_ms / 1000.0)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -392,11 +405,7 @@ def run_ours(args, world, rank, local):
         dom_ms = [v / args.steps for v in sums]
     clk = clocks.stop()
 
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = world * tokens_per_step / (step_ms / 1000.0)
+    step_ms, value = aggregate(step_ms, tokens_per_step, world, device=dev)
 
     roofline = None
     if dom_ms:

@@ -207,6 +207,33 @@ nvfp4_status nvfp4_gemm_swiglu_quant_ex(const uint8_t *a_fp4, const uint8_t *a_s
                                         int64_t k, void *workspace, size_t ws_bytes,
                                         nvfp4_algo algo, nvfp4_stream_t stream);
 
+/* Per-token dynamic activation scales ([P3] MoE excerpt: nvfp4_quantize(...,
+ * per_token_activation=True) returns a per-token scale).  Each row r gets its
+ * own global scale gs_r = fp32(448*6 / amax(row r)) (1 for an all-zero row)
+ * and is quantized exactly as nvfp4_quantize with it; out_row_scale[r] =
+ * fp32(1 / gs_r) is written for the GEMM.
+ *   x bf16 [m, k];  out_fp4 uint8 [m, k/2];  out_sf as nvfp4_quantize;
+ *   out_row_scale fp32 [m] DEVICE.  Requires k % 16 == 0. */
+nvfp4_status nvfp4_quantize_per_token(const uint16_t *x, int64_t m, int64_t k, uint8_t *out_fp4,
+                                      uint8_t *out_sf, nvfp4_sf_layout sf_layout, float *out_row_scale,
+                                      nvfp4_stream_t stream);
+
+/* nvfp4_gemm_ex / nvfp4_gemm_swiglu_quant_ex for activations quantized per
+ * token: every accumulator row m is multiplied by alpha * a_row_scale[m]
+ * (alpha then holds only the weight factor 1/gs_w).
+ *   a_row_scale fp32 [m] DEVICE, as written by nvfp4_quantize_per_token. */
+nvfp4_status nvfp4_gemm_per_token(const uint8_t *a_fp4, const uint8_t *a_sf, const float *a_row_scale,
+                                  const uint8_t *b_fp4, const uint8_t *b_sf, const float *alpha,
+                                  uint16_t *d, int64_t m, int64_t n, int64_t k, void *workspace,
+                                  size_t ws_bytes, nvfp4_algo algo, nvfp4_stream_t stream);
+nvfp4_status nvfp4_gemm_swiglu_quant_per_token(const uint8_t *a_fp4, const uint8_t *a_sf,
+                                               const float *a_row_scale, const uint8_t *w_int_fp4,
+                                               const uint8_t *w_int_sf, const float *alpha,
+                                               const float *out_global_scale, uint8_t *out_fp4,
+                                               uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
+                                               void *workspace, size_t ws_bytes, nvfp4_algo algo,
+                                               nvfp4_stream_t stream);
+
 /* W4A16 GEMM ([P3] fp4_gemm, quant_mode "w4a16" -> mm_bf16_fp4):
  *   d[m, n] = bf16( alpha * sum_k a[m, k] * (E2M1(b)*SF_b)[n, k] )
  *   a bf16 [m, k];  b_fp4/b_sf as nvfp4_gemm;  alpha fp32 [1] = 1/gs_b only.

@@ -31,6 +31,10 @@ _SIGS = {
     "nvfp4_quantize": [_P, _I64, _I64, _P, _P, _P, _I, _P],
     "silu_mul_nvfp4_quantize": [_P, _I64, _I64, _P, _P, _P, _P],
     "silu_mul_nvfp4_quantize_masked": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "nvfp4_quantize_per_token": [_P, _I64, _I64, _P, _P, _I, _P, _P],
+    "nvfp4_gemm_per_token": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
+    "nvfp4_gemm_swiglu_quant_per_token": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ,
+                                          _I, _P],
     "silu_mul_bf16": [_P, _I64, _I64, _P, _P],
     "nvfp4_gemm": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
     "nvfp4_gemm_ex": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
@@ -121,6 +125,25 @@ def silu_mul_nvfp4_quantize_masked(gate_up, masked_m, g, m_max, i, global_scale,
                                    stream=None):
     _call("silu_mul_nvfp4_quantize_masked", _ptr(gate_up), _ptr(masked_m), g, m_max, i, _ptr(global_scale),
           _ptr(out_fp4), _ptr(out_sf), _stream(stream))
+
+
+def nvfp4_quantize_per_token(x, m, k, out_fp4, out_sf, sf_layout, out_row_scale, stream=None):
+    _call("nvfp4_quantize_per_token", _ptr(x), m, k, _ptr(out_fp4), _ptr(out_sf), sf_layout,
+          _ptr(out_row_scale), _stream(stream))
+
+
+def nvfp4_gemm_per_token(a_fp4, a_sf, a_row_scale, b_fp4, b_sf, alpha, d, m, n, k, workspace=None,
+                         ws_bytes=0, algo=ALGO_AUTO, stream=None):
+    _call("nvfp4_gemm_per_token", _ptr(a_fp4), _ptr(a_sf), _ptr(a_row_scale), _ptr(b_fp4), _ptr(b_sf),
+          _ptr(alpha), _ptr(d), m, n, k, _ptr(workspace), ws_bytes, algo, _stream(stream))
+
+
+def nvfp4_gemm_swiglu_quant_per_token(a_fp4, a_sf, a_row_scale, w_int_fp4, w_int_sf, alpha,
+                                      out_global_scale, out_fp4, out_sf, m, n, k, workspace=None,
+                                      ws_bytes=0, algo=ALGO_AUTO, stream=None):
+    _call("nvfp4_gemm_swiglu_quant_per_token", _ptr(a_fp4), _ptr(a_sf), _ptr(a_row_scale), _ptr(w_int_fp4),
+          _ptr(w_int_sf), _ptr(alpha), _ptr(out_global_scale), _ptr(out_fp4), _ptr(out_sf), m, n, k,
+          _ptr(workspace), ws_bytes, algo, _stream(stream))
 
 
 def silu_mul_bf16(gate_up, m, i, out, stream=None):

@@ -133,10 +133,14 @@ nvfp4_status silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16
   return from_cuda(launch_silu_mul_bf16(gate_up, m, i, out, (cudaStream_t)stream));
 }
 
-nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, const uint8_t *b_fp4,
-                           const uint8_t *b_sf, const float *alpha, uint16_t *d, int64_t m,
-                           int64_t n, int64_t k, void *workspace, size_t ws_bytes, nvfp4_algo algo,
-                           nvfp4_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+nvfp4_status gemm_impl(const uint8_t *a_fp4, const uint8_t *a_sf, const float *a_row_scale,
+                       const uint8_t *b_fp4, const uint8_t *b_sf, const float *alpha, uint16_t *d,
+                       int64_t m, int64_t n, int64_t k, void *workspace, size_t ws_bytes,
+                       nvfp4_algo algo, nvfp4_stream_t stream) {
   if (!a_fp4 || !a_sf || !b_fp4 || !b_sf || !alpha || !d) return NVFP4_ERR_INVALID_ARG;
   if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
   if (!aligned16(a_fp4) || !aligned16(a_sf) || !aligned16(b_fp4) || !aligned16(b_sf) || !aligned16(d))
@@ -148,15 +152,93 @@ nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, const uint
   if (algo == NVFP4_ALGO_AUTO) algo = pick_algo(TC_W4A4, m, n, k);
   if (algo == NVFP4_ALGO_GEMV)
     return from_cuda(launch_gemv(GEMV_W4A4, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
-                                 nullptr, m, n, k, st));
+                                 nullptr, m, n, k, st, a_row_scale));
   if (algo == NVFP4_ALGO_TC_SWAPAB) {
     if (!swapab_supported(TC_W4A4, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     return from_cuda(launch_swapab(TC_W4A4, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
-                                   nullptr, m, n, k, workspace, ws_bytes, g_wait_limit.load(), st));
+                                   nullptr, m, n, k, workspace, ws_bytes, g_wait_limit.load(), st,
+                                   a_row_scale));
   }
   if (!tc_supported(TC_W4A4, false, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   return from_cuda(launch_tc(TC_W4A4, false, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
-                             nullptr, m, n, k, g_wait_limit.load(), st));
+                             nullptr, m, n, k, g_wait_limit.load(), st, a_row_scale));
+}
+
+nvfp4_status swiglu_impl(const uint8_t *a_fp4, const uint8_t *a_sf, const float *a_row_scale,
+                         const uint8_t *w_int_fp4, const uint8_t *w_int_sf, const float *alpha,
+                         const float *out_global_scale, uint8_t *out_fp4, uint8_t *out_sf, int64_t m,
+                         int64_t n, int64_t k, void *workspace, size_t ws_bytes, nvfp4_algo algo,
+                         nvfp4_stream_t stream) {
+  if (!a_fp4 || !a_sf || !w_int_fp4 || !w_int_sf || !alpha || !out_global_scale || !out_fp4 || !out_sf)
+    return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
+  if (n % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a_fp4) || !aligned16(a_sf) || !aligned16(w_int_fp4) || !aligned16(w_int_sf) ||
+      !aligned16(out_fp4) || !aligned16(out_sf))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (algo == NVFP4_ALGO_AUTO) algo = pick_algo(TC_W4A4_SWIGLU, m, n, k);
+  if (algo == NVFP4_ALGO_GEMV)
+    return from_cuda(launch_gemv(GEMV_W4A4_SWIGLU, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
+                                 out_global_scale, nullptr, out_fp4, out_sf, m, n, k, st, a_row_scale));
+  if (algo == NVFP4_ALGO_TC_SWAPAB) {
+    if (!swapab_supported(TC_W4A4_SWIGLU, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    return from_cuda(launch_swapab(TC_W4A4_SWIGLU, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
+                                   out_global_scale, nullptr, out_fp4, out_sf, m, n, k, workspace,
+                                   ws_bytes, g_wait_limit.load(), st, a_row_scale));
+  }
+  if (!tc_supported(TC_W4A4_SWIGLU, false, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A4_SWIGLU, false, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
+                             out_global_scale, nullptr, out_fp4, out_sf, m, n, k, g_wait_limit.load(),
+                             st, a_row_scale));
+}
+
+}  // namespace
+
+extern "C" {
+
+nvfp4_status nvfp4_gemm_ex(const uint8_t *a_fp4, const uint8_t *a_sf, const uint8_t *b_fp4,
+                           const uint8_t *b_sf, const float *alpha, uint16_t *d, int64_t m,
+                           int64_t n, int64_t k, void *workspace, size_t ws_bytes, nvfp4_algo algo,
+                           nvfp4_stream_t stream) {
+  return gemm_impl(a_fp4, a_sf, nullptr, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes, algo, stream);
+}
+
+nvfp4_status nvfp4_gemm_per_token(const uint8_t *a_fp4, const uint8_t *a_sf, const float *a_row_scale,
+                                  const uint8_t *b_fp4, const uint8_t *b_sf, const float *alpha,
+                                  uint16_t *d, int64_t m, int64_t n, int64_t k, void *workspace,
+                                  size_t ws_bytes, nvfp4_algo algo, nvfp4_stream_t stream) {
+  if (!a_row_scale) return NVFP4_ERR_INVALID_ARG;
+  return gemm_impl(a_fp4, a_sf, a_row_scale, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes, algo,
+                   stream);
+}
+
+nvfp4_status nvfp4_gemm_swiglu_quant_per_token(const uint8_t *a_fp4, const uint8_t *a_sf,
+                                               const float *a_row_scale, const uint8_t *w_int_fp4,
+                                               const uint8_t *w_int_sf, const float *alpha,
+                                               const float *out_global_scale, uint8_t *out_fp4,
+                                               uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
+                                               void *workspace, size_t ws_bytes, nvfp4_algo algo,
+                                               nvfp4_stream_t stream) {
+  if (!a_row_scale) return NVFP4_ERR_INVALID_ARG;
+  return swiglu_impl(a_fp4, a_sf, a_row_scale, w_int_fp4, w_int_sf, alpha, out_global_scale, out_fp4,
+                     out_sf, m, n, k, workspace, ws_bytes, algo, stream);
+}
+
+nvfp4_status nvfp4_quantize_per_token(const uint16_t *x, int64_t m, int64_t k, uint8_t *out_fp4,
+                                      uint8_t *out_sf, nvfp4_sf_layout sf_layout, float *out_row_scale,
+                                      nvfp4_stream_t stream) {
+  if (!x || !out_fp4 || !out_sf || !out_row_scale || m < 0 || k <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (sf_layout != NVFP4_SF_LINEAR && sf_layout != NVFP4_SF_SWIZZLED_128x4) return NVFP4_ERR_INVALID_ARG;
+  if (k % 16 != 0 || !aligned16(x) || !aligned16(out_fp4) || m >= (int64_t(1) << 31))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  return from_cuda(launch_quantize_per_token(x, m, k, out_fp4, out_sf, sf_layout == NVFP4_SF_SWIZZLED_128x4,
+                                             out_row_scale, (cudaStream_t)stream));
 }
 
 nvfp4_status nvfp4_gemm(const uint8_t *a_fp4, const uint8_t *a_sf, const uint8_t *b_fp4,
@@ -172,31 +254,8 @@ nvfp4_status nvfp4_gemm_swiglu_quant_ex(const uint8_t *a_fp4, const uint8_t *a_s
                                         uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
                                         int64_t k, void *workspace, size_t ws_bytes, nvfp4_algo algo,
                                         nvfp4_stream_t stream) {
-  if (!a_fp4 || !a_sf || !w_int_fp4 || !w_int_sf || !alpha || !out_global_scale || !out_fp4 || !out_sf)
-    return NVFP4_ERR_INVALID_ARG;
-  if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
-  if (n % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(a_fp4) || !aligned16(a_sf) || !aligned16(w_int_fp4) || !aligned16(w_int_sf) ||
-      !aligned16(out_fp4) || !aligned16(out_sf))
-    return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
-  if (nvfp4_status s = check_arch()) return s;
-  if (m == 0) return NVFP4_OK;
-  const cudaStream_t st = (cudaStream_t)stream;
-  if (algo == NVFP4_ALGO_AUTO) algo = pick_algo(TC_W4A4_SWIGLU, m, n, k);
-  if (algo == NVFP4_ALGO_GEMV)
-    return from_cuda(launch_gemv(GEMV_W4A4_SWIGLU, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
-                                 out_global_scale, nullptr, out_fp4, out_sf, m, n, k, st));
-  if (algo == NVFP4_ALGO_TC_SWAPAB) {
-    if (!swapab_supported(TC_W4A4_SWIGLU, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    return from_cuda(launch_swapab(TC_W4A4_SWIGLU, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
-                                   out_global_scale, nullptr, out_fp4, out_sf, m, n, k, workspace,
-                                   ws_bytes, g_wait_limit.load(), st));
-  }
-  if (!tc_supported(TC_W4A4_SWIGLU, false, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  return from_cuda(launch_tc(TC_W4A4_SWIGLU, false, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
-                             out_global_scale, nullptr, out_fp4, out_sf, m, n, k,
-                             g_wait_limit.load(), st));
+  return swiglu_impl(a_fp4, a_sf, nullptr, w_int_fp4, w_int_sf, alpha, out_global_scale, out_fp4, out_sf, m, n,
+                     k, workspace, ws_bytes, algo, stream);
 }
 
 nvfp4_status nvfp4_gemm_swiglu_quant(const uint8_t *a_fp4, const uint8_t *a_sf,

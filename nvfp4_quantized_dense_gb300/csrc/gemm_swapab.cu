@@ -66,6 +66,7 @@ struct SwapArgs {
   int32_t split_ok;          // 0: no workspace, every CTA owns whole tiles
   uint32_t wait_limit;
   int *status;
+  const float *rs;      // optional per-token activation dequant factor [M]
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -328,14 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < NT; ++t)
             if (t < mt) {
-              const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v[t]);
+              const float at = p.rs ? alpha * p.rs[t] : alpha;
+              const __nv_bfloat16 o = __float2bfloat16_rn(at * v[t]);
               p.d[(size_t)t * p.n + n] = *reinterpret_cast<const uint16_t *>(&o);
             }
         }
       } else {
         // rows 0..63 of the tile are up, 64..127 gate, for features 64*tile + (0..63)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) s_out[r * C::PITCH + t] = alpha * v[t];
+        for (int t = 0; t < NT; ++t) s_out[r * C::PITCH + t] = (p.rs && t < mt ? alpha * p.rs[t] : alpha) * v[t];
         epi_bar();
         const int inter = p.n >> 1;
         const int ocp4 = ((inter >> 4) + 3) >> 2;
@@ -407,7 +409,7 @@ template <int MODE, int NT>
 cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, const uint8_t *w,
                       const uint8_t *w_sf, const float *alpha, const float *out_gs, uint16_t *d,
                       uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k, void *ws,
-                      uint32_t wait_limit, cudaStream_t st) {
+                      uint32_t wait_limit, cudaStream_t st, const float *rs) {
   using C = Cfg<NT>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -443,6 +445,7 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   a.grid = split ? pl.grid : (pl.tiles < num_sms() ? pl.tiles : num_sms());
   a.wait_limit = wait_limit;
   a.status = device_status_ptr();
+  a.rs = rs;
   if (!a.status) return cudaErrorInvalidValue;
   return launch_pdl(swapab_kernel<MODE, NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_w, tm_x, a);
 }
@@ -451,17 +454,17 @@ template <int MODE>
 cudaError_t launch_mode(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, const uint8_t *w,
                         const uint8_t *w_sf, const float *alpha, const float *out_gs, uint16_t *d,
                         uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k, void *ws,
-                        uint32_t wait_limit, cudaStream_t st) {
+                        uint32_t wait_limit, cudaStream_t st, const float *rs) {
   switch (pl.nt) {
     case 16:
       return launch_nt<MODE, 16>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
-                                 wait_limit, st);
+                                 wait_limit, st, rs);
     case 32:
       return launch_nt<MODE, 32>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
-                                 wait_limit, st);
+                                 wait_limit, st, rs);
     default:
       return launch_nt<MODE, 64>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
-                                 wait_limit, st);
+                                 wait_limit, st, rs);
   }
 }
 
@@ -482,7 +485,8 @@ size_t swapab_workspace_bytes(TcMode mode, int64_t m, int64_t n, int64_t k) {
 cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,
                           const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
                           uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
-                          void *workspace, size_t ws_bytes, uint32_t wait_limit, cudaStream_t st) {
+                          void *workspace, size_t ws_bytes, uint32_t wait_limit, cudaStream_t st,
+                          const float *a_row_scale) {
   if (!swapab_supported(mode, m, n, k)) return cudaErrorNotSupported;
   Plan pl = make_plan(m, n, k);
   if (pl.ws_bytes > 0 && (workspace == nullptr || ws_bytes < pl.ws_bytes)) {
@@ -493,9 +497,9 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
   const uint8_t *x = static_cast<const uint8_t *>(a);
   if (mode == TC_W4A4)
     return launch_mode<TC_W4A4>(pl, x, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, workspace,
-                                wait_limit, st);
+                                wait_limit, st, a_row_scale);
   return launch_mode<TC_W4A4_SWIGLU>(pl, x, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k,
-                                     workspace, wait_limit, st);
+                                     workspace, wait_limit, st, a_row_scale);
 }
 
 }  // namespace nvfp4

@@ -54,14 +54,18 @@ constexpr int BM = 128, BN = 256, BK = 256;
 constexpr int KSTEPS = BK / 64;                 // MMAs per stage
 constexpr int STAGES = 4;
 constexpr uint32_t A_BYTES = BM * BK / 2;       // 16 KB
-constexpr uint32_t B_BYTES = BN * BK / 2;       // 32 KB
+constexpr uint32_t B_BYTES = BN * BK / 2;       // 32 KB (two 16 KB halves, one per CTA of the pair)
+constexpr uint32_t B_HALF = B_BYTES / 2;
 constexpr uint32_t SFA_BYTES = (BM / 128) * KSTEPS * 512;
 constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int kThreads = 320;           // producer, MMA, 8 epilogue warps
+constexpr int kThreads = 352;           // producer, MMA, 8 epilogue warps, scale-copy warp
+constexpr int kCluster = 2;             // CTAs sharing one weight tile
+constexpr uint16_t kPairMask = 0x3;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0, SFA_COL = 256, SFB_COL = 256 + 4 * KSTEPS;
+// accumulator 256 columns; two scale slots of 48 columns (SFA 16 + SFB 32)
+constexpr uint32_t ACC_COL = 0, SF_COL = 256, SF_SLOT = 64, SFB_OFF = 4 * KSTEPS;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
 constexpr uint32_t kDrainPolls = 1u << 22;
 
@@ -81,9 +85,10 @@ struct TcArgs {
   uint8_t *out_fp4;       // fused: [M, N/4]
   uint8_t *out_sf;        // fused: swizzled over M rows, N/32 columns
   int32_t m, n, k;
-  int32_t num_m, num_n;
+  int32_t num_m, num_n, num_mpairs;
   uint32_t wait_limit;
   int *status;            // device status word
+  const float *rs;        // optional per-row activation dequant factor [M]
 };
 
 struct Smem {
@@ -97,7 +102,9 @@ struct Smem {
   __device__ uint64_t *tfull() const { return empty() + STAGES; }
   __device__ uint64_t *tempty() const { return tfull() + 1; }
   __device__ uint64_t *drain() const { return tempty() + 1; }
-  __device__ uint32_t *tslot() const { return reinterpret_cast<uint32_t *>(drain() + 1); }
+  __device__ uint64_t *sf_full() const { return drain() + 1; }
+  __device__ uint64_t *sf_empty() const { return sf_full() + 2; }
+  __device__ uint32_t *tslot() const { return reinterpret_cast<uint32_t *>(sf_empty() + 2); }
   __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(tslot() + 1); }
 };
 
@@ -111,6 +118,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Kernel shape (clusters of two CTAs, one CTA per SM, persistent): the two
+// CTAs of a cluster compute the 128-row tiles 2p and 2p+1 of M against the
+// same 256-row weight tile, k-block by k-block in lockstep.  Each CTA loads
+// its own activation tile and scales, and one 128-row half of the weight tile
+// plus that half's scales, delivered by TMA multicast to both CTAs -- so the
+// weight stream is read from L2 once per pair.  A stage is refilled only when
+// the MMAs of both CTAs are done with it (their commits arrive on both CTAs'
+// empty barriers).  Roles per CTA:
+//   warp 0      TMA producer;
+//   warp 1      TMEM owner, single-thread MMA issuer;
+//   warp 10     copies each stage's block scales into one of two TMEM scale
+//               slots (tcgen05.cp) ahead of the MMAs;
+//   warps 2..9  epilogue: TMEM -> registers, TMEM released at once, then bf16
+//               output or the fused SwiGLU + NVFP4 requantize.
 template <int MODE>  // TC_W4A4: bf16 out; TC_W4A4_SWIGLU: fused SwiGLU + NVFP4 requant
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -119,16 +140,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem sm{reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int *abort_flag = sm.abort_flag();
+  const int rank = (int)ptx::cluster_ctarank();
   pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm.full()[s], 1);
-      ptx::mbar_init(&sm.empty()[s], 1);
+      ptx::mbar_init(&sm.empty()[s], kCluster);   // one commit from each CTA's MMA
     }
     ptx::mbar_init(sm.tfull(), 1);
     ptx::mbar_init(sm.tempty(), 256);
     ptx::mbar_init(sm.drain(), 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sm.sf_full()[b], 1);
+      ptx::mbar_init(&sm.sf_empty()[b], 1);
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tm_a);
@@ -139,18 +165,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();          // both CTAs' barriers exist before any multicast lands
   ptx::tc_fence_after();
   const uint32_t tmem = *sm.tslot();
 
-  const int num_tiles = p.num_m * p.num_n;
+  const int cluster = blockIdx.x / kCluster, num_clusters = gridDim.x / kCluster;
+  const int num_pairs = p.num_mpairs * p.num_n;
   const int ksteps_total = p.k >> 6;              // K / 64
   const int num_kb = (ksteps_total + KSTEPS - 1) / KSTEPS;
-  const int cp4a = ksteps_total, cp4b = ksteps_total;   // 512-byte scale tiles per row block
+  const int cp4 = ksteps_total;                   // 512-byte scale tiles per 128-row block
   const int nrb_b = (p.n + 127) >> 7;             // 128-row blocks of B
   const uint32_t limit = p.wait_limit;
+  auto tile_of = [&](int pair, int &mt, int &nt) {
+    nt = pair / p.num_mpairs;
+    mt = (pair - nt * p.num_mpairs) * kCluster + rank;
+  };
 
-  // producer bookkeeping for the drain: last issued phase parity per stage
   uint32_t issued_mask = 0, issued_parity = 0;
   bool mma_issued = false;
 
@@ -160,25 +190,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_b = ptx::l2_policy_evict_first();
       int s = 0;
       uint32_t ph = 0;
-      // The first STAGES stages get their weight (B) tiles before the previous
-      // kernel on the stream has finished; their activation (A) tiles follow
-      // once it has.
+      // The first STAGES stages get their weight halves before the previous
+      // kernel on the stream has finished; the activation tiles follow once
+      // it has.
       int pend_s[STAGES], pend_kb[STAGES], pend_mt[STAGES];
       int npend = 0, c = 0;
       bool flushed = false;
       auto issue_a = [&](int st, int mt, int kb) {
         const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
         ptx::tma_load_2d(sm.a(st), &tm_a, &sm.full()[st], kb * (BK / 2), mt * BM, pol_a);
-        ptx::bulk_load(sm.sfa(st), p.sfa + ((size_t)mt * cp4a + kb * KSTEPS) * 512, nk * 512u, &sm.full()[st],
-                       pol_a);
+        if (mt < p.num_m)
+          ptx::bulk_load(sm.sfa(st), p.sfa + ((size_t)mt * cp4 + kb * KSTEPS) * 512, nk * 512u,
+                         &sm.full()[st], pol_a);
       };
       auto flush = [&]() {
         pdl_wait();
         for (int i = 0; i < npend; ++i) issue_a(pend_s[i], pend_mt[i], pend_kb[i]);
         flushed = true;
       };
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-        const int mt = tile % p.num_m, nt = tile / p.num_m;
+      for (int pair = cluster; pair < num_pairs && !*abort_flag; pair += num_clusters) {
+        int mt, nt;
+        tile_of(pair, mt, nt);
+        const int nbv = min(2, nrb_b - nt * 2);
         for (int kb = 0; kb < num_kb; ++kb, ++c) {
           if (c == STAGES && !flushed) flush();
           if (!ptx::mbar_wait_bounded(&sm.empty()[s], ph ^ 1u, limit, kDefaultTimeoutNs, abort_flag)) {
@@ -186,14 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
-          const int nbv = min(2, nrb_b - nt * 2);
-          const uint32_t bytes = A_BYTES + B_BYTES + (uint32_t)nk * 512u * (1u + (uint32_t)nbv);
-          ptx::mbar_arrive_expect_tx(&sm.full()[s], bytes);
-          ptx::tma_load_2d(sm.b(s), &tm_b, &sm.full()[s], kb * (BK / 2), nt * BN, pol_b);
-          for (int rb = 0; rb < nbv; ++rb)
-            ptx::bulk_load(sm.sfb(s) + rb * (KSTEPS * 512),
-                           p.sfb + ((size_t)(nt * 2 + rb) * cp4b + kb * KSTEPS) * 512, nk * 512u,
-                           &sm.full()[s], pol_b);
+          const uint32_t sfa_bytes = mt < p.num_m ? (uint32_t)nk * 512u : 0u;
+          ptx::mbar_arrive_expect_tx(&sm.full()[s], A_BYTES + B_BYTES + sfa_bytes + (uint32_t)nk * 512u * nbv);
+          // my half of the weight tile and of its scales, to both CTAs
+          ptx::tma_load_2d_mc(sm.b(s) + rank * B_HALF, &tm_b, &sm.full()[s], kb * (BK / 2), nt * BN + rank * 128,
+                              kPairMask, pol_b);
+          if (rank < nbv)
+            ptx::bulk_load_mc(sm.sfb(s) + rank * (KSTEPS * 512),
+                              p.sfb + ((size_t)(nt * 2 + rank) * cp4 + kb * KSTEPS) * 512, nk * 512u,
+                              &sm.full()[s], kPairMask, pol_b);
           if (c < STAGES) {
             pend_s[npend] = s;
             pend_kb[npend] = kb;
@@ -213,55 +247,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
     if (ptx::elect_one()) {
       constexpr uint32_t idesc = idesc_nvfp4(BM, BN);
-      int s = 0;
+      int s = 0, g = 0;                            // stage, global k-block count
       uint32_t ph = 0;
       int it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+      for (int pair = cluster; pair < num_pairs && !*abort_flag; pair += num_clusters, ++it) {
         if (!ptx::mbar_wait_bounded(sm.tempty(), (uint32_t)(it & 1) ^ 1u, limit, kDefaultTimeoutNs,
                                     abort_flag)) {
           give_up(abort_flag, p.status);
           break;
         }
         ptx::tc_fence_after();
-        const int nt = tile / p.num_m;
-        const int nbv = min(2, nrb_b - nt * 2);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const int slot = g & 1;
+          if (!ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag) ||
+              !ptx::mbar_wait_bounded(&sm.sf_full()[slot], (uint32_t)((g >> 1) & 1), limit, kDefaultTimeoutNs,
+                                      abort_flag)) {
             give_up(abort_flag, p.status);
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
-          const uint32_t sfa_s = ptx::smem_u32(sm.sfa(s)), sfb_s = ptx::smem_u32(sm.sfb(s));
-          for (int j = 0; j < nk; ++j) {
-            ptx::tmem_cp_32x128b_x4(tmem + SFA_COL + 4 * j, ptx::smem_desc(sfa_s + 512 * j, 0, 128, 0));
-            for (int rb = 0; rb < nbv; ++rb)
-              ptx::tmem_cp_32x128b_x4(tmem + SFB_COL + 8 * j + 4 * rb,
-                                      ptx::smem_desc(sfb_s + rb * (KSTEPS * 512) + 512 * j, 0, 128, 0));
-          }
+          const uint32_t sf = tmem + SF_COL + slot * SF_SLOT;
           const uint32_t a_s = ptx::smem_u32(sm.a(s)), b_s = ptx::smem_u32(sm.b(s));
-          for (int j = 0; j < nk; ++j) {
+          for (int j = 0; j < nk; ++j)
             ptx::mma_nvfp4(tmem + ACC_COL, ptx::smem_desc(a_s + 32 * j, 16, 1024, 2),
-                           ptx::smem_desc(b_s + 32 * j, 16, 1024, 2), idesc, tmem + SFA_COL + 4 * j,
-                           tmem + SFB_COL + 8 * j, (kb | j) != 0);
-          }
+                           ptx::smem_desc(b_s + 32 * j, 16, 1024, 2), idesc, sf + 4 * j, sf + SFB_OFF + 8 * j,
+                           (kb | j) != 0);
           mma_issued = true;
-          ptx::tc_commit(&sm.empty()[s]);
+          ptx::tc_commit_mc(&sm.empty()[s], kPairMask);   // this stage is free for both producers
+          ptx::tc_commit(&sm.sf_empty()[slot]);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
         ptx::tc_commit(sm.tfull());
       }
     }
+  } else if (warp == 10) {
+    // --------------------------------------------------------- scale copies
+    pdl_wait();
+    if (ptx::elect_one()) {
+      int s = 0, g = 0;
+      uint32_t ph = 0;
+      for (int pair = cluster; pair < num_pairs && !*abort_flag; pair += num_clusters) {
+        int mt, nt;
+        tile_of(pair, mt, nt);
+        const int nbv = min(2, nrb_b - nt * 2);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const int slot = g & 1;
+          if (!ptx::mbar_wait_bounded(&sm.sf_empty()[slot], (uint32_t)((g >> 1) & 1) ^ 1u, limit,
+                                      kDefaultTimeoutNs, abort_flag) ||
+              !ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
+            give_up(abort_flag, p.status);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
+          const uint32_t sf = tmem + SF_COL + slot * SF_SLOT;
+          const uint32_t sfa_s = ptx::smem_u32(sm.sfa(s)), sfb_s = ptx::smem_u32(sm.sfb(s));
+          for (int j = 0; j < nk; ++j) {
+            ptx::tmem_cp_32x128b_x4(sf + 4 * j, ptx::smem_desc(sfa_s + 512 * j, 0, 128, 0));
+            for (int rb = 0; rb < nbv; ++rb)
+              ptx::tmem_cp_32x128b_x4(sf + SFB_OFF + 8 * j + 4 * rb,
+                                      ptx::smem_desc(sfb_s + rb * (KSTEPS * 512) + 512 * j, 0, 128, 0));
+          }
+          ptx::tc_commit(&sm.sf_full()[slot]);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Eight warps: warp w reads TMEM lane quarter w % 4 (the hardware lets a
-    // warp reach only its own quarter) and column half (w - 2) / 4, i.e. 128
-    // accumulator columns of its 32 rows.  It holds them in registers and
-    // releases TMEM before any math or store, so the MMAs of the next tile run
-    // while this tile's epilogue finishes.
+    // Warp w reads TMEM lane quarter w % 4 (the hardware lets a warp reach
+    // only its own quarter) and column half (w - 2) / 4: 128 accumulator
+    // columns of its 32 rows, held in registers; TMEM is released before any
+    // math or store, so the next tile's MMAs run meanwhile.
     pdl_wait();
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
@@ -269,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_base = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL + 128 * half;
     const float alpha = __ldg(p.alpha);
     int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+    for (int pair = cluster; pair < num_pairs; pair += num_clusters, ++it) {
       if (!ptx::mbar_wait_bounded(sm.tfull(), (uint32_t)(it & 1), limit, kDefaultTimeoutNs, abort_flag)) {
         give_up(abort_flag, p.status);
         break;
@@ -282,8 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(sm.tempty());            // accumulator free for the next tile
 
-      const int mt = tile % p.num_m, nt = tile / p.num_m;
+      int mt, nt;
+      tile_of(pair, mt, nt);
+      if (mt >= p.num_m) continue;              // odd tail: this CTA only fed its partner
       const int m = mt * BM + row;
+      const float am = (p.rs && m < p.m) ? alpha * p.rs[m] : alpha;
       if constexpr (MODE == TC_W4A4) {
         const int n0 = nt * BN + 128 * half;
         if (m < p.m) {
@@ -293,10 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = n0 + 8 * c;
             if (n < p.n) {
               uint4 o;
-              o.x = pack_bf16x2(alpha * __uint_as_float(acc[8 * c + 0]), alpha * __uint_as_float(acc[8 * c + 1]));
-              o.y = pack_bf16x2(alpha * __uint_as_float(acc[8 * c + 2]), alpha * __uint_as_float(acc[8 * c + 3]));
-              o.z = pack_bf16x2(alpha * __uint_as_float(acc[8 * c + 4]), alpha * __uint_as_float(acc[8 * c + 5]));
-              o.w = pack_bf16x2(alpha * __uint_as_float(acc[8 * c + 6]), alpha * __uint_as_float(acc[8 * c + 7]));
+              o.x = pack_bf16x2(am * __uint_as_float(acc[8 * c + 0]), am * __uint_as_float(acc[8 * c + 1]));
+              o.y = pack_bf16x2(am * __uint_as_float(acc[8 * c + 2]), am * __uint_as_float(acc[8 * c + 3]));
+              o.z = pack_bf16x2(am * __uint_as_float(acc[8 * c + 4]), am * __uint_as_float(acc[8 * c + 5]));
+              o.w = pack_bf16x2(am * __uint_as_float(acc[8 * c + 6]), am * __uint_as_float(acc[8 * c + 7]));
               *reinterpret_cast<uint4 *>(drow + n) = o;
             }
           }
@@ -316,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float hv[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                hv[i] = silu_mul_fast(alpha * __uint_as_float(acc[64 + 16 * qb + i]),
-                                      alpha * __uint_as_float(acc[16 * qb + i]));
+                hv[i] = silu_mul_fast(am * __uint_as_float(acc[64 + 16 * qb + i]),
+                                      am * __uint_as_float(acc[16 * qb + i]));
               sfw |= quantize_block16(hv, gs, codes[2 * qb], codes[2 * qb + 1]) << (8 * qb);
             }
             uint4 *dst = reinterpret_cast<uint4 *>(p.out_fp4 + (size_t)m * (inter >> 1) + f0 / 2);
@@ -350,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();          // the partner no longer multicasts into this CTA
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -404,25 +471,49 @@ namespace {
 template <int MODE>
 cudaError_t launch_mode(const uint8_t *a, const uint8_t *a_sf, const uint8_t *b, const uint8_t *b_sf,
                         const float *alpha, const float *out_gs, uint16_t *d, uint8_t *out_fp4,
-                        uint8_t *out_sf, int64_t m, int64_t n, int64_t k, uint32_t wait_limit,
-                        cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
+                          uint8_t *out_sf, int64_t m, int64_t n, int64_t k, uint32_t wait_limit,
+                        cudaStream_t st, const float *rs) {
+  static int max_clusters[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (!max_clusters[dev]) {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    // how many 2-CTA clusters of this kernel the device holds at once
+    cfg.gridDim = dim3(kCluster * (num_sms() / kCluster));
+    int nc = 0;
+    e = cudaOccupancyMaxActiveClusters(&nc, tc_gemm_kernel<MODE>, &cfg);
+    if (e != cudaSuccess || nc <= 0) nc = num_sms() / kCluster;
+    max_clusters[dev] = nc;
   }
   CUtensorMap tm_a, tm_b;
-  // codes [rows, k/2] bytes; box 128 bytes of K x tile rows, 128-byte swizzle
-  if (!make_byte_map(&tm_a, a, m, k / 2, 128, BM, true) || !make_byte_map(&tm_b, b, n, k / 2, 128, BN, true))
+  // codes [rows, k/2] bytes; box 128 bytes of K x (128 activation rows | 128
+  // weight rows = half a weight tile), 128-byte swizzle
+  if (!make_byte_map(&tm_a, a, m, k / 2, 128, BM, true) || !make_byte_map(&tm_b, b, n, k / 2, 128, BN / 2, true))
     return cudaErrorInvalidValue;
   TcArgs args{a_sf, b_sf, alpha, out_gs, d, out_fp4, out_sf, (int32_t)m, (int32_t)n, (int32_t)k,
-              (int32_t)((m + BM - 1) / BM), (int32_t)((n + BN - 1) / BN), wait_limit, device_status_ptr()};
+              (int32_t)((m + BM - 1) / BM), (int32_t)((n + BN - 1) / BN), 0, wait_limit, device_status_ptr(), rs};
   if (!args.status) return cudaErrorInvalidValue;
-  const int tiles = args.num_m * args.num_n;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_pdl(tc_gemm_kernel<MODE>, dim3(grid), dim3(kThreads), SMEM_BYTES, st, tm_a, tm_b, args);
+  args.num_mpairs = (args.num_m + kCluster - 1) / kCluster;
+  const int pairs = args.num_mpairs * args.num_n;
+  const int clusters = pairs < max_clusters[dev] ? pairs : max_clusters[dev];
+  cfg.gridDim = dim3(kCluster * clusters);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE>, tm_a, tm_b, args);
 }
 
 }  // namespace
@@ -438,13 +529,14 @@ bool tc_supported(TcMode mode, bool swap_ab, int64_t m, int64_t n, int64_t k) {
 cudaError_t launch_tc(TcMode mode, bool swap_ab, const void *a, const uint8_t *a_sf, const uint8_t *b,
                       const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
                       uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
-                      uint32_t wait_limit, cudaStream_t st) {
+                      uint32_t wait_limit, cudaStream_t st, const float *a_row_scale) {
   if (!tc_supported(mode, swap_ab, m, n, k)) return cudaErrorNotSupported;
   const uint8_t *a8 = static_cast<const uint8_t *>(a);
   if (mode == TC_W4A4)
-    return launch_mode<TC_W4A4>(a8, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, wait_limit, st);
+    return launch_mode<TC_W4A4>(a8, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, wait_limit, st,
+                                a_row_scale);
   return launch_mode<TC_W4A4_SWIGLU>(a8, a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k,
-                                     wait_limit, st);
+                                     wait_limit, st, a_row_scale);
 }
 
 }  // namespace nvfp4

@@ -106,6 +106,7 @@ struct GemvArgs {
   uint8_t *out_sf;     // fused: swizzled over M rows, N/32 columns
   int64_t m, n, k;
   int64_t m0;          // first token of this pass
+  const float *rs;     // optional per-token dequant factor [M]
 };
 
 // Weight row handled by warp `w`, sub-row `r` of CTA `cta`.  Plain mode: rows
@@ -134,8 +135,9 @@ __device__ __forceinline__ void swiglu_epilogue(const GemvArgs &p, float (&acc)[
       const float v = warp_sum(acc[t][r]);
       if (lane == 0) {
         const int f = (warp & 3) * R + r;
-        if (warp < 4) s_up[t][f] = alpha * v;
-        else s_gate[t][f] = alpha * v;
+        const float at = (p.rs && t < mt) ? alpha * p.rs[p.m0 + t] : alpha;
+        if (warp < 4) s_up[t][f] = at * v;
+        else s_gate[t][f] = at * v;
       }
     }
   __syncthreads();
@@ -230,7 +232,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_w4a4_kernel(GemvArgs p) {
       for (int r = 0; r < R; ++r) {
         const float v = warp_sum(acc[t][r]);
         if (lane == 0 && t < mt) {
-          const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v);
+          const float at = p.rs ? alpha * p.rs[p.m0 + t] : alpha;
+          const __nv_bfloat16 o = __float2bfloat16_rn(at * v);
           p.d[(p.m0 + t) * p.n + rows[r]] = *reinterpret_cast<const uint16_t *>(&o);
         }
       }
@@ -322,9 +325,9 @@ cudaError_t launch_mt(GemvMode mode, const GemvArgs &a, cudaStream_t st) {
 cudaError_t launch_gemv(GemvMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,
                         const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
                         uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
-                        cudaStream_t st) {
+                        cudaStream_t st, const float *a_row_scale) {
   GemvArgs args{static_cast<const uint8_t *>(a), a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf,
-                m, n, k, 0};
+                m, n, k, 0, a_row_scale};
   // passes of 16, 8, 4, 2 or 1 tokens until every token is covered
   for (int64_t m0 = 0; m0 < m;) {
     const int64_t left = m - m0;

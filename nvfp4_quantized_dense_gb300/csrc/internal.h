@@ -29,6 +29,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 cudaError_t launch_quantize(const uint16_t *x, int64_t m, int64_t k, const float *gs,
                             uint8_t *out_fp4, uint8_t *out_sf, bool swizzled, cudaStream_t st);
+cudaError_t launch_quantize_per_token(const uint16_t *x, int64_t m, int64_t k, uint8_t *out_fp4,
+                                      uint8_t *out_sf, bool swizzled, float *row_scale, cudaStream_t st);
 cudaError_t launch_silu_mul_quantize(const uint16_t *gate_up, int64_t m, int64_t i, const float *gs,
                                      uint8_t *out_fp4, uint8_t *out_sf, cudaStream_t st);
 cudaError_t launch_silu_mul_quantize_masked(const uint16_t *gate_up, const int32_t *masked_m, int64_t g,
@@ -41,17 +43,20 @@ cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf_lin, int64_t n, i
 
 // CUDA-core GEMV family (any M; meant for decode-sized M).
 enum GemvMode { GEMV_W4A4 = 0, GEMV_W4A4_SWIGLU = 1, GEMV_W4A16 = 2 };
+// a_row_scale (optional, fp32 [m]): per-row activation dequant factor that
+// multiplies alpha (per-token activation scales); nullptr for none.
 cudaError_t launch_gemv(GemvMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,
                         const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
                         uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
-                        cudaStream_t st);
+                        cudaStream_t st, const float *a_row_scale = nullptr);
 
 // tcgen05 tensor-core family.
 enum TcMode { TC_W4A4 = 0, TC_W4A4_SWIGLU = 1, TC_W4A16 = 2 };
 cudaError_t launch_tc(TcMode mode, bool swap_ab, const void *a, const uint8_t *a_sf,
                       const uint8_t *b, const uint8_t *b_sf, const float *alpha,
                       const float *out_gs, uint16_t *d, uint8_t *out_fp4, uint8_t *out_sf,
-                      int64_t m, int64_t n, int64_t k, uint32_t wait_limit, cudaStream_t st);
+                      int64_t m, int64_t n, int64_t k, uint32_t wait_limit, cudaStream_t st,
+                      const float *a_row_scale = nullptr);
 bool tc_supported(TcMode mode, bool swap_ab, int64_t m, int64_t n, int64_t k);
 
 // Device status word of the current device (set by kernels that give up a
@@ -74,7 +79,7 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
                           const uint8_t *b_sf, const float *alpha, const float *out_gs,
                           uint16_t *d, uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
                           int64_t k, void *workspace, size_t ws_bytes, uint32_t wait_limit,
-                          cudaStream_t st);
+                          cudaStream_t st, const float *a_row_scale = nullptr);
 
 // W4A16 on the tensor cores (weights dequantized to bf16 in shared memory).
 bool w4a16_tc_supported(int64_t m, int64_t n, int64_t k);

@@ -59,6 +59,53 @@ __global__ void __launch_bounds__(kTileThreads) quantize_kernel(
   }
 }
 
+// Per-token quantize: one CTA per row (rows past m only zero their padding
+// scales).  Pass 1 reduces the row's amax, gs = fp32(448*6 / amax) (1 for an
+// all-zero row); pass 2 quantizes every 16-block with gs exactly as
+// quantize_kernel; row_scale[row] = fp32(1 / gs) is the dequant factor a GEMM
+// folds into that row.
+__global__ void __launch_bounds__(256) quantize_per_token_kernel(
+    const uint16_t *__restrict__ x, int64_t m, int64_t k, uint8_t *__restrict__ out_fp4,
+    uint8_t *__restrict__ out_sf, bool swizzled, float *__restrict__ row_scale) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t row = blockIdx.x;
+  const int64_t cols = k >> 4, cp4 = (cols + 3) >> 2;
+  const int64_t cols_pad = swizzled ? cp4 * 4 : cols;
+  if (row >= m) {        // padding rows of the swizzled layout
+    for (int64_t j = threadIdx.x; j < cols_pad; j += blockDim.x) out_sf[sf_swizzled_offset(row, j, cp4)] = 0;
+    return;
+  }
+  __shared__ float s_red[8];
+  float amax = 0.0f;
+  for (int64_t j = threadIdx.x; j < cols; j += blockDim.x) {
+    float v[16];
+    load16_bf16(x + row * k + j * 16, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.0f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, s_red[w]);
+  const float gs = amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;    // 448 * 6
+  for (int64_t j = threadIdx.x; j < cols_pad; j += blockDim.x) {
+    uint32_t sf = 0;
+    if (j < cols) {
+      float v[16];
+      load16_bf16(x + row * k + j * 16, v);
+      uint32_t lo, hi;
+      sf = quantize_block16(v, gs, lo, hi);
+      *reinterpret_cast<uint2 *>(out_fp4 + row * (k >> 1) + j * 8) = make_uint2(lo, hi);
+    }
+    if (swizzled) out_sf[sf_swizzled_offset(row, j, cp4)] = (uint8_t)sf;
+    else out_sf[row * cols + j] = (uint8_t)sf;
+  }
+  if (threadIdx.x == 0) row_scale[row] = __fdiv_rn(1.0f, gs);
+}
+
 // gate_up [m, 2i] bf16 ([gate | up]) -> h = silu(gate)*up (fp32) -> NVFP4
 // with swizzled scales.  Same tiling as quantize_kernel over h [m, i].  With
 // groups (blockIdx.z), group e's rows start at e * m rows of every tensor, its
@@ -180,6 +227,13 @@ cudaError_t launch_quantize(const uint16_t *x, int64_t m, int64_t k, const float
                             uint8_t *out_fp4, uint8_t *out_sf, bool swizzled, cudaStream_t st) {
   const dim3 grid((unsigned)((k / 16 + 3) / 4), (unsigned)((m + 127) / 128));
   return launch_pdl(quantize_kernel, grid, dim3(kTileThreads), 0, st, x, m, k, gs, out_fp4, out_sf, swizzled);
+}
+
+cudaError_t launch_quantize_per_token(const uint16_t *x, int64_t m, int64_t k, uint8_t *out_fp4,
+                                      uint8_t *out_sf, bool swizzled, float *row_scale, cudaStream_t st) {
+  const int64_t rows = swizzled ? (m + 127) / 128 * 128 : m;
+  return launch_pdl(quantize_per_token_kernel, dim3((unsigned)rows), dim3(256), 0, st, x, m, k, out_fp4, out_sf,
+                    swizzled, row_scale);
 }
 
 cudaError_t launch_silu_mul_quantize(const uint16_t *gate_up, int64_t m, int64_t i, const float *gs,

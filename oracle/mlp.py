@@ -44,6 +44,16 @@ def gemm_w4a4(a_packed, a_sf, b_packed, b_sf, alpha, round_bf16=True):
     return bf16_round(d) if round_bf16 else d
 
 
+def gemm_w4a4_per_token(a_packed, a_sf, a_row_scale, b_packed, b_sf, alpha, round_bf16=True):
+    """W4A4 GEMM with a per-row activation dequant factor:
+    D[m, n] = alpha * row_scale[m] * sum_k (E2M1(A)*SF_A)(E2M1(B)*SF_B)."""
+    a = dequantize_nvfp4(a_packed, a_sf)
+    b = dequantize_nvfp4(b_packed, b_sf)
+    rs = np.asarray(a_row_scale, dtype=np.float32).astype(np.float64)[:, None]
+    d = float(np.float32(alpha)) * rs * (a @ b.T)
+    return bf16_round(d) if round_bf16 else d
+
+
 def gemm_w4a16(x, b_packed, b_sf, alpha, round_bf16=True):
     """x: bf16 values as float32/float64 [M, K]."""
     b = dequantize_nvfp4(b_packed, b_sf)

@@ -85,3 +85,23 @@ def dequantize_nvfp4(packed, sf):
     rows, k = vals.shape
     scale = e4m3_decode(np.asarray(sf, dtype=np.uint8)[:, : k // BLOCK])
     return (vals.reshape(rows, k // BLOCK, BLOCK) * scale[..., None]).reshape(rows, k)
+
+
+def quantize_nvfp4_per_token(x):
+    """Per-token dynamic global scale ([P3] "关键源码片段", MoE excerpt:
+    nvfp4_quantize(..., per_token_activation=True) returns a per-token scale).
+    Reading: each row r gets its own gs_r = fp32(448 * 6 / amax(row r)) (an
+    all-zero row uses gs_r = 1) and is quantized exactly as quantize_nvfp4 with
+    it; the returned row scale fp32(1 / gs_r) is the per-row dequant factor a
+    GEMM multiplies into row r.  Returns (packed, linear sf, row_scale)."""
+    x = np.asarray(x, dtype=np.float32)
+    rows, k = x.shape
+    packed = np.empty((rows, k // 2), dtype=np.uint8)
+    sf = np.empty((rows, k // 16), dtype=np.uint8)
+    row_scale = np.empty(rows, dtype=np.float32)
+    for r in range(rows):
+        amax = np.abs(x[r]).max()
+        gs = global_scale(amax) if amax > 0 else np.float32(1.0)
+        packed[r:r + 1], sf[r:r + 1] = quantize_nvfp4(x[r:r + 1], gs)
+        row_scale[r] = np.float32(np.float32(1.0) / gs)
+    return packed, sf, row_scale

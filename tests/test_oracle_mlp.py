@@ -139,3 +139,12 @@ def test_masked_groups_reduce_to_dense_calls():
         ref = oracle.silu_mul_quant(gu[e, :valid], np.float32(20.0))
         assert np.array_equal(out[e][0], ref[0]) and np.array_equal(out[e][1], ref[1])
     assert out[2][0].shape == (0, 16)
+
+
+def test_per_token_gemm_is_row_scaled_gemm():
+    a, sa = _rand_nvfp4(4, 64, 41)
+    b, sb = _rand_nvfp4(6, 64, 42)
+    rs = np.array([0.5, 2.0, 1.0, 0.125], dtype=np.float32)
+    d = oracle.gemm_w4a4_per_token(a, sa, rs, b, sb, np.float32(0.25), round_bf16=False)
+    base = oracle.gemm_w4a4(a, sa, b, sb, np.float32(0.25), round_bf16=False)
+    assert np.array_equal(d, base * rs[:, None].astype(np.float64))

@@ -91,3 +91,34 @@ def test_unpack_inverts_packing():
     codes = g.integers(0, 16, (7, 64), dtype=np.uint8)
     packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
     assert np.array_equal(oracle.unpack_codes(packed), codes)
+
+
+def test_per_token_reduces_to_static_when_rows_share_amax():
+    """Rows with equal amax: per-token quantize equals the static quantize with
+    the shared global scale, and the row scale is its reciprocal."""
+    g = np.random.default_rng(31)
+    x = g.standard_normal((6, 128)).astype(np.float32)
+    x[:, 0] = np.float32(5.0)                 # every row's amax is exactly 5
+    x = np.clip(x, -4.5, 4.5).astype(np.float32)
+    x[:, 0] = np.float32(5.0)
+    p, s, rs = oracle.quantize_nvfp4_per_token(x)
+    gs = oracle.global_scale(5.0)
+    p2, s2 = oracle.quantize_nvfp4(x, gs)
+    assert np.array_equal(p, p2) and np.array_equal(s, s2)
+    assert np.all(rs == np.float32(np.float32(1.0) / gs))
+
+
+def test_per_token_row_independence_and_zero_rows():
+    g = np.random.default_rng(32)
+    x = g.standard_normal((5, 64)).astype(np.float32) * np.array([1, 10, 0.01, 0, 1000], np.float32)[:, None]
+    p, s, rs = oracle.quantize_nvfp4_per_token(x)
+    assert rs[3] == np.float32(1.0) and np.all(s[3] == 0)
+    assert np.all(oracle.e2m1_decode(oracle.unpack_codes(p[3:4])) == 0)   # +-0 codes
+    for r in (0, 1, 2, 4):
+        assert s[r].max() == 0x7E            # each row's own max block maps to SF 448
+        p1, s1, r1 = oracle.quantize_nvfp4_per_token(x[r:r + 1])
+        assert np.array_equal(p1[0], p[r]) and r1[0] == rs[r]
+    # dequantized rows recover x within the FP4 error
+    xd = oracle.dequantize_nvfp4(p, s) * rs[:, None].astype(np.float64)
+    for r in (0, 1, 2, 4):
+        assert np.linalg.norm(xd[r] - x[r]) <= 0.15 * np.linalg.norm(x[r])
