@@ -246,6 +246,41 @@ nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uin
                               void *workspace, size_t ws_bytes, nvfp4_algo algo,
                               nvfp4_stream_t stream);
 
+/* NVFP4_AWQ activation pre-scale ([P3] "实现拆解" item 2: in W4A16 mode the
+ * linear layer's apply keeps the AWQ pre_quant_scale multiply of x and then
+ * runs the bf16 x FP4 GEMM on the result):
+ *   out[r, c] = bf16(x[r, c] * pre_quant_scale[c])
+ * the exact product rounded once to bf16 (RNE), as a bf16 tensor multiply.
+ *   x, out bf16 [m, k] DEVICE (out may equal x);  pre_quant_scale bf16 [k].
+ * Requires k % 8 == 0 and 16-byte aligned pointers. */
+nvfp4_status bf16_awq_prescale(const uint16_t *x, const uint16_t *pre_quant_scale, uint16_t *out,
+                               int64_t m, int64_t k, nvfp4_stream_t stream);
+
+/* W4A16 GEMM on AWQ-pre-scaled activations, in one call:
+ *   d[m, n] = bf16( alpha * sum_k bf16(a[m, k] * s[k]) * (E2M1(b)*SF_b)[n, k] )
+ *   pre_quant_scale  bf16 [k] DEVICE, 16-byte aligned (s above; nullptr is
+ *                    NVFP4_ERR_INVALID_ARG, a misaligned pointer
+ *                    NVFP4_ERR_UNSUPPORTED_SHAPE).
+ *   workspace        DEVICE scratch of at least
+ *                    bf16_fp4_gemm_prescaled_workspace_bytes(m, n, k, algo)
+ *                    bytes, 16-byte aligned, no initial contents needed
+ *                    (less: NVFP4_ERR_INVALID_ARG, nothing runs).
+ *   Everything else as bf16_fp4_gemm_ex (same algo choices and shape rules).
+ * a * s is rounded once to bf16, the activation type, as the separate
+ * multiply would.  The GEMV scales each activation as it loads it (no
+ * workspace).  The tensor-core path first writes the scaled activations to
+ * the workspace with bf16_awq_prescale, then runs the W4A16 GEMM on them:
+ * scaling inside the GEMM would lengthen its converter warps, its critical
+ * path, and repeat the work for every weight tile. */
+nvfp4_status bf16_fp4_gemm_prescaled(const uint16_t *a, const uint16_t *pre_quant_scale,
+                                     const uint8_t *b_fp4, const uint8_t *b_sf, const float *alpha,
+                                     uint16_t *d, int64_t m, int64_t n, int64_t k, void *workspace,
+                                     size_t ws_bytes, nvfp4_algo algo, nvfp4_stream_t stream);
+/* Scratch bytes for bf16_fp4_gemm_prescaled: m*k*2 when it runs on the
+ * tensor cores (NVFP4_ALGO_AUTO on a supported shape, TC or TC_SWAPAB),
+ * 0 on the GEMV.  Host only, no GPU needed. */
+size_t bf16_fp4_gemm_prescaled_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo);
+
 /* Weight prep, run once at load time ([P2] modelopt_quant.py excerpt:
  * process_weights_after_loading; [P3] "实现拆解" item 2:
  * prepare_bf16_fp4_weights).  Takes the LINEAR scales (the pages snapshot the

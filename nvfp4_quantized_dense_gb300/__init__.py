@@ -42,6 +42,8 @@ _SIGS = {
     "nvfp4_gemm_swiglu_quant_ex": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
     "bf16_fp4_gemm": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
     "bf16_fp4_gemm_ex": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
+    "bf16_fp4_gemm_prescaled": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
+    "bf16_awq_prescale": [_P, _P, _P, _I64, _I64, _P],
     "nvfp4_prepare_weights": [_P, _P, _I64, _I64, _P, _P, _P],
     "nvfp4_prepare_gate_up_interleaved": [_P, _P, _I64, _I64, _P, _P, _P],
     "nvfp4_gemm_decode_noalloc": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
@@ -49,7 +51,7 @@ _SIGS = {
     "nvfp4_set_wait_limit": [ctypes.c_uint32],
 }
 EXPORTS = sorted(list(_SIGS) + ["nvfp4_status_string", "nvfp4_version", "nvfp4_sf_bytes",
-                                "nvfp4_workspace_bytes"])
+                                "nvfp4_workspace_bytes", "bf16_fp4_gemm_prescaled_workspace_bytes"])
 
 
 def load(path=LIB_PATH):
@@ -68,6 +70,8 @@ def load(path=LIB_PATH):
     lib.nvfp4_version.argtypes, lib.nvfp4_version.restype = [], _I
     lib.nvfp4_sf_bytes.argtypes, lib.nvfp4_sf_bytes.restype = [_I64, _I64, _I], _SZ
     lib.nvfp4_workspace_bytes.argtypes, lib.nvfp4_workspace_bytes.restype = [_I64, _I64, _I64, _I], _SZ
+    lib.bf16_fp4_gemm_prescaled_workspace_bytes.argtypes = [_I64, _I64, _I64, _I]
+    lib.bf16_fp4_gemm_prescaled_workspace_bytes.restype = _SZ
     _lib = lib
     return lib
 
@@ -109,6 +113,14 @@ def nvfp4_sf_bytes(rows, k, layout=SF_SWIZZLED_128x4):
 
 def nvfp4_workspace_bytes(m, n, k, algo=ALGO_AUTO):
     return load().nvfp4_workspace_bytes(m, n, k, algo)
+
+
+def bf16_fp4_gemm_prescaled_workspace_bytes(m, n, k, algo=ALGO_AUTO):
+    return load().bf16_fp4_gemm_prescaled_workspace_bytes(m, n, k, algo)
+
+
+def bf16_awq_prescale(x, pre_quant_scale, out, m, k, stream=None):
+    _call("bf16_awq_prescale", _ptr(x), _ptr(pre_quant_scale), _ptr(out), m, k, _stream(stream))
 
 
 def nvfp4_quantize(x, m, k, global_scale, out_fp4, out_sf, sf_layout=SF_SWIZZLED_128x4, stream=None):
@@ -185,6 +197,12 @@ def bf16_fp4_gemm_ex(a, b_fp4, b_sf, alpha, d, m, n, k, workspace=None, ws_bytes
                      stream=None):
     _call("bf16_fp4_gemm_ex", _ptr(a), _ptr(b_fp4), _ptr(b_sf), _ptr(alpha), _ptr(d), m, n, k,
           _ptr(workspace), ws_bytes, algo, _stream(stream))
+
+
+def bf16_fp4_gemm_prescaled(a, pre_quant_scale, b_fp4, b_sf, alpha, d, m, n, k, workspace=None, ws_bytes=0,
+                            algo=ALGO_AUTO, stream=None):
+    _call("bf16_fp4_gemm_prescaled", _ptr(a), _ptr(pre_quant_scale), _ptr(b_fp4), _ptr(b_sf), _ptr(alpha),
+          _ptr(d), m, n, k, _ptr(workspace), ws_bytes, algo, _stream(stream))
 
 
 def nvfp4_prepare_weights(w_fp4, sf_linear, n, k, w_out, sf_out, stream=None):

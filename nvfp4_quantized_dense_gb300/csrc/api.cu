@@ -269,13 +269,17 @@ nvfp4_status nvfp4_gemm_swiglu_quant(const uint8_t *a_fp4, const uint8_t *a_sf,
                                     NVFP4_ALGO_AUTO, stream);
 }
 
-nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
-                              const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
-                              void *, size_t, nvfp4_algo algo, nvfp4_stream_t stream) {
+}  // extern "C"
+
+namespace {
+nvfp4_status w4a16_impl(const uint16_t *a, const uint16_t *pre_scale, const uint8_t *b_fp4, const uint8_t *b_sf,
+                        const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k, void *workspace,
+                        size_t ws_bytes, nvfp4_algo algo, nvfp4_stream_t stream) {
   if (!a || !b_fp4 || !b_sf || !alpha || !d) return NVFP4_ERR_INVALID_ARG;
   if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
   if (!aligned16(a) || !aligned16(b_fp4) || !aligned16(b_sf) || !aligned16(d))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (pre_scale && !aligned16(pre_scale)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
   if (nvfp4_status s = check_arch()) return s;
   if (m == 0) return NVFP4_OK;
@@ -286,9 +290,53 @@ nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uin
     algo = w4a16_tc_supported(m, n, k) ? NVFP4_ALGO_TC : NVFP4_ALGO_GEMV;
   if (algo == NVFP4_ALGO_GEMV)
     return from_cuda(launch_gemv(GEMV_W4A16, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
-                                 nullptr, m, n, k, st));
+                                 nullptr, m, n, k, st, nullptr, pre_scale));
   if (!w4a16_tc_supported(m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (pre_scale) {
+    // The tensor-core kernel's converter warps are its critical path, and
+    // every weight tile reads the same activations: scale them once, into the
+    // workspace, in a pass of their own.
+    if (!workspace || ws_bytes < (size_t)(m * k * 2)) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    uint16_t *xs = static_cast<uint16_t *>(workspace);
+    if (cudaError_t e = launch_awq_prescale(a, pre_scale, m, k, xs, st)) return from_cuda(e);
+    a = xs;
+  }
   return from_cuda(launch_w4a16_tc(a, b_fp4, b_sf, alpha, d, m, n, k, g_wait_limit.load(), st));
+}
+}  // namespace
+
+extern "C" {
+
+nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
+                              const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
+                              void *, size_t, nvfp4_algo algo, nvfp4_stream_t stream) {
+  return w4a16_impl(a, nullptr, b_fp4, b_sf, alpha, d, m, n, k, nullptr, 0, algo, stream);
+}
+
+nvfp4_status bf16_fp4_gemm_prescaled(const uint16_t *a, const uint16_t *pre_quant_scale,
+                                     const uint8_t *b_fp4, const uint8_t *b_sf, const float *alpha,
+                                     uint16_t *d, int64_t m, int64_t n, int64_t k, void *workspace,
+                                     size_t ws_bytes, nvfp4_algo algo, nvfp4_stream_t stream) {
+  if (!pre_quant_scale) return NVFP4_ERR_INVALID_ARG;
+  return w4a16_impl(a, pre_quant_scale, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes, algo, stream);
+}
+
+size_t bf16_fp4_gemm_prescaled_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo) {
+  if (m <= 0 || n <= 0 || k <= 0 || algo == NVFP4_ALGO_GEMV) return 0;
+  if (m > (int64_t(1) << 31) || k > (int64_t(1) << 31)) return 0;
+  if (algo == NVFP4_ALGO_AUTO && !w4a16_tc_supported(m, n, k)) return 0;
+  return (size_t)(m * k * 2);
+}
+
+nvfp4_status bf16_awq_prescale(const uint16_t *x, const uint16_t *pre_quant_scale, uint16_t *out, int64_t m,
+                               int64_t k, nvfp4_stream_t stream) {
+  if (!x || !pre_quant_scale || !out || m < 0 || k <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (k % 8 != 0 || !aligned16(x) || !aligned16(pre_quant_scale) || !aligned16(out))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  return from_cuda(launch_awq_prescale(x, pre_quant_scale, m, k, out, (cudaStream_t)stream));
 }
 
 nvfp4_status bf16_fp4_gemm(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,

@@ -93,6 +93,14 @@ __device__ __forceinline__ float silu_mul_fast(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
+// bf16x2 * bf16x2 rounded once to bf16x2: the fp32 product of two bf16
+// values is exact, so this is the correctly rounded bf16 product.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t x, uint32_t s) {
+  const __nv_bfloat162 r =
+      __floats2bfloat162_rn(__fmul_rn(bf16_lo(x), bf16_lo(s)), __fmul_rn(bf16_hi(x), bf16_hi(s)));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // silu(g) * u in fp32 with an IEEE division.
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);

@@ -1,21 +1,23 @@
 // tcgen05 tensor-core GEMMs: NVFP4 block-scaled MMA (E2M1 x E2M1, UE4M3 per
 // 16 elements), accumulators in TMEM.
 //
-// Kernel shape (one CTA per SM, persistent over output tiles):
+// Kernel shape (clusters of two CTAs, one CTA per SM, persistent over output
+// tiles; the roles are listed at the kernel):
 //   warp 0      TMA producer: A/B code tiles (2-D tensor maps, 128-byte
 //               swizzle) and the matching 512-byte tiles of the swizzled
-//               block scales (1-D bulk copies), one mbarrier per stage;
-//   warp 1      allocates TMEM; one elected thread copies each stage's
-//               scales into TMEM (tcgen05.cp) and issues the MMAs, then
-//               commits the stage back to the producer;
+//               block scales (1-D bulk copies), one mbarrier per stage; the
+//               weight half-tiles are multicast to both CTAs of the cluster;
+//   warp 1      allocates TMEM; one elected thread issues the MMAs and
+//               commits each stage back to both producers;
+//   warps 10-13 write each stage's block scales into TMEM (tcgen05.st);
 //   warps 2..9  epilogue: TMEM -> registers (tcgen05.ld), TMEM released at
 //               once, then bf16 output or the fused SwiGLU + NVFP4 requantize
 //               of the gate_up GEMM while the next tile's MMAs run.
-// Tile 128 (M) x 256 (N) x 256 (K); one MMA instruction covers K = 64, so a
-// stage holds four.  Every mbarrier wait is bounded: a wait that gives up
-// records NVFP4_ERR_DEVICE_TIMEOUT, every role leaves its loop, outstanding
-// copies and MMAs are drained with a second bounded wait, TMEM is freed and
-// the kernel returns.
+// Tile 128 (M) x 256 (N) x 256 (K) per CTA; one MMA instruction covers K =
+// 64, so a stage holds four.  Every mbarrier wait is bounded: a wait that
+// gives up records NVFP4_ERR_DEVICE_TIMEOUT, every role leaves its loop,
+// outstanding copies and MMAs are drained with a second bounded wait, TMEM is
+// freed and the kernel returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -60,7 +62,7 @@ constexpr uint32_t SFA_BYTES = (BM / 128) * KSTEPS * 512;
 constexpr uint32_t SFB_BYTES = (BN / 128) * KSTEPS * 512;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int kThreads = 352;           // producer, MMA, 8 epilogue warps, scale-copy warp
+constexpr int kThreads = 448;           // producer, MMA, 8 epilogue warps, 4 scale-writer warps
 constexpr int kCluster = 2;             // CTAs sharing one weight tile
 constexpr uint16_t kPairMask = 0x3;
 constexpr uint32_t TMEM_COLS = 512;
@@ -128,8 +130,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // empty barriers).  Roles per CTA:
 //   warp 0      TMA producer;
 //   warp 1      TMEM owner, single-thread MMA issuer;
-//   warp 10     copies each stage's block scales into one of two TMEM scale
-//               slots (tcgen05.cp) ahead of the MMAs;
+//   warps 10-13 write each stage's block scales into one of two TMEM scale
+//               slots (tcgen05.st, one warp per lane quarter) ahead of the MMAs;
 //   warps 2..9  epilogue: TMEM -> registers, TMEM released at once, then bf16
 //               output or the fused SwiGLU + NVFP4 requantize.
 template <int MODE>  // TC_W4A4: bf16 out; TC_W4A4_SWIGLU: fused SwiGLU + NVFP4 requant
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(sm.tempty(), 256);
     ptx::mbar_init(sm.drain(), 1);
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&sm.sf_full()[b], 1);
+      ptx::mbar_init(&sm.sf_full()[b], 4);     // one arrival per scale-writer warp
       ptx::mbar_init(&sm.sf_empty()[b], 1);
     }
     *abort_flag = 0;
@@ -284,41 +286,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit(sm.tfull());
       }
     }
-  } else if (warp == 10) {
-    // --------------------------------------------------------- scale copies
+  } else if (warp >= 10) {
+    // ------------------------------------------------------ scale writers
+    // Warp w fills TMEM lane quarter w % 4 (a warp reaches only its own
+    // quarter) of the stage's scale slot from registers with tcgen05.st: the
+    // same 4 columns x 32 lanes per 512-byte scale tile that a warpx4 copy
+    // of the tile would write, replicated in every quarter.  These stores
+    // do not queue behind the MMAs in the tensor pipe as tcgen05.cp does.
     pdl_wait();
-    if (ptx::elect_one()) {
-      int s = 0, g = 0;
-      uint32_t ph = 0;
-      for (int pair = cluster; pair < num_pairs && !*abort_flag; pair += num_clusters) {
-        int mt, nt;
-        tile_of(pair, mt, nt);
-        const int nbv = min(2, nrb_b - nt * 2);
-        bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb, ++g) {
-          const int slot = g & 1;
-          if (!ptx::mbar_wait_bounded(&sm.sf_empty()[slot], (uint32_t)((g >> 1) & 1) ^ 1u, limit,
-                                      kDefaultTimeoutNs, abort_flag) ||
-              !ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
-            give_up(abort_flag, p.status);
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
-          const uint32_t sf = tmem + SF_COL + slot * SF_SLOT;
-          const uint32_t sfa_s = ptx::smem_u32(sm.sfa(s)), sfb_s = ptx::smem_u32(sm.sfb(s));
-          for (int j = 0; j < nk; ++j) {
-            ptx::tmem_cp_32x128b_x4(sf + 4 * j, ptx::smem_desc(sfa_s + 512 * j, 0, 128, 0));
-            for (int rb = 0; rb < nbv; ++rb)
-              ptx::tmem_cp_32x128b_x4(sf + SFB_OFF + 8 * j + 4 * rb,
-                                      ptx::smem_desc(sfb_s + rb * (KSTEPS * 512) + 512 * j, 0, 128, 0));
-          }
-          ptx::tc_commit(&sm.sf_full()[slot]);
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    int s = 0, g = 0;
+    uint32_t ph = 0;
+    for (int pair = cluster; pair < num_pairs && !*abort_flag; pair += num_clusters) {
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; ++kb, ++g) {
+        const int slot = g & 1;
+        if (!ptx::mbar_wait_bounded(&sm.sf_empty()[slot], (uint32_t)((g >> 1) & 1) ^ 1u, limit,
+                                    kDefaultTimeoutNs, abort_flag) ||
+            !ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
+          give_up(abort_flag, p.status);
+          ok = false;
+          break;
         }
-        if (!ok) break;
+        ptx::tc_fence_after();
+        // lane l takes bytes 16l .. 16l+15 of every scale tile of the stage
+        // (rows l, l+32, l+64, l+96; 4 scales each).  Tiles past the K tail
+        // or the last weight block hold stale bytes the MMAs never use.
+        const uint8_t *sfa = sm.sfa(s) + lane * 16, *sfb = sm.sfb(s) + lane * 16;
+        uint32_t ra[16], rb0[16], rb1[16];
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(sfa + 512 * j);
+          ra[4 * j] = v.x; ra[4 * j + 1] = v.y; ra[4 * j + 2] = v.z; ra[4 * j + 3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < KSTEPS; ++j)
+#pragma unroll
+          for (int rb = 0; rb < 2; ++rb) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(sfb + rb * (KSTEPS * 512) + 512 * j);
+            uint32_t *d = (j < 2 ? rb0 : rb1) + 8 * (j & 1) + 4 * rb;   // column 8j + 4rb of the SFB slot
+            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+          }
+        const uint32_t sf = tmem + lane_off + SF_COL + slot * SF_SLOT;
+        ptx::tmem_st16(sf, ra);
+        ptx::tmem_st16(sf + SFB_OFF, rb0);
+        ptx::tmem_st16(sf + SFB_OFF + 16, rb1);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.sf_full()[slot]);
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
       }
+      if (!ok) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue

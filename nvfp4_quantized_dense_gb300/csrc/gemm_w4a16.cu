@@ -166,11 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pend_s[STAGES], pend_kb[STAGES], pend_tt[STAGES];
       int npend = 0, c = 0;
       bool flushed = false;
+      auto load_x = [&](int st, int kb, int tt) {
+        ptx::tma_load_2d(st_x(st), &tm_x, &full[st], kb * (BK * 2), tt * NT, pol_x);
+      };
       auto flush = [&]() {
         pdl_wait();
-        for (int i = 0; i < npend; ++i)
-          ptx::tma_load_2d(st_x(pend_s[i]), &tm_x, &full[pend_s[i]], pend_kb[i] * (BK * 2), pend_tt[i] * NT,
-                           pol_x);
+        for (int i = 0; i < npend; ++i) load_x(pend_s[i], pend_kb[i], pend_tt[i]);
         flushed = true;
       };
       for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pend_tt[npend] = tt;
             ++npend;
           } else {
-            ptx::tma_load_2d(st_x(s), &tm_x, &full[s], kb * (BK * 2), tt * NT, pol_x);
+            load_x(s, kb, tt);
           }
           issued_mask |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (ph << s);

@@ -107,6 +107,7 @@ struct GemvArgs {
   int64_t m, n, k;
   int64_t m0;          // first token of this pass
   const float *rs;     // optional per-token dequant factor [M]
+  const uint16_t *pqs; // W4A16: optional AWQ pre_quant_scale, bf16 [K]
 };
 
 // Weight row handled by warp `w`, sub-row `r` of CTA `cta`.  Plain mode: rows
@@ -273,6 +274,15 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_w4a16_kernel(GemvArgs p) {
       wf[2 * i + 1] = __high2float(v);
     }
     const float s0 = e4m3_decode(wsf & 0xFF), s1 = e4m3_decode((wsf >> 8) & 0xFF);
+    uint32_t pw[16];                 // AWQ pre-scale of these 32 channels (bf16 pairs)
+    if (p.pqs) {
+      const uint4 *sp = reinterpret_cast<const uint4 *>(p.pqs + c * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = __ldg(sp + q);
+        pw[4 * q] = v.x; pw[4 * q + 1] = v.y; pw[4 * q + 2] = v.z; pw[4 * q + 3] = v.w;
+      }
+    }
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       if (t < mt) {
@@ -286,8 +296,13 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_w4a16_kernel(GemvArgs p) {
           for (int e = 0; e < 4; ++e) {
             const int idx = q * 8 + e * 2;
             float &bs = (idx < 16) ? b0 : b1;
-            bs = fmaf(bf16_lo(w4[e]), wf[idx], bs);
-            bs = fmaf(bf16_hi(w4[e]), wf[idx + 1], bs);
+            float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
+            if (p.pqs) {             // bf16(x * s): the fp32 product is exact, one rounding
+              x0 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(x0, bf16_lo(pw[4 * q + e]))));
+              x1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(x1, bf16_hi(pw[4 * q + e]))));
+            }
+            bs = fmaf(x0, wf[idx], bs);
+            bs = fmaf(x1, wf[idx + 1], bs);
           }
         }
         acc[t] = fmaf(b0, s0, acc[t]);
@@ -325,9 +340,9 @@ cudaError_t launch_mt(GemvMode mode, const GemvArgs &a, cudaStream_t st) {
 cudaError_t launch_gemv(GemvMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,
                         const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
                         uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
-                        cudaStream_t st, const float *a_row_scale) {
+                        cudaStream_t st, const float *a_row_scale, const uint16_t *pre_scale) {
   GemvArgs args{static_cast<const uint8_t *>(a), a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf,
-                m, n, k, 0, a_row_scale};
+                m, n, k, 0, a_row_scale, pre_scale};
   // passes of 16, 8, 4, 2 or 1 tokens until every token is covered
   for (int64_t m0 = 0; m0 < m;) {
     const int64_t left = m - m0;

@@ -38,6 +38,9 @@ cudaError_t launch_silu_mul_quantize_masked(const uint16_t *gate_up, const int32
                                             uint8_t *out_sf, cudaStream_t st);
 cudaError_t launch_silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
                                  cudaStream_t st);
+// out [m, k] = bf16(x * s[k]) (AWQ pre-scale); k % 8 == 0, 16-byte aligned.
+cudaError_t launch_awq_prescale(const uint16_t *x, const uint16_t *s, int64_t m, int64_t k, uint16_t *out,
+                                cudaStream_t st);
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf_lin, int64_t n, int64_t k,
                            uint8_t *w_out, uint8_t *sf_out, bool interleave, cudaStream_t st);
 
@@ -45,10 +48,13 @@ cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf_lin, int64_t n, i
 enum GemvMode { GEMV_W4A4 = 0, GEMV_W4A4_SWIGLU = 1, GEMV_W4A16 = 2 };
 // a_row_scale (optional, fp32 [m]): per-row activation dequant factor that
 // multiplies alpha (per-token activation scales); nullptr for none.
+// pre_scale (optional, GEMV_W4A16 only, bf16 [k]): AWQ per-channel activation
+// scale, the product rounded to bf16 before it meets the weight.
 cudaError_t launch_gemv(GemvMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,
                         const uint8_t *b_sf, const float *alpha, const float *out_gs, uint16_t *d,
                         uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
-                        cudaStream_t st, const float *a_row_scale = nullptr);
+                        cudaStream_t st, const float *a_row_scale = nullptr,
+                        const uint16_t *pre_scale = nullptr);
 
 // tcgen05 tensor-core family.
 enum TcMode { TC_W4A4 = 0, TC_W4A4_SWIGLU = 1, TC_W4A16 = 2 };

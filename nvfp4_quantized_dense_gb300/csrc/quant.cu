@@ -167,6 +167,29 @@ __global__ void __launch_bounds__(256) silu_mul_bf16_kernel(const uint16_t *__re
   }
 }
 
+// NVFP4_AWQ activation pre-scale: out[r, c] = bf16(x[r, c] * s[c]); the fp32
+// product of two bf16 values is exact, so the result is rounded once.  Eight
+// elements per thread, grid-stride.
+__global__ void __launch_bounds__(256) awq_prescale_kernel(const uint16_t *__restrict__ x,
+                                                           const uint16_t *__restrict__ s, int64_t m,
+                                                           int64_t k, uint16_t *__restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t per_row = k >> 3;
+  const int64_t total = m * per_row;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = idx / per_row, c8 = idx - row * per_row;
+    const uint4 xv = __ldcs(reinterpret_cast<const uint4 *>(x + row * k + c8 * 8));
+    const uint4 sv = __ldg(reinterpret_cast<const uint4 *>(s + c8 * 8));
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, sw[4] = {sv.x, sv.y, sv.z, sv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(xw[i], sw[i]);
+    *reinterpret_cast<uint4 *>(out + row * k + c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // Output row -> source row of the gate/up interleave: blocks of 128 rows are
 // [up 64b..64b+63 ; gate 64b..64b+63], with [gate; up] source rows.
 __device__ __forceinline__ int64_t interleave_src(int64_t o, int64_t n) {
@@ -256,6 +279,11 @@ cudaError_t launch_silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, 
                                  cudaStream_t st) {
   return launch_pdl(silu_mul_bf16_kernel, dim3(grid_for(m * (i / 8), 256)), dim3(256), 0, st, gate_up, m, i,
                     out);
+}
+
+cudaError_t launch_awq_prescale(const uint16_t *x, const uint16_t *s, int64_t m, int64_t k, uint16_t *out,
+                                cudaStream_t st) {
+  return launch_pdl(awq_prescale_kernel, dim3(grid_for(m * (k / 8), 256)), dim3(256), 0, st, x, s, m, k, out);
 }
 
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf_lin, int64_t n, int64_t k,

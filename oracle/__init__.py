@@ -32,7 +32,7 @@ from .formats import (E2M1_MAGNITUDES, e2m1_decode, e2m1_encode, e4m3_decode,
 from .quant import quantize_nvfp4, quantize_nvfp4_per_token, dequantize_nvfp4, unpack_codes, global_scale
 from .layouts import (sf_swizzle_128x4, sf_unswizzle_128x4, sf_swizzled_bytes,
                       interleave_gate_up, interleave_gate_up_scales_then_swizzle)
-from .mlp import (gemm_w4a4, gemm_w4a4_per_token, gemm_w4a16, silu, swiglu_h, silu_mul_quant, silu_mul_quant_masked,
+from .mlp import (gemm_w4a4, gemm_w4a4_per_token, gemm_w4a16, awq_prescale, gemm_w4a16_prescaled, silu, swiglu_h, silu_mul_quant, silu_mul_quant_masked,
                   silu_mul_bf16, gemm_swiglu_quant, mlp_w4a4_fused, mlp_w4a4_unfused,
                   mlp_w4a16)
 

@@ -11,6 +11,10 @@ W4A16 GEMM ([P3] "关键源码片段", fp4_gemm with quant_mode "w4a16";
 "实现拆解" item 3: alpha holds only the weight dequant factor):
     D[m, n] = alpha * sum_k x[m, k] * (E2M1(B)*SF_B)[n, k], alpha = 1/gs_b.
 
+NVFP4_AWQ pre-scale ([P3] "实现拆解" item 2: in W4A16 mode apply keeps the
+AWQ pre_quant_scale multiply): x' = bf16(x[m, k] * s[k]), one rounding of the
+exact product, then the W4A16 GEMM on x'.
+
 SwiGLU ([P2] "实现拆解" item 1: gate_up GEMM -> silu -> FP4 quantize;
 [P2] "关键源码片段": gate_up rows are [gate; up]):
     g = D[:, :I], u = D[:, I:] taken in float64 *before* bf16 rounding,
@@ -27,7 +31,8 @@ once to bf16 from float64.
 Pins (tests/test_oracle_mlp.py): brute-force triple loops on tiny shapes,
 exact integer results with power-of-two scales, silu closed forms
 (silu(0)=0, silu(x)-silu(-x)=x, limits), the fused == unfused invariant, and
-W4A16 == W4A4 when x is exactly representable.  The whole-MLP numbers have no
+W4A16 == W4A4 when x is exactly representable, hand-worked bf16 products of
+the AWQ pre-scale and agreement with ml_dtypes' bf16 multiply.  The whole-MLP numbers have no
 external implementation to compare against: parity unpinned beyond these.
 """
 import numpy as np
@@ -59,6 +64,23 @@ def gemm_w4a16(x, b_packed, b_sf, alpha, round_bf16=True):
     b = dequantize_nvfp4(b_packed, b_sf)
     d = float(np.float32(alpha)) * (np.asarray(x, dtype=np.float64) @ b.T)
     return bf16_round(d) if round_bf16 else d
+
+
+def awq_prescale(x, pre_quant_scale):
+    """NVFP4_AWQ activation pre-scale ([P3] "实现拆解" item 2: the W4A16 branch
+    of the linear layer's apply multiplies x by the per-input-channel
+    pre_quant_scale before the bf16 x FP4 GEMM).  Both are bf16 values; the
+    product is taken in the activation type, i.e. the exact product rounded
+    once to bf16 (exact in double: 8 x 8 significant bits).
+    x [M, K], pre_quant_scale [K] -> [M, K] bf16 values as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    s = np.asarray(pre_quant_scale, dtype=np.float64).reshape(1, -1)
+    return bf16_round(x * s)
+
+
+def gemm_w4a16_prescaled(x, pre_quant_scale, b_packed, b_sf, alpha, round_bf16=True):
+    """W4A16 GEMM on the AWQ-pre-scaled activations ([P3] "实现拆解" item 2)."""
+    return gemm_w4a16(awq_prescale(x, pre_quant_scale), b_packed, b_sf, alpha, round_bf16)
 
 
 def silu(g):

@@ -43,7 +43,7 @@ WORKLOADS = {
     4: Workload(4, "W4A16 dense MLP (H5120 I17408)", 5120, 17408, (1, 16, 128, 1024), "w4a16"),
 }
 
-T_X, T_WGU, T_WDOWN, T_OUTLIER = 0, 1, 2, 3
+T_X, T_WGU, T_WDOWN, T_OUTLIER, T_AWQ = 0, 1, 2, 3, 4
 
 # Workloads with the same MLP shape draw the same weights: the prefill
 # workload reuses the DeepSeek-V3-shaped decode weights and the W4A16 workload
@@ -86,6 +86,16 @@ def weight(wid, which, rows=None, cols=None, seed=SEED):
         raise ValueError(which)
     shape = (rows or shape[0], cols or shape[1])
     return (rng(wid, tid, seed).standard_normal(shape, dtype=np.float32) * np.float32(0.02)).astype(np.float32)
+
+
+def awq_pre_quant_scale(wid, k=None, seed=SEED):
+    """Per-input-channel AWQ activation scales, bf16 [k] as (bits, values):
+    positive, log-uniform over [1/4, 4] (AWQ scales are positive factors near
+    1 that grow on the channels with large activations)."""
+    w = WORKLOADS[wid]
+    k = w.hidden if k is None else k
+    e = rng(wid, T_AWQ, seed).uniform(-2.0, 2.0, k)
+    return to_bf16_bits(np.exp2(e).astype(np.float32))
 
 
 def random_matrix(shape, seed_key, scale=1.0, dtype=np.float32):

@@ -106,3 +106,19 @@ def test_missing_library_raises(tmp_path):
             nv.load(str(tmp_path / "missing.so"))
     finally:
         nv._lib = saved
+
+
+def test_awq_prescale_host_checks(lib):
+    # workspace: m*k bf16 on the tensor cores, none on the GEMV
+    assert nv.bf16_fp4_gemm_prescaled_workspace_bytes(1, 256, 512) == 512 * 2
+    assert nv.bf16_fp4_gemm_prescaled_workspace_bytes(65, 256, 512) == 65 * 512 * 2
+    assert nv.bf16_fp4_gemm_prescaled_workspace_bytes(0, 256, 512) == 0
+    assert nv.bf16_fp4_gemm_prescaled_workspace_bytes(1024, 34816, 5120, nv.ALGO_TC) == 1024 * 5120 * 2
+    assert nv.bf16_fp4_gemm_prescaled_workspace_bytes(1024, 34816, 5120, nv.ALGO_GEMV) == 0
+    assert lib.bf16_awq_prescale(None, FAKE, FAKE, 4, 256, None) == nv.ERR_INVALID_ARG
+    assert lib.bf16_awq_prescale(FAKE, FAKE, FAKE, 4, 100, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.bf16_awq_prescale(FAKE, FAKE + 2, FAKE, 4, 256, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.bf16_fp4_gemm_prescaled(FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None, 0, 0,
+                                       None) == nv.ERR_INVALID_ARG
+    assert lib.bf16_fp4_gemm_prescaled(FAKE, FAKE + 8, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None, 0, 0,
+                                       None) == nv.ERR_UNSUPPORTED_SHAPE

@@ -148,3 +148,43 @@ def test_per_token_gemm_is_row_scaled_gemm():
     d = oracle.gemm_w4a4_per_token(a, sa, rs, b, sb, np.float32(0.25), round_bf16=False)
     base = oracle.gemm_w4a4(a, sa, b, sb, np.float32(0.25), round_bf16=False)
     assert np.array_equal(d, base * rs[:, None].astype(np.float64))
+
+
+def test_awq_prescale_hand_worked_roundings():
+    # bf16 keeps 7 fraction bits; each product below was worked by hand
+    cases = [
+        (1.0078125, 1.5, 1.515625),         # 1.51171875 lies halfway: ties to the even 1.515625
+        (1.0078125, 1.0078125, 1.015625),   # 1 + 2^-6 + 2^-14: the 2^-14 is below half an ulp
+        (-3.0, 0.5, -1.5),
+        (0.0, -2.0, -0.0),
+        (1.5 * 2.0 ** 127, 2.0, math.inf),  # past the largest bf16: overflows
+        (2.0 ** -130, 0.5, 2.0 ** -131),    # subnormal, exact
+    ]
+    for x, s, want in cases:
+        got = oracle.awq_prescale([[x]], [s])[0, 0]
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), (x, s, got)
+
+
+def test_awq_prescale_matches_library_bf16_multiply():
+    g = np.random.default_rng(51)
+    x = g.standard_normal((7, 96)).astype(ml_dtypes.bfloat16)
+    s = g.uniform(0.05, 8.0, 96).astype(ml_dtypes.bfloat16)
+    want = (x * s[None, :]).astype(np.float64)     # float32 product, one rounding to bf16
+    got = oracle.awq_prescale(x.astype(np.float64), s.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_prescaled_w4a16_brute_force():
+    # the scale runs along K (input channels), not along M or N
+    g = np.random.default_rng(52)
+    m, n, k = 3, 5, 48
+    x = g.standard_normal((m, k)).astype(ml_dtypes.bfloat16)
+    s = g.uniform(0.1, 3.0, k).astype(ml_dtypes.bfloat16)
+    b, sb = _rand_nvfp4(n, k, 53)
+    d = oracle.gemm_w4a16_prescaled(x.astype(np.float64), s.astype(np.float64), b, sb, np.float32(0.5),
+                                    round_bf16=False)
+    bv = _lib_decode(b, sb)
+    for i in range(m):
+        for j in range(n):
+            acc = sum(float(x[i, t] * s[t]) * bv[j, t] for t in range(k))
+            assert d[i, j] == pytest.approx(0.5 * acc, rel=1e-12, abs=1e-12)
