@@ -91,6 +91,7 @@ struct TcArgs {
   uint32_t wait_limit;
   int *status;            // device status word
   const float *rs;        // optional per-row activation dequant factor [M]
+  int32_t group_mp;       // tile order: m-pairs per group (see tile_of)
 };
 
 struct Smem {
@@ -178,9 +179,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cp4 = ksteps_total;                   // 512-byte scale tiles per 128-row block
   const int nrb_b = (p.n + 127) >> 7;             // 128-row blocks of B
   const uint32_t limit = p.wait_limit;
+  // Work order: groups of group_mp m-pairs; within a group the m-pair runs
+  // fastest, then the weight tile.  The clusters running at one time then
+  // share a bounded set of activation rows (kept in L2 across the group's
+  // sweep over the weights), and every weight tile is read once per group.
   auto tile_of = [&](int pair, int &mt, int &nt) {
-    nt = pair / p.num_mpairs;
-    mt = (pair - nt * p.num_mpairs) * kCluster + rank;
+    const int per_group = p.group_mp * p.num_n;
+    const int g = pair / per_group;
+    const int r = pair - g * per_group;
+    const int gsz = min(p.group_mp, p.num_mpairs - g * p.group_mp);
+    nt = r / gsz;
+    mt = (g * p.group_mp + (r - nt * gsz)) * kCluster + rank;
   };
 
   uint32_t issued_mask = 0, issued_parity = 0;
@@ -529,6 +538,14 @@ cudaError_t launch_mode(const uint8_t *a, const uint8_t *a_sf, const uint8_t *b,
               (int32_t)((m + BM - 1) / BM), (int32_t)((n + BN - 1) / BN), 0, wait_limit, device_status_ptr(), rs};
   if (!args.status) return cudaErrorInvalidValue;
   args.num_mpairs = (args.num_m + kCluster - 1) / kCluster;
+  {
+    // Activation rows of one group: at most ~32 MiB, so that, together with
+    // the weight tiles in flight (and any copies the two dies' L2 halves
+    // keep), they stay in the 129 MB L2 while the group sweeps the weights.
+    const int64_t pair_bytes = (int64_t)kCluster * BM * (k / 2);
+    const int64_t g = (int64_t(32) << 20) / pair_bytes;
+    args.group_mp = (int32_t)(g < 1 ? 1 : g > args.num_mpairs ? args.num_mpairs : g);
+  }
   const int pairs = args.num_mpairs * args.num_n;
   const int clusters = pairs < max_clusters[dev] ? pairs : max_clusters[dev];
   cfg.gridDim = dim3(kCluster * clusters);
