@@ -281,6 +281,51 @@ nvfp4_status bf16_fp4_gemm_prescaled(const uint16_t *a, const uint16_t *pre_quan
  * 0 on the GEMV.  Host only, no GPU needed. */
 size_t bf16_fp4_gemm_prescaled_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo);
 
+/* The whole decode MLP in one kernel launch: nvfp4_quantize of x, the gate_up
+ * GEMM with the SwiGLU + NVFP4 requantize epilogue, and the down_proj GEMM
+ * ([P1] "关键源码片段": quantize -> gate_up -> silu_mul_nvfp4_quantize ->
+ * down_proj; [P2] "实现拆解" item 1: the fused gate_up + SwiGLU + FP4
+ * quantize).  One CTA per SM streams its share of the gate_up weights and
+ * then of the down_proj weights with no pause between the steps; the steps
+ * that depend on each other meet at grid-wide counters in the workspace.
+ *   x                bf16 [m, hidden]
+ *   x_global_scale   fp32 [1] DEVICE (gs of x, as nvfp4_quantize)
+ *   w_gate_up_int(_sf)  the gate/up-interleaved weight [2*inter, hidden/2]
+ *                    and its swizzled scales (nvfp4_prepare_gate_up_interleaved)
+ *   alpha_gate_up    fp32 [1] = 1/(gs_x * gs_w_gate_up)
+ *   h_global_scale   fp32 [1]: static input scale of down_proj
+ *   w_down(_sf)      [hidden, inter/2] and swizzled scales (nvfp4_prepare_weights)
+ *   alpha_down       fp32 [1] = 1/(gs_h * gs_w_down)
+ *   x_fp4, x_sf      OUT: quantized x, exactly as nvfp4_quantize (swizzled
+ *                    scales, nvfp4_sf_bytes(m, hidden) bytes)
+ *   h_fp4, h_sf      OUT: NVFP4 h [m, inter/2] + swizzled scales
+ *                    (nvfp4_sf_bytes(m, inter) bytes)
+ *   out              OUT: bf16 [m, hidden]
+ *   round_gate_up_bf16  1: the gate_up result is rounded to bf16 before
+ *                    SwiGLU, as nvfp4_gemm followed by silu_mul_nvfp4_quantize
+ *                    computes it; 0: SwiGLU on the fp32 accumulators, as
+ *                    nvfp4_gemm_swiglu_quant.
+ *   workspace        DEVICE, >= nvfp4_mlp_decode_workspace_bytes(m, hidden,
+ *                    inter), zero-filled once before first use; every
+ *                    complete call leaves its counters at zero again.  Calls
+ *                    sharing a workspace must not run concurrently.  After
+ *                    NVFP4_ERR_DEVICE_TIMEOUT zero-fill it again.
+ * Requires 1 <= m <= 64 (m == 0 is a no-op), hidden % 128 == 0,
+ * inter % 64 == 0, 16-byte aligned buffers.  The kernel's CTAs wait on each
+ * other: it is launched with at most one CTA per SM, and a kernel that the
+ * caller runs concurrently on another stream can delay it but not block it.
+ * Tolerances as the separate calls. */
+nvfp4_status nvfp4_mlp_decode(const uint16_t *x, const float *x_global_scale,
+                              const uint8_t *w_gate_up_int, const uint8_t *w_gate_up_int_sf,
+                              const float *alpha_gate_up, const float *h_global_scale,
+                              const uint8_t *w_down, const uint8_t *w_down_sf,
+                              const float *alpha_down, uint8_t *x_fp4, uint8_t *x_sf,
+                              uint8_t *h_fp4, uint8_t *h_sf, uint16_t *out, int64_t m,
+                              int64_t hidden, int64_t inter, int round_gate_up_bf16,
+                              void *workspace, size_t ws_bytes, nvfp4_stream_t stream);
+/* Workspace bytes for nvfp4_mlp_decode (0 for an unsupported shape). */
+size_t nvfp4_mlp_decode_workspace_bytes(int64_t m, int64_t hidden, int64_t inter);
+
 /* Weight prep, run once at load time ([P2] modelopt_quant.py excerpt:
  * process_weights_after_loading; [P3] "实现拆解" item 2:
  * prepare_bf16_fp4_weights).  Takes the LINEAR scales (the pages snapshot the

@@ -44,6 +44,8 @@ _SIGS = {
     "bf16_fp4_gemm_ex": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
     "bf16_fp4_gemm_prescaled": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
     "bf16_awq_prescale": [_P, _P, _P, _I64, _I64, _P],
+    "nvfp4_mlp_decode": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, _SZ,
+                         _P],
     "nvfp4_prepare_weights": [_P, _P, _I64, _I64, _P, _P, _P],
     "nvfp4_prepare_gate_up_interleaved": [_P, _P, _I64, _I64, _P, _P, _P],
     "nvfp4_gemm_decode_noalloc": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P],
@@ -51,7 +53,8 @@ _SIGS = {
     "nvfp4_set_wait_limit": [ctypes.c_uint32],
 }
 EXPORTS = sorted(list(_SIGS) + ["nvfp4_status_string", "nvfp4_version", "nvfp4_sf_bytes",
-                                "nvfp4_workspace_bytes", "bf16_fp4_gemm_prescaled_workspace_bytes"])
+                                "nvfp4_workspace_bytes", "bf16_fp4_gemm_prescaled_workspace_bytes",
+                                "nvfp4_mlp_decode_workspace_bytes"])
 
 
 def load(path=LIB_PATH):
@@ -72,6 +75,8 @@ def load(path=LIB_PATH):
     lib.nvfp4_workspace_bytes.argtypes, lib.nvfp4_workspace_bytes.restype = [_I64, _I64, _I64, _I], _SZ
     lib.bf16_fp4_gemm_prescaled_workspace_bytes.argtypes = [_I64, _I64, _I64, _I]
     lib.bf16_fp4_gemm_prescaled_workspace_bytes.restype = _SZ
+    lib.nvfp4_mlp_decode_workspace_bytes.argtypes = [_I64, _I64, _I64]
+    lib.nvfp4_mlp_decode_workspace_bytes.restype = _SZ
     _lib = lib
     return lib
 
@@ -117,6 +122,19 @@ def nvfp4_workspace_bytes(m, n, k, algo=ALGO_AUTO):
 
 def bf16_fp4_gemm_prescaled_workspace_bytes(m, n, k, algo=ALGO_AUTO):
     return load().bf16_fp4_gemm_prescaled_workspace_bytes(m, n, k, algo)
+
+
+def nvfp4_mlp_decode_workspace_bytes(m, hidden, inter):
+    return load().nvfp4_mlp_decode_workspace_bytes(m, hidden, inter)
+
+
+def nvfp4_mlp_decode(x, x_global_scale, w_gate_up_int, w_gate_up_int_sf, alpha_gate_up, h_global_scale,
+                     w_down, w_down_sf, alpha_down, x_fp4, x_sf, h_fp4, h_sf, out, m, hidden, inter,
+                     round_gate_up_bf16, workspace, ws_bytes, stream=None):
+    _call("nvfp4_mlp_decode", _ptr(x), _ptr(x_global_scale), _ptr(w_gate_up_int), _ptr(w_gate_up_int_sf),
+          _ptr(alpha_gate_up), _ptr(h_global_scale), _ptr(w_down), _ptr(w_down_sf), _ptr(alpha_down),
+          _ptr(x_fp4), _ptr(x_sf), _ptr(h_fp4), _ptr(h_sf), _ptr(out), m, hidden, inter,
+          1 if round_gate_up_bf16 else 0, _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def bf16_awq_prescale(x, pre_quant_scale, out, m, k, stream=None):

@@ -329,6 +329,54 @@ size_t bf16_fp4_gemm_prescaled_workspace_bytes(int64_t m, int64_t n, int64_t k, 
   return (size_t)(m * k * 2);
 }
 
+nvfp4_status nvfp4_mlp_decode(const uint16_t *x, const float *x_global_scale, const uint8_t *w_gate_up_int,
+                              const uint8_t *w_gate_up_int_sf, const float *alpha_gate_up,
+                              const float *h_global_scale, const uint8_t *w_down, const uint8_t *w_down_sf,
+                              const float *alpha_down, uint8_t *x_fp4, uint8_t *x_sf, uint8_t *h_fp4,
+                              uint8_t *h_sf, uint16_t *out, int64_t m, int64_t hidden, int64_t inter,
+                              int round_gate_up_bf16, void *workspace, size_t ws_bytes,
+                              nvfp4_stream_t stream) {
+  if (!x || !x_global_scale || !w_gate_up_int || !w_gate_up_int_sf || !alpha_gate_up || !h_global_scale ||
+      !w_down || !w_down_sf || !alpha_down || !x_fp4 || !x_sf || !h_fp4 || !h_sf || !out)
+    return NVFP4_ERR_INVALID_ARG;
+  if (m < 0 || hidden <= 0 || inter <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (m == 0) return NVFP4_OK;
+  if (!mlp_decode_supported(m, hidden, inter)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  const void *ptrs[] = {x, w_gate_up_int, w_gate_up_int_sf, w_down, w_down_sf, x_fp4, x_sf, h_fp4, h_sf, out};
+  for (const void *q : ptrs)
+    if (!aligned16(q)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace || ws_bytes < mlp_decode_workspace_bytes(m, hidden, inter)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  MlpDecodeParams q{};
+  q.x = x;
+  q.gs_x = x_global_scale;
+  q.w_gu = w_gate_up_int;
+  q.w_gu_sf = w_gate_up_int_sf;
+  q.alpha_gu = alpha_gate_up;
+  q.gs_h = h_global_scale;
+  q.w_dn = w_down;
+  q.w_dn_sf = w_down_sf;
+  q.alpha_dn = alpha_down;
+  q.x_fp4 = x_fp4;
+  q.x_sf = x_sf;
+  q.h_fp4 = h_fp4;
+  q.h_sf = h_sf;
+  q.out = out;
+  q.m = m;
+  q.hidden = hidden;
+  q.inter = inter;
+  q.round_bf16 = round_gate_up_bf16 != 0;
+  q.workspace = workspace;
+  q.ws_bytes = ws_bytes;
+  q.wait_limit = g_wait_limit.load();
+  return from_cuda(launch_mlp_decode(q, (cudaStream_t)stream));
+}
+
+size_t nvfp4_mlp_decode_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {
+  return mlp_decode_workspace_bytes(m, hidden, inter);
+}
+
 nvfp4_status bf16_awq_prescale(const uint16_t *x, const uint16_t *pre_quant_scale, uint16_t *out, int64_t m,
                                int64_t k, nvfp4_stream_t stream) {
   if (!x || !pre_quant_scale || !out || m < 0 || k <= 0) return NVFP4_ERR_INVALID_ARG;

@@ -21,6 +21,7 @@
 // epilogue (TMEM lane = weight row).  Bounded waits as in gemm_tc.cu.
 #include "common.cuh"
 #include "internal.h"
+#include "splitk.cuh"
 #include "tc_ptx.cuh"
 
 namespace nvfp4 {
@@ -70,41 +71,6 @@ struct SwapArgs {
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Contiguous partition of W = tiles * kb_total k-blocks over `grid` CTAs:
-// CTA j owns [start(j), start(j+1)), start(j) = floor(j * W / grid).  Without
-// a workspace the cut points are rounded to whole tiles instead.
-struct Partition {
-  int64_t w, grid, kbt;
-  bool whole_tiles;
-  int64_t tiles;
-  __device__ __forceinline__ int64_t start(int64_t j) const {
-    if (whole_tiles) return (j * tiles / grid) * kbt;
-    return j * w / grid;
-  }
-  // CTA owning global k-block x (inverse of start)
-  __device__ __forceinline__ int64_t cta_of(int64_t x) const {
-    if (whole_tiles) {
-      const int64_t t = x / kbt;
-      return ((t + 1) * grid - 1) / tiles;
-    }
-    return ((x + 1) * grid - 1) / w;
-  }
-};
-
-// Iterates the fragments of one CTA: tile, [kb0, kb1) within the tile.
-struct FragIter {
-  int64_t x, end, kbt;
-  __device__ __forceinline__ bool next(int &tile, int &kb0, int &kb1) {
-    if (x >= end) return false;
-    tile = (int)(x / kbt);
-    kb0 = (int)(x - (int64_t)tile * kbt);
-    const int64_t room = end - x;
-    kb1 = (int)min((int64_t)kbt, kb0 + room);
-    x += kb1 - kb0;
-    return true;
-  }
-};
 
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -273,11 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tile, kb0, kb1;
     for (; fi.next(tile, kb0, kb1); ++it) {
       const int ab = it & 1;
-      if (!ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag)) {
+      const bool got =
+          ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag);
+      if (!got) {
         *abort_flag = 1;
         atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
-        break;
       }
+      if (ptx::bar_any(1, 128, !got || *abort_flag)) break;   // the four warps leave together
       ptx::tc_fence_after();
       float v[NT];
 #pragma unroll
@@ -303,23 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < NT; ++t)
           if (t < mt) mine[t * 128 + r] = v[t];
         epi_bar();                    // every partial write of the CTA precedes the release below
-        if (et == 0) {
-          asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          const int old = atomicAdd(&p.counters[tile], 1);
-          const int last = old == (int)(c_last - c_first);
-          if (last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          *last_flag = last;
-        }
+        if (et == 0)
+          *last_flag = atom_add_acq_rel_gpu(&p.counters[tile], 1) == (uint32_t)(c_last - c_first);
         epi_bar();
         if (!*last_flag) continue;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) v[t] = 0.0f;
-        for (int64_t c = c_first; c <= c_last; ++c) {      // K order
-          const float *pc = slot(c);
-#pragma unroll
-          for (int t = 0; t < NT; ++t)
-            if (t < mt) v[t] += __ldcg(pc + t * 128 + r);
-        }
+        sum_partials_in_k_order<NT>(v, c_first, c_last, mt, r, slot);
         if (et == 0) p.counters[tile] = 0;
       }
 
@@ -339,6 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < NT; ++t) s_out[r * C::PITCH + t] = (p.rs && t < mt ? alpha * p.rs[t] : alpha) * v[t];
         epi_bar();
+        // SwiGLU one element per thread; h replaces the up value in s_out
+        for (int idx = et; idx < mt * 64; idx += 128) {
+          const int t = idx >> 6, i = idx & 63;
+          s_out[i * C::PITCH + t] = silu_mul_fast(s_out[(64 + i) * C::PITCH + t], s_out[i * C::PITCH + t]);
+        }
+        epi_bar();
         const int inter = p.n >> 1;
         const int ocp4 = ((inter >> 4) + 3) >> 2;
         const float gs = __ldg(p.out_gs);
@@ -346,8 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = idx >> 2, qb = idx & 3;
           float h[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            h[i] = silu_mul_fast(s_out[(64 + 16 * qb + i) * C::PITCH + t], s_out[(16 * qb + i) * C::PITCH + t]);
+          for (int i = 0; i < 16; ++i) h[i] = s_out[(16 * qb + i) * C::PITCH + t];
           uint32_t lo, hi;
           const uint32_t sf = quantize_block16(h, gs, lo, hi);
           const int f = 64 * tile + 16 * qb;

@@ -248,8 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!ptx::mbar_wait_bounded(&full[s], ph, limit, kTimeoutNs, abort_flag)) {
-          give_up();
+        const bool got = ptx::mbar_wait_bounded(&full[s], ph, limit, kTimeoutNs, abort_flag);
+        if (!got) give_up();
+        if (ptx::bar_any(1, 128, !got || *abort_flag)) {   // the four warps leave together
           ok = false;
           break;
         }

@@ -93,4 +93,24 @@ cudaError_t launch_w4a16_tc(const uint16_t *x, const uint8_t *w, const uint8_t *
                             uint16_t *d, int64_t m, int64_t n, int64_t k, uint32_t wait_limit,
                             cudaStream_t st);
 
+// Whole decode MLP in one persistent kernel (mlp_decode.cu).
+struct MlpDecodeParams {
+  const uint16_t *x;                         // bf16 [m, hidden]
+  const float *gs_x;                         // x global scale
+  const uint8_t *w_gu, *w_gu_sf;             // interleaved gate_up weight, swizzled scales
+  const float *alpha_gu, *gs_h;
+  const uint8_t *w_dn, *w_dn_sf;             // down_proj weight [hidden, inter/2], swizzled scales
+  const float *alpha_dn;
+  uint8_t *x_fp4, *x_sf, *h_fp4, *h_sf;      // intermediates (outputs too)
+  uint16_t *out;                             // bf16 [m, hidden]
+  int64_t m, hidden, inter;
+  bool round_bf16;
+  void *workspace;
+  size_t ws_bytes;
+  uint32_t wait_limit;
+};
+bool mlp_decode_supported(int64_t m, int64_t hidden, int64_t inter);
+size_t mlp_decode_workspace_bytes(int64_t m, int64_t hidden, int64_t inter);
+cudaError_t launch_mlp_decode(const MlpDecodeParams &q, cudaStream_t st);
+
 }  // namespace nvfp4

@@ -86,6 +86,57 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
+// Named barrier `id` over `nthreads` threads that also ORs a flag across
+// them: every participant gets the same answer, so a group can leave a loop
+// together when any one of its threads gave up a bounded wait (a thread that
+// left alone would leave the others blocked at the group's next barrier).
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t nthreads, bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "bar.red.or.pred q, %2, %3, p;\n"
+      "selp.u32 %0, 1, 0, q;\n"
+      "}"
+      : "=r"(r)
+      : "r"((uint32_t)flag), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// ------------------------------------------------------- grid-wide counters
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Generic-proxy global writes of this thread become visible to async-proxy
+// (TMA / bulk copy) reads ordered after it, and vice versa.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *ctr >= target (acquire), with the same give-up rules as
+// mbar_wait_bounded.  Returns false when it gave up.
+__device__ __forceinline__ bool counter_wait_bounded(const uint32_t *ctr, uint32_t target, uint32_t limit,
+                                                     uint64_t timeout_ns, volatile int *abort) {
+  uint64_t t0 = 0;
+  for (uint32_t polls = 1;; ++polls) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if (*abort) return false;
+    if (limit) {
+      if (polls >= limit) return false;
+    } else if ((polls & 63u) == 0) {
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > timeout_ns) return false;
+    }
+    __nanosleep(64);
+  }
+}
+
 // ---------------------------------------------------------------- TMA / bulk
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");

@@ -122,3 +122,24 @@ def test_awq_prescale_host_checks(lib):
                                        None) == nv.ERR_INVALID_ARG
     assert lib.bf16_fp4_gemm_prescaled(FAKE, FAKE + 8, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None, 0, 0,
                                        None) == nv.ERR_UNSUPPORTED_SHAPE
+
+
+def test_mlp_decode_host_checks(lib):
+    args = [FAKE] * 14 + [4, 256, 512, 1, FAKE, 1 << 30, None]
+    bad = list(args)
+    bad[1] = None                                    # no x global scale
+    assert lib.nvfp4_mlp_decode(*bad) == nv.ERR_INVALID_ARG
+    bad = list(args)
+    bad[14] = 65                                     # more tokens than the kernel takes
+    assert lib.nvfp4_mlp_decode(*bad) == nv.ERR_UNSUPPORTED_SHAPE
+    bad = list(args)
+    bad[15] = 320                                    # hidden % 128
+    assert lib.nvfp4_mlp_decode(*bad) == nv.ERR_UNSUPPORTED_SHAPE
+    bad = list(args)
+    bad[19] = 16                                     # workspace too small
+    assert lib.nvfp4_mlp_decode(*bad) == nv.ERR_INVALID_ARG
+    bad = list(args)
+    bad[14] = 0                                      # no tokens: nothing to do
+    assert lib.nvfp4_mlp_decode(*bad) == nv.OK
+    assert nv.nvfp4_mlp_decode_workspace_bytes(4, 256, 512) > 0
+    assert nv.nvfp4_mlp_decode_workspace_bytes(65, 256, 512) == 0
