@@ -3,7 +3,10 @@
 
 Workload: the decode dense MLP, W4A4 NVFP4, hidden 5120, intermediate 17408
 (gate_up 34816 x 5120, down 5120 x 17408).  One step runs the MLP forward
-once for each decode batch M in {1, 2, 4, 8, 16} (31 tokens per step):
+once for each decode batch M in {1, 2, 4, 8, 16} (31 tokens per step) as one
+nvfp4_mlp_decode launch each: quantize x -> gate_up GEMM -> SwiGLU (on the
+bf16-rounded gate_up, as silu_mul_nvfp4_quantize) + NVFP4 requantize ->
+down GEMM.  `--decode-path chain` runs the same step as four launches:
     nvfp4_quantize(x) -> nvfp4_gemm(gate_up) -> silu_mul_nvfp4_quantize
     -> nvfp4_gemm(down)
 Weights are synthetic N(0, 0.02), quantized to NVFP4 on the device by the
@@ -44,6 +47,8 @@ def parse():
     p.add_argument("--workload", default="decode", choices=["decode", "prefill", "w4a16"],
                    help="decode (default line) | prefill H7168/I18432 | w4a16 H5120/I17408")
     p.add_argument("--m", type=int, default=None, help="single M for prefill / w4a16")
+    p.add_argument("--decode-path", default="fused", choices=["fused", "chain"],
+                   help="decode step as one nvfp4_mlp_decode launch (default) or the four-launch chain")
     return p.parse_args()
 
 
@@ -248,8 +253,10 @@ def run_ours(args, world, rank, local):
         workload = f"W4A16 dense MLP (bf16 x NVFP4), hidden 5120, intermediate 17408, M in {ms}"
     tokens_per_step = sum(ms)
     mmax = max(ms)
+    fused_decode = wl == "decode" and args.decode_path == "fused"
+    interleaved = wl == "prefill" or fused_decode
 
-    w_gu0 = make_weight(2 * inter, hid, interleave=(wl == "prefill"))
+    w_gu0 = make_weight(2 * inter, hid, interleave=interleaved)
     w_dn0 = make_weight(hid, inter)
     copies = [(w_gu0, w_dn0)]
     for _ in range(ncopy - 1):
@@ -274,7 +281,7 @@ def run_ours(args, world, rank, local):
         a_gu = scalar(np.float32(1.0) / (gs_x * w_gu0[2]))
         nv.nvfp4_gemm(xq, xs, w_gu0[0], w_gu0[1], a_gu, gu_tmp, mc, 2 * inter, hid)
         gf = gu_tmp.float()
-        if wl == "prefill":   # interleaved rows: blocks of 128 = [64 up ; 64 gate]
+        if interleaved:       # interleaved rows: blocks of 128 = [64 up ; 64 gate]
             gf = gf.view(mc, 2 * inter // 128, 2, 64)
             u, g = gf[:, :, 0, :].reshape(mc, inter), gf[:, :, 1, :].reshape(mc, inter)
         else:
@@ -300,6 +307,8 @@ def run_ours(args, world, rank, local):
     # sized for the largest GEMM of the chain and shared by its sequential calls
     ws_bytes = max([nv.nvfp4_workspace_bytes(m, 2 * inter, hid) for m in ms] +
                    [nv.nvfp4_workspace_bytes(m, hid, inter) for m in ms] + [0])
+    if fused_decode:
+        ws_bytes = max(nv.nvfp4_mlp_decode_workspace_bytes(m, hid, inter) for m in ms)
     ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     def forward(m, wc, ev=None):
@@ -315,6 +324,14 @@ def run_ours(args, world, rank, local):
             nv.silu_mul_bf16(b["gu"], m, inter, b["h16"])
             nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter)
             return
+        if fused_decode:
+            if ev is not None:
+                ev[0].record()
+            nv.nvfp4_mlp_decode(x_in[m], gs_x_d, gq, gsf, a_gu, gs_h_d, dq, dsf, a_dn, b["xq"], b["xs"],
+                                b["hq"], b["hs"], b["out"], m, hid, inter, True, ws, ws_bytes)
+            if ev is not None:
+                ev[1].record()
+            return
         nv.nvfp4_quantize(x_in[m], m, hid, gs_x_d, b["xq"], b["xs"])
         if ev is not None:
             ev[0].record()
@@ -329,7 +346,7 @@ def run_ours(args, world, rank, local):
             nv.silu_mul_nvfp4_quantize(b["gu"], m, inter, gs_h_d, b["hq"], b["hs"])
         nv.nvfp4_gemm(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
 
-    launches_per_step = sum({"decode": 4, "prefill": 3, "w4a16": 3}[wl] for _ in ms)
+    launches_per_step = sum((1 if fused_decode else {"decode": 4, "prefill": 3, "w4a16": 3}[wl]) for _ in ms)
 
     try:
         torch.cuda.Event(enable_timing=True, external=True)
@@ -413,7 +430,14 @@ def run_ours(args, world, rank, local):
                        f"averaged over a {args.steps}-step pass right after the headline pass")
         per_m_us = {str(m): 1000.0 * t for m, t in zip(ms, dom_ms)}
         tot_s = sum(dom_ms) / 1000.0
-        if wl == "decode":
+        if fused_decode:
+            # weights (codes + scales) of both GEMMs, x in, output out
+            nbytes = sum(3 * inter * hid * 9 // 16 + 2 * m * hid * 2 for m in ms)
+            achieved = nbytes / tot_s / 1e9
+            roofline = {"bound": "hbm", "kernel": "nvfp4_mlp_decode (whole decode MLP, one launch, M=1..16)",
+                        "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                        "traffic": None, "algorithmic_bytes_per_step": nbytes}
+        elif wl == "decode":
             nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 9 // 16 + m * 2 * inter * 2 for m in ms)
             achieved = nbytes / tot_s / 1e9
             roofline = {"bound": "hbm", "kernel": "nvfp4_gemm gate_up 34816x5120 (GEMV, M=1..16)",
@@ -474,7 +498,8 @@ def run_ours(args, world, rank, local):
             "data": "synthetic",
             "config": {"workload": workload, "tokens_per_step": tokens_per_step,
                        "l2": f"{ncopy} rotating weight copies, {ncopy * weight_bytes / 1e6:.0f} MB > L2",
-                       "graph": "one CUDA graph per step", "parallelism": f"replicas{world}"},
+                       "graph": "one CUDA graph per step", "parallelism": f"replicas{world}",
+                       **({"decode_path": args.decode_path} if wl == "decode" else {})},
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "note": "direct API calls, no graph, pinned host buffers"},
