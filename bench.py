@@ -309,6 +309,9 @@ def run_ours(args, world, rank, local):
                    [nv.nvfp4_workspace_bytes(m, hid, inter) for m in ms] + [0])
     if fused_decode:
         ws_bytes = max(nv.nvfp4_mlp_decode_workspace_bytes(m, hid, inter) for m in ms)
+    if wl == "w4a16":
+        ws_bytes = max([nv.bf16_fp4_gemm_workspace_bytes(m, 2 * inter, hid) for m in ms] +
+                       [nv.bf16_fp4_gemm_workspace_bytes(m, hid, inter) for m in ms] + [0])
     ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     def forward(m, wc, ev=None):
@@ -318,11 +321,11 @@ def run_ours(args, world, rank, local):
         if wl == "w4a16":
             if ev is not None:
                 ev[0].record()
-            nv.bf16_fp4_gemm(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid)
+            nv.bf16_fp4_gemm(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes)
             if ev is not None:
                 ev[1].record()
             nv.silu_mul_bf16(b["gu"], m, inter, b["h16"])
-            nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter)
+            nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
             return
         if fused_decode:
             if ev is not None:

@@ -237,6 +237,13 @@ nvfp4_status nvfp4_gemm_swiglu_quant_per_token(const uint8_t *a_fp4, const uint8
 /* W4A16 GEMM ([P3] fp4_gemm, quant_mode "w4a16" -> mm_bf16_fp4):
  *   d[m, n] = bf16( alpha * sum_k a[m, k] * (E2M1(b)*SF_b)[n, k] )
  *   a bf16 [m, k];  b_fp4/b_sf as nvfp4_gemm;  alpha fp32 [1] = 1/gs_b only.
+ *   workspace  optional DEVICE scratch (nullptr / 0 allowed): with
+ *              bf16_fp4_gemm_workspace_bytes(m, n, k, algo) bytes, 16-byte
+ *              aligned and zero-filled once before first use, the tensor-core
+ *              path splits up to 64 tokens along K over all SMs (the
+ *              counters are left at zero after every complete call; calls
+ *              sharing it must be stream-ordered); with less, every SM owns
+ *              whole 128-row weight tiles.  The result does not depend on it.
  * Requires k % 64 == 0, n % 32 == 0. */
 nvfp4_status bf16_fp4_gemm(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
                            const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
@@ -245,6 +252,8 @@ nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uin
                               const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
                               void *workspace, size_t ws_bytes, nvfp4_algo algo,
                               nvfp4_stream_t stream);
+/* Split-K workspace bytes for bf16_fp4_gemm(_ex) (0: none needed).  Host only. */
+size_t bf16_fp4_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo);
 
 /* NVFP4_AWQ activation pre-scale ([P3] "实现拆解" item 2: in W4A16 mode the
  * linear layer's apply keeps the AWQ pre_quant_scale multiply of x and then
@@ -261,10 +270,12 @@ nvfp4_status bf16_awq_prescale(const uint16_t *x, const uint16_t *pre_quant_scal
  *   pre_quant_scale  bf16 [k] DEVICE, 16-byte aligned (s above; nullptr is
  *                    NVFP4_ERR_INVALID_ARG, a misaligned pointer
  *                    NVFP4_ERR_UNSUPPORTED_SHAPE).
- *   workspace        DEVICE scratch of at least
- *                    bf16_fp4_gemm_prescaled_workspace_bytes(m, n, k, algo)
- *                    bytes, 16-byte aligned, no initial contents needed
- *                    (less: NVFP4_ERR_INVALID_ARG, nothing runs).
+ *   workspace        DEVICE scratch, 16-byte aligned: on the tensor cores the
+ *                    scaled activations take its first m*k*2 bytes (rounded
+ *                    up to 256; less: NVFP4_ERR_INVALID_ARG, nothing runs),
+ *                    and the rest serves as bf16_fp4_gemm's split-K
+ *                    workspace (zero-filled once before first use);
+ *                    bf16_fp4_gemm_prescaled_workspace_bytes gives both.
  *   Everything else as bf16_fp4_gemm_ex (same algo choices and shape rules).
  * a * s is rounded once to bf16, the activation type, as the separate
  * multiply would.  The GEMV scales each activation as it loads it (no
@@ -276,9 +287,10 @@ nvfp4_status bf16_fp4_gemm_prescaled(const uint16_t *a, const uint16_t *pre_quan
                                      const uint8_t *b_fp4, const uint8_t *b_sf, const float *alpha,
                                      uint16_t *d, int64_t m, int64_t n, int64_t k, void *workspace,
                                      size_t ws_bytes, nvfp4_algo algo, nvfp4_stream_t stream);
-/* Scratch bytes for bf16_fp4_gemm_prescaled: m*k*2 when it runs on the
- * tensor cores (NVFP4_ALGO_AUTO on a supported shape, TC or TC_SWAPAB),
- * 0 on the GEMV.  Host only, no GPU needed. */
+/* Scratch bytes for bf16_fp4_gemm_prescaled: the scaled activations
+ * (m*k*2 rounded up to 256) plus bf16_fp4_gemm_workspace_bytes when it runs
+ * on the tensor cores (NVFP4_ALGO_AUTO on a supported shape, TC or
+ * TC_SWAPAB), 0 on the GEMV.  Host only, no GPU needed. */
 size_t bf16_fp4_gemm_prescaled_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo);
 
 /* The whole decode MLP in one kernel launch: nvfp4_quantize of x, the gate_up

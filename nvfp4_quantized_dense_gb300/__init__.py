@@ -54,6 +54,7 @@ _SIGS = {
 }
 EXPORTS = sorted(list(_SIGS) + ["nvfp4_status_string", "nvfp4_version", "nvfp4_sf_bytes",
                                 "nvfp4_workspace_bytes", "bf16_fp4_gemm_prescaled_workspace_bytes",
+                                "bf16_fp4_gemm_workspace_bytes",
                                 "nvfp4_mlp_decode_workspace_bytes"])
 
 
@@ -75,6 +76,8 @@ def load(path=LIB_PATH):
     lib.nvfp4_workspace_bytes.argtypes, lib.nvfp4_workspace_bytes.restype = [_I64, _I64, _I64, _I], _SZ
     lib.bf16_fp4_gemm_prescaled_workspace_bytes.argtypes = [_I64, _I64, _I64, _I]
     lib.bf16_fp4_gemm_prescaled_workspace_bytes.restype = _SZ
+    lib.bf16_fp4_gemm_workspace_bytes.argtypes = [_I64, _I64, _I64, _I]
+    lib.bf16_fp4_gemm_workspace_bytes.restype = _SZ
     lib.nvfp4_mlp_decode_workspace_bytes.argtypes = [_I64, _I64, _I64]
     lib.nvfp4_mlp_decode_workspace_bytes.restype = _SZ
     _lib = lib
@@ -118,6 +121,10 @@ def nvfp4_sf_bytes(rows, k, layout=SF_SWIZZLED_128x4):
 
 def nvfp4_workspace_bytes(m, n, k, algo=ALGO_AUTO):
     return load().nvfp4_workspace_bytes(m, n, k, algo)
+
+
+def bf16_fp4_gemm_workspace_bytes(m, n, k, algo=ALGO_AUTO):
+    return load().bf16_fp4_gemm_workspace_bytes(m, n, k, algo)
 
 
 def bf16_fp4_gemm_prescaled_workspace_bytes(m, n, k, algo=ALGO_AUTO):

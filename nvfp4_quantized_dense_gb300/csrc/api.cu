@@ -272,6 +272,8 @@ nvfp4_status nvfp4_gemm_swiglu_quant(const uint8_t *a_fp4, const uint8_t *a_sf,
 }  // extern "C"
 
 namespace {
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
 nvfp4_status w4a16_impl(const uint16_t *a, const uint16_t *pre_scale, const uint8_t *b_fp4, const uint8_t *b_sf,
                         const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k, void *workspace,
                         size_t ws_bytes, nvfp4_algo algo, nvfp4_stream_t stream) {
@@ -292,17 +294,22 @@ nvfp4_status w4a16_impl(const uint16_t *a, const uint16_t *pre_scale, const uint
     return from_cuda(launch_gemv(GEMV_W4A16, a, nullptr, b_fp4, b_sf, alpha, nullptr, d, nullptr,
                                  nullptr, m, n, k, st, nullptr, pre_scale));
   if (!w4a16_tc_supported(m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (workspace && !aligned16(workspace)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (pre_scale) {
     // The tensor-core kernel's converter warps are its critical path, and
     // every weight tile reads the same activations: scale them once, into the
-    // workspace, in a pass of their own.
-    if (!workspace || ws_bytes < (size_t)(m * k * 2)) return NVFP4_ERR_INVALID_ARG;
-    if (!aligned16(workspace)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    // front of the workspace, in a pass of their own.
+    const size_t xs_bytes = round256((size_t)(m * k * 2));
+    if (!workspace || ws_bytes < xs_bytes) return NVFP4_ERR_INVALID_ARG;
     uint16_t *xs = static_cast<uint16_t *>(workspace);
     if (cudaError_t e = launch_awq_prescale(a, pre_scale, m, k, xs, st)) return from_cuda(e);
     a = xs;
+    workspace = static_cast<uint8_t *>(workspace) + xs_bytes;
+    ws_bytes -= xs_bytes;
   }
-  return from_cuda(launch_w4a16_tc(a, b_fp4, b_sf, alpha, d, m, n, k, g_wait_limit.load(), st));
+  if (ws_bytes == 0) workspace = nullptr;
+  return from_cuda(launch_w4a16_tc(a, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes,
+                                   g_wait_limit.load(), st));
 }
 }  // namespace
 
@@ -310,8 +317,13 @@ extern "C" {
 
 nvfp4_status bf16_fp4_gemm_ex(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
                               const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
-                              void *, size_t, nvfp4_algo algo, nvfp4_stream_t stream) {
-  return w4a16_impl(a, nullptr, b_fp4, b_sf, alpha, d, m, n, k, nullptr, 0, algo, stream);
+                              void *workspace, size_t ws_bytes, nvfp4_algo algo, nvfp4_stream_t stream) {
+  return w4a16_impl(a, nullptr, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes, algo, stream);
+}
+
+size_t bf16_fp4_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, nvfp4_algo algo) {
+  if (m <= 0 || n <= 0 || k <= 0 || algo == NVFP4_ALGO_GEMV) return 0;
+  return w4a16_workspace_bytes(m, n, k);
 }
 
 nvfp4_status bf16_fp4_gemm_prescaled(const uint16_t *a, const uint16_t *pre_quant_scale,
@@ -326,7 +338,7 @@ size_t bf16_fp4_gemm_prescaled_workspace_bytes(int64_t m, int64_t n, int64_t k, 
   if (m <= 0 || n <= 0 || k <= 0 || algo == NVFP4_ALGO_GEMV) return 0;
   if (m > (int64_t(1) << 31) || k > (int64_t(1) << 31)) return 0;
   if (algo == NVFP4_ALGO_AUTO && !w4a16_tc_supported(m, n, k)) return 0;
-  return (size_t)(m * k * 2);
+  return round256((size_t)(m * k * 2)) + w4a16_workspace_bytes(m, n, k);
 }
 
 nvfp4_status nvfp4_mlp_decode(const uint16_t *x, const float *x_global_scale, const uint8_t *w_gate_up_int,

@@ -4,59 +4,83 @@
 //
 // The tensor cores need both operands of a kind::f16 MMA in the same type,
 // so the weight is dequantized to bf16 in shared memory: converter warps read
-// the stage's E2M1 codes and E4M3 scales (TMA / bulk copies) and write
-// E2M1 * scale -- exact in bf16, at most 5 significant bits -- into a
-// 128-byte-swizzled K-major tile that the MMA reads directly.  The weight is
-// the MMA's 128-row operand and the tokens its N (16..256), so each weight
-// element is dequantized once per 256-token tile; D^T[n, t] accumulates in
-// TMEM (two buffers) and the epilogue writes D[t, n] with the 32 lanes of a
-// warp on 32 consecutive n.
+// a k-block's E2M1 codes and E4M3 scales and write E2M1 * scale -- exact in
+// bf16, at most 5 significant bits -- into a 128-byte-swizzled K-major tile
+// that the MMA reads directly.  The weight is the MMA's 128-row operand and
+// the tokens its N (16..256); D^T[n, t] accumulates in TMEM (two buffers) and
+// the epilogue writes D[t, n] with the 32 lanes of a warp on 32 consecutive n.
 //
-// Roles (320 threads, one CTA per SM, persistent over (weight tile, token
-// tile) pairs, token tile fastest): warp 0 TMA producer, warp 1 TMEM owner +
-// MMA issuer, warps 2..5 converters, warps 6..9 epilogue.  Bounded waits as
-// in gemm_tc.cu.
+// Two rings: a deep one of raw k-blocks (4.5 KB of weight codes and scales
+// from HBM plus the k-block's activation tile), so that ~100 KB of weight
+// bytes per SM are in flight at decode sizes, and a shallow one of
+// dequantized 16 KB weight tiles.  A raw stage is released by the MMA (it
+// reads the activation tile there), a dequantized tile likewise.
+//
+// Work split: as in the swap-AB kernel, the (weight tile, 64-wide k-block)
+// pairs are cut into one contiguous run per CTA when the caller gives a
+// workspace (tokens <= 64); a tile shared by CTAs is finished by the last to
+// arrive, which sums the fp32 partials in K order.  Without a workspace, or
+// for more tokens, every CTA owns whole tiles.
+//
+// Roles (448 threads, one CTA per SM): warp 0 TMA producer, warp 1 TMEM owner
+// + MMA issuer, warps 2..9 converters, warps
+// 10..13 epilogue.  Bounded waits as in gemm_tc.cu.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "splitk.cuh"
 #include "tc_ptx.cuh"
 
 namespace nvfp4 {
 namespace {
 
-constexpr int BK = 64;                      // K per stage: 128 bytes of bf16 per row
+constexpr int BK = 64;                      // K per k-block: 128 bytes of bf16 per row
 constexpr uint32_t WC_BYTES = 128 * BK / 2; // weight codes, 4 KB
 constexpr uint32_t WS_BYTES = 512;          // one 128x4 scale tile
 constexpr uint32_t WB_BYTES = 128 * BK * 2; // dequantized weight tile, 16 KB
-constexpr int kThreads = 320;
+constexpr int kConvWarps = 8;               // converter warps
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kThreads = 64 + kConvThreads + 128;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kDrainPolls = 1u << 22;
 
 template <int NT>
 struct Cfg {
   static constexpr uint32_t X_BYTES = NT * BK * 2;                       // NT rows x 128 B
-  static constexpr uint32_t RAW = X_BYTES + WB_BYTES + WC_BYTES + WS_BYTES;
-  static constexpr uint32_t STAGE_BYTES = (RAW + 1023) / 1024 * 1024;
-  static constexpr int STAGES = (220 * 1024) / STAGE_BYTES > 8 ? 8 : (220 * 1024) / STAGE_BYTES;
-  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr uint32_t RAW_BYTES = (X_BYTES + WC_BYTES + WS_BYTES + 1023) / 1024 * 1024;
+  // Up to 64 tokens each converter warp dequantizes whole k-blocks (k-block
+  // j -> warp j % DSTAGES, which owns tile j % DSTAGES): many k-blocks in
+  // flight for the weight stream.  Above, every warp takes 16 rows of every
+  // k-block: short latency per k-block for the compute-bound MMA.
+  static constexpr bool WHOLE_KB = NT <= 64;
+  static constexpr int DSTAGES = NT <= 32 ? 8 : NT == 64 ? 6 : 4;         // dequantized tiles
+  static_assert(!WHOLE_KB || DSTAGES <= kConvWarps, "one converter warp per dequantized tile");
+  static constexpr int RSTAGES_FIT = (int)((220u * 1024 - DSTAGES * WB_BYTES) / RAW_BYTES);
+  static constexpr int RSTAGES = RSTAGES_FIT > 32 ? 32 : RSTAGES_FIT;   // raw k-blocks in flight
+  static_assert(RSTAGES >= DSTAGES, "raw ring at least as deep as the dequantized one");
+  static constexpr uint32_t BAR_BYTES = 1024;
+  static constexpr uint32_t SMEM_BYTES = DSTAGES * WB_BYTES + RSTAGES * RAW_BYTES + BAR_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * NT <= 32 ? 32 : 2 * NT <= 64 ? 64 : 2 * NT <= 128 ? 128 : 2 * NT <= 256 ? 256 : 512;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  static_assert(STAGES >= 3, "pipeline depth");
+  static_assert(RSTAGES >= 4, "pipeline depth");
+  static_assert((2 * RSTAGES + 2 * DSTAGES + 5) * 8 + 16 <= BAR_BYTES, "barrier area");
 };
 
 struct W4A16Args {
-  const uint8_t *w;        // codes [N, K/2]
   const uint8_t *wsf;      // swizzled scales over N rows
   const float *alpha;
   uint16_t *d;             // bf16 [M, N]
+  float *partials;         // [grid][maxfrag][NT][128] fp32 (tiles shared by CTAs)
+  int *counters;           // [tiles] arrival counters
   int32_t m, n, k;
-  int32_t wtiles, ttiles;
+  int32_t wtiles, ttiles, nkb;
+  int32_t grid, maxfrag, split_ok;
   uint32_t wait_limit;
   int *status;
 };
 
-__device__ __forceinline__ void conv_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -100,29 +124,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     w4a16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                  const W4A16Args p) {
   using C = Cfg<NT>;
-  constexpr int STAGES = C::STAGES;
+  constexpr int RST = C::RSTAGES;
+  constexpr int DSTAGES = C::DSTAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(base + STAGES * C::STAGE_BYTES);
-  uint64_t *conv = full + STAGES;
-  uint64_t *empty = conv + STAGES;
-  uint64_t *tfull = empty + STAGES;
+  auto st_wb = [&](int d) { return base + d * WB_BYTES; };
+  auto st_x = [&](int r) { return base + DSTAGES * WB_BYTES + r * C::RAW_BYTES; };
+  auto st_wc = [&](int r) { return st_x(r) + C::X_BYTES; };
+  auto st_ws = [&](int r) { return st_wc(r) + WC_BYTES; };
+  uint64_t *rfull = reinterpret_cast<uint64_t *>(base + DSTAGES * WB_BYTES + RST * C::RAW_BYTES);
+  uint64_t *rempty = rfull + RST;
+  uint64_t *dfull = rempty + RST;
+  uint64_t *dempty = dfull + DSTAGES;
+  uint64_t *tfull = dempty + DSTAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
-  auto st_x = [&](int s) { return base + s * C::STAGE_BYTES; };
-  auto st_wb = [&](int s) { return st_x(s) + C::X_BYTES; };
-  auto st_wc = [&](int s) { return st_wb(s) + WB_BYTES; };
-  auto st_ws = [&](int s) { return st_wc(s) + WC_BYTES; };
+  volatile int *last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&conv[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+    for (int r = 0; r < RST; ++r) {
+      ptx::mbar_init(&rfull[r], 1);
+      ptx::mbar_init(&rempty[r], 1);
+    }
+    for (int d = 0; d < DSTAGES; ++d) {
+      ptx::mbar_init(&dfull[d], C::WHOLE_KB ? 1 : kConvWarps);   // arrivals of the warps filling it
+      ptx::mbar_init(&dempty[d], 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], 1);
@@ -144,8 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tslot;
 
   const int tiles = p.wtiles * p.ttiles;
-  const int nkb = p.k / BK;
   const int cp4 = p.k >> 6;              // 512-byte scale tiles per 128-row block
+  const Partition part{(int64_t)tiles * p.nkb, p.grid, p.nkb, p.split_ok == 0, tiles};
+  const int64_t my_start = part.start(blockIdx.x), my_end = part.start(blockIdx.x + 1);
   const uint32_t limit = p.wait_limit;
   uint32_t issued_mask = 0, issued_parity = 0;
   bool mma_issued = false;
@@ -155,61 +186,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (ptx::elect_one()) {
       const uint64_t pol_w = ptx::l2_policy_evict_first();
       const uint64_t pol_x = ptx::l2_policy_evict_last();
-      int s = 0;
+      int r = 0;
       uint32_t ph = 0;
-      // The first STAGES stages get their weight codes and scales before the
-      // previous kernel on the stream has finished; their activation tiles
-      // follow once it has.
-      int pend_s[STAGES], pend_kb[STAGES], pend_tt[STAGES];
+      // The first RST raw stages get their weight codes and scales before
+      // the previous kernel on the stream has finished; their activation
+      // tiles follow once it has.
+      int pend_r[RST], pend_kb[RST], pend_tt[RST];
       int npend = 0, c = 0;
       bool flushed = false;
       auto load_x = [&](int st, int kb, int tt) {
-        ptx::tma_load_2d(st_x(st), &tm_x, &full[st], kb * (BK * 2), tt * NT, pol_x);
+        ptx::tma_load_2d(st_x(st), &tm_x, &rfull[st], kb * (BK * 2), tt * NT, pol_x);
       };
       auto flush = [&]() {
         pdl_wait();
-        for (int i = 0; i < npend; ++i) load_x(pend_s[i], pend_kb[i], pend_tt[i]);
+        for (int i = 0; i < npend; ++i) load_x(pend_r[i], pend_kb[i], pend_tt[i]);
         flushed = true;
       };
-      for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
-        const int wt = tile / p.ttiles, tt = tile % p.ttiles;
-        for (int kb = 0; kb < nkb; ++kb, ++c) {
-          if (c == STAGES && !flushed) flush();
-          if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
+      FragIter fi{my_start, my_end, p.nkb};
+      int tile, kb0, kb1;
+      bool ok = true;
+      while (ok && !*abort_flag && fi.next(tile, kb0, kb1)) {
+        const int wt = tile / p.ttiles, tt = tile - wt * p.ttiles;
+        for (int kb = kb0; kb < kb1; ++kb, ++c) {
+          if (c == RST && !flushed) flush();
+          if (!ptx::mbar_wait_bounded(&rempty[r], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
             give_up();
+            ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[s], C::X_BYTES + WC_BYTES + WS_BYTES);
-          ptx::tma_load_2d(st_wc(s), &tm_w, &full[s], kb * (BK / 2), wt * 128, pol_w);
-          ptx::bulk_load(st_ws(s), p.wsf + ((size_t)wt * cp4 + kb) * 512, WS_BYTES, &full[s], pol_w);
-          if (c < STAGES) {
-            pend_s[npend] = s;
+          ptx::mbar_arrive_expect_tx(&rfull[r], C::X_BYTES + WC_BYTES + WS_BYTES);
+          ptx::tma_load_2d(st_wc(r), &tm_w, &rfull[r], kb * (BK / 2), wt * 128, pol_w);
+          ptx::bulk_load(st_ws(r), p.wsf + ((size_t)wt * cp4 + kb) * 512, WS_BYTES, &rfull[r], pol_w);
+          if (c < RST) {
+            pend_r[npend] = r;
             pend_kb[npend] = kb;
             pend_tt[npend] = tt;
             ++npend;
           } else {
-            load_x(s, kb, tt);
+            load_x(r, kb, tt);
           }
-          issued_mask |= 1u << s;
-          issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          issued_mask |= 1u << r;
+          issued_parity = (issued_parity & ~(1u << r)) | (ph << r);
+          if (++r == RST) { r = 0; ph ^= 1u; }
         }
       }
       if (!flushed) flush();
     }
   } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
     pdl_wait();
     if (ptx::elect_one()) {
       // kind::f16: F32 accumulator (bits 4-5 = 1), A = B = BF16 (1), K-major,
       // N >> 3 in bits 17-22, M = 128 >> 4 in bits 24-28
       constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) | (8u << 24);
-      int s = 0;
-      uint32_t ph = 0;
-      int it = 0;
-      for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x, ++it) {
+      int r = 0, d = 0, it = 0;
+      uint32_t rph = 0, dph = 0;
+      FragIter fi{my_start, my_end, p.nkb};
+      int tile, kb0, kb1;
+      for (; !*abort_flag && fi.next(tile, kb0, kb1); ++it) {
         const int ab = it & 1;
         if (!ptx::mbar_wait_bounded(&tempty[ab], (uint32_t)((it >> 1) & 1) ^ 1u, limit, kTimeoutNs, abort_flag)) {
           give_up();
@@ -217,59 +255,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!ptx::mbar_wait_bounded(&full[s], ph, limit, kTimeoutNs, abort_flag) ||
-              !ptx::mbar_wait_bounded(&conv[s], ph, limit, kTimeoutNs, abort_flag)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+          // the converters released the tile after seeing the raw stage
+          // complete; the raw stage's wait is for the activation tile
+          if (!ptx::mbar_wait_bounded(&dfull[d], dph, limit, kTimeoutNs, abort_flag) ||
+              !ptx::mbar_wait_bounded(&rfull[r], rph, limit, kTimeoutNs, abort_flag)) {
             give_up();
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t wb = ptx::smem_u32(st_wb(s)), xs = ptx::smem_u32(st_x(s));
+          const uint32_t wb = ptx::smem_u32(st_wb(d)), xs = ptx::smem_u32(st_x(r));
 #pragma unroll
           for (int j = 0; j < BK / 16; ++j)
             ptx::mma_bf16(tmem + ab * NT, ptx::smem_desc(wb + 32 * j, 16, 1024, 2),
-                          ptx::smem_desc(xs + 32 * j, 16, 1024, 2), idesc, (kb | j) != 0);
+                          ptx::smem_desc(xs + 32 * j, 16, 1024, 2), idesc, (kb != kb0) || (j != 0));
           mma_issued = true;
-          ptx::tc_commit(&empty[s]);
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          ptx::tc_commit(&dempty[d]);
+          ptx::tc_commit(&rempty[r]);
+          if (++d == DSTAGES) { d = 0; dph ^= 1u; }
+          if (++r == RST) { r = 0; rph ^= 1u; }
         }
         if (!ok) break;
         ptx::tc_commit(&tfull[ab]);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kConvWarps) {
     // ---------------------------------------------------------- converters
     pdl_wait();
-    const int r = threadIdx.x - 64;             // weight row of the tile, 0..127
-    const int swz = r & 7;
-    int s = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const bool got = ptx::mbar_wait_bounded(&full[s], ph, limit, kTimeoutNs, abort_flag);
-        if (!got) give_up();
-        if (ptx::bar_any(1, 128, !got || *abort_flag)) {   // the four warps leave together
+    const int cw = warp - 2;
+    FragIter fi{my_start, my_end, p.nkb};
+    int tile, kb0, kb1;
+    int j = 0;                                  // index of the k-block in this CTA's sequence
+    bool ok = !C::WHOLE_KB || cw < DSTAGES;     // spare warps have no tile
+    // A warp walks its k-blocks in order and waits for its tile's release
+    // before the raw stage (RSTAGES >= DSTAGES), so no barrier parity is
+    // ambiguous; no barrier joins the converter warps.
+    while (ok && fi.next(tile, kb0, kb1)) {
+      for (int kb = kb0; kb < kb1; ++kb, ++j) {
+        if (C::WHOLE_KB && j % DSTAGES != cw) continue;
+        const int r = j % RST, d = j % DSTAGES;
+        const uint32_t rph = (uint32_t)((j / RST) & 1), dph = (uint32_t)((j / DSTAGES) & 1);
+        bool got = ptx::mbar_wait_bounded(&dempty[d], dph ^ 1u, limit, kTimeoutNs, abort_flag);
+        if (got) got = ptx::mbar_wait_bounded(&rfull[r], rph, limit, kTimeoutNs, abort_flag);
+        if (__any_sync(0xffffffffu, !got)) {   // the warp leaves together
+          give_up();
           ok = false;
           break;
         }
-        const uint4 *codes = reinterpret_cast<const uint4 *>(st_wc(s) + r * (BK / 2));
-        const uint4 c0 = codes[0], c1 = codes[1];
-        const uint32_t sfw =
-            *reinterpret_cast<const uint32_t *>(st_ws(s) + ((r & 31) << 4) + (((r >> 5) & 3) << 2));
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint8_t *rowp = st_wb(s) + (r >> 3) * 1024 + (r & 7) * 128;
+        if constexpr (C::WHOLE_KB) {
+          // the whole 128 x 64 tile: lane l takes rows l, l+32, l+64, l+96
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {           // 16-byte chunk c = elements 8c .. 8c+7
-          uint32_t o[4];
-          dequant8(cw[c], e4m3_to_h2((sfw >> (8 * (c >> 1))) & 0xFFu), o);
-          *reinterpret_cast<uint4 *>(rowp + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int rr = 0; rr < 4; ++rr) {
+            const int row = lane + 32 * rr;
+            const uint4 *codes = reinterpret_cast<const uint4 *>(st_wc(r) + row * (BK / 2));
+            const uint4 c0 = codes[0], c1 = codes[1];
+            const uint32_t sfw =
+                *reinterpret_cast<const uint32_t *>(st_ws(r) + ((row & 31) << 4) + (((row >> 5) & 3) << 2));
+            const uint32_t cwd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            uint8_t *rowp = st_wb(d) + (row >> 3) * 1024 + (row & 7) * 128;
+            const int swz = row & 7;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {       // 16-byte chunk c = elements 8c .. 8c+7
+              uint32_t o[4];
+              dequant8(cwd[c], e4m3_to_h2((sfw >> (8 * (c >> 1))) & 0xFFu), o);
+              *reinterpret_cast<uint4 *>(rowp + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        } else {
+          // 16 rows of the tile: two lanes per row, 32 elements each
+          const int row = 16 * cw + (lane >> 1), hf = lane & 1;
+          const uint4 cv = *reinterpret_cast<const uint4 *>(st_wc(r) + row * (BK / 2) + hf * 16);
+          const uint32_t sfw =
+              *reinterpret_cast<const uint32_t *>(st_ws(r) + ((row & 31) << 4) + (((row >> 5) & 3) << 2));
+          const uint32_t cwd[4] = {cv.x, cv.y, cv.z, cv.w};
+          uint8_t *rowp = st_wb(d) + (row >> 3) * 1024 + (row & 7) * 128;
+          const int swz = row & 7;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = 4 * hf + i;
+            uint32_t o[4];
+            dequant8(cwd[i], e4m3_to_h2((sfw >> (8 * (c >> 1))) & 0xFFu), o);
+            *reinterpret_cast<uint4 *>(rowp + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
         }
         fence_proxy_async();                     // generic-proxy writes -> tensor-core reads
-        conv_bar();
-        if (r == 0) ptx::mbar_arrive(&conv[s]);
-        if (++s == STAGES) { s = 0; ph ^= 1u; }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&dfull[d]);
       }
     }
   } else {
@@ -277,47 +349,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    const int et = threadIdx.x - (64 + kConvThreads);
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
     const float alpha = __ldg(p.alpha);
+    constexpr int TG = NT < 32 ? NT : 32;        // tokens summed per pass of the reduction
     int it = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
+    FragIter fi{my_start, my_end, p.nkb};
+    int tile, kb0, kb1;
+    for (; fi.next(tile, kb0, kb1); ++it) {
       const int ab = it & 1;
-      if (!ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag)) {
-        give_up();
-        break;
-      }
+      const bool got = ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag);
+      if (!got) give_up();
+      if (ptx::bar_any(2, 128, !got || *abort_flag)) break;   // the four warps leave together
       ptx::tc_fence_after();
-      const int wt = tile / p.ttiles, tt = tile % p.ttiles;
+      const int wt = tile / p.ttiles, tt = tile - wt * p.ttiles;
       const int n = wt * 128 + row;
       const int t0 = tt * NT;
+      const int mt = min(p.m - t0, NT);
+      const int64_t c_first = part.cta_of((int64_t)tile * p.nkb);
+      const int64_t c_last = part.cta_of((int64_t)tile * p.nkb + p.nkb - 1);
+      if (c_last == c_first) {
+        // the whole tile is this CTA's: straight to the output
+#pragma unroll 1
+        for (int c = 0; c < NT / 16; ++c) {
+          uint32_t v[16];
+          ptx::tmem_ld16(t_row + ab * NT + 16 * c, v);
+          ptx::tmem_wait_ld();
+          if (n < p.n) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int tk = 16 * c + i;
+              if (tk < mt) {
+                const __nv_bfloat16 o = __float2bfloat16_rn(alpha * __uint_as_float(v[i]));
+                p.d[(size_t)(t0 + tk) * p.n + n] = *reinterpret_cast<const uint16_t *>(&o);
+              }
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tempty[ab]);
+        continue;
+      }
+      // shared tile: this CTA's fp32 partial to the workspace; the last
+      // contributor to arrive sums all of them in K order
+      auto slot = [&](int64_t cc) {
+        return p.partials + ((size_t)cc * p.maxfrag + (size_t)(tile - part.start(cc) / p.nkb)) * NT * 128;
+      };
+      float *mine = slot(blockIdx.x);
 #pragma unroll 1
       for (int c = 0; c < NT / 16; ++c) {
         uint32_t v[16];
         ptx::tmem_ld16(t_row + ab * NT + 16 * c, v);
         ptx::tmem_wait_ld();
-        if (n < p.n) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int t = t0 + 16 * c + i;
-            if (t < p.m) {
-              const __nv_bfloat16 o = __float2bfloat16_rn(alpha * __uint_as_float(v[i]));
-              p.d[(size_t)t * p.n + n] = *reinterpret_cast<const uint16_t *>(&o);
-            }
-          }
-        }
+        for (int i = 0; i < 16; ++i)
+          if (16 * c + i < mt) mine[(16 * c + i) * 128 + row] = __uint_as_float(v[i]);
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tempty[ab]);
+      epi_bar();                    // every partial write of the CTA precedes the release below
+      if (et == 0)
+        *last_flag = atom_add_acq_rel_gpu(&p.counters[tile], 1) == (uint32_t)(c_last - c_first);
+      epi_bar();
+      if (!*last_flag) continue;
+      if (et == 0) p.counters[tile] = 0;
+#pragma unroll 1
+      for (int g0 = 0; g0 < mt; g0 += TG) {
+        float acc[TG];
+#pragma unroll
+        for (int i = 0; i < TG; ++i) acc[i] = 0.0f;
+        for (int64_t cc = c_first; cc <= c_last; ++cc) {       // K order
+          const float *pc = slot(cc) + (size_t)g0 * 128 + row;
+          float tmp[TG];
+#pragma unroll
+          for (int i = 0; i < TG; ++i) tmp[i] = (g0 + i < mt) ? __ldcg(pc + i * 128) : 0.0f;
+#pragma unroll
+          for (int i = 0; i < TG; ++i) acc[i] += tmp[i];
+        }
+        if (n < p.n) {
+#pragma unroll
+          for (int i = 0; i < TG; ++i)
+            if (g0 + i < mt) {
+              const __nv_bfloat16 o = __float2bfloat16_rn(alpha * acc[i]);
+              p.d[(size_t)(t0 + g0 + i) * p.n + n] = *reinterpret_cast<const uint16_t *>(&o);
+            }
+        }
+      }
     }
   }
 
   __syncthreads();
   if (*abort_flag) {
     if (warp == 0 && issued_mask) {
-      for (int s = 0; s < STAGES; ++s)
-        if (issued_mask & (1u << s)) {
+      for (int r = 0; r < RST; ++r)
+        if (issued_mask & (1u << r)) {
           volatile int no_abort = 0;
-          ptx::mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, kDrainPolls, 0, &no_abort);
+          ptx::mbar_wait_bounded(&rfull[r], (issued_parity >> r) & 1u, kDrainPolls, 0, &no_abort);
         }
     }
     if (warp == 1 && mma_issued) {
@@ -332,9 +459,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+int pick_nt(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : m <= 128 ? 128 : 256; }
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Work split of one call: split-K over (tile, k-block) pairs for up to 64
+// tokens (one token tile), whole tiles otherwise.
+struct Plan {
+  int nt, wtiles, ttiles, nkb, grid, maxfrag;
+  bool can_split;
+  size_t ws_bytes;   // workspace the split needs (0: none)
+};
+
+Plan make_plan(int64_t m, int64_t n, int64_t k) {
+  Plan pl{};
+  pl.nt = pick_nt(m);
+  pl.wtiles = (int)((n + 127) / 128);
+  pl.ttiles = (int)((m + pl.nt - 1) / pl.nt);
+  pl.nkb = (int)(k / BK);
+  const int tiles = pl.wtiles * pl.ttiles;
+  pl.can_split = pl.nt <= 64;
+  if (pl.can_split) {
+    const int64_t w = (int64_t)tiles * pl.nkb;
+    pl.grid = (int)(w < num_sms() ? w : num_sms());
+    const int64_t per = (w + pl.grid - 1) / pl.grid;
+    pl.maxfrag = (int)((per + pl.nkb - 1) / pl.nkb + 1);
+    const bool shared = (w % pl.grid != 0) || ((w / pl.grid) % pl.nkb != 0);
+    pl.ws_bytes = shared ? round256((size_t)tiles * 4) + (size_t)pl.grid * pl.maxfrag * pl.nt * 128 * 4 : 0;
+  } else {
+    pl.grid = tiles < num_sms() ? tiles : num_sms();
+  }
+  return pl;
+}
+
 template <int NT>
-cudaError_t launch_nt(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, const float *alpha, uint16_t *d,
-                      int64_t m, int64_t n, int64_t k, uint32_t wait_limit, cudaStream_t st) {
+cudaError_t launch_nt(const Plan &pl, const uint16_t *x, const uint8_t *w, const uint8_t *wsf, const float *alpha,
+                      uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws, size_t ws_bytes, uint32_t wait_limit,
+                      cudaStream_t st) {
   using C = Cfg<NT>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -349,21 +510,35 @@ cudaError_t launch_nt(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, c
   if (!make_byte_map(&tm_x, x, m, k * 2, 128, NT, true) || !make_byte_map(&tm_w, w, n, k / 2, 32, 128, false))
     return cudaErrorInvalidValue;
   W4A16Args a{};
-  a.w = w;
   a.wsf = wsf;
   a.alpha = alpha;
   a.d = d;
   a.m = (int32_t)m;
   a.n = (int32_t)n;
   a.k = (int32_t)k;
-  a.wtiles = (int32_t)((n + 127) / 128);
-  a.ttiles = (int32_t)((m + NT - 1) / NT);
+  a.wtiles = pl.wtiles;
+  a.ttiles = pl.ttiles;
+  a.nkb = pl.nkb;
+  const bool split = pl.can_split && (pl.ws_bytes == 0 || (ws != nullptr && ws_bytes >= pl.ws_bytes));
+  if (split) {
+    a.grid = pl.grid;
+    a.maxfrag = pl.maxfrag;
+    a.split_ok = 1;
+    if (pl.ws_bytes) {
+      a.counters = static_cast<int *>(ws);
+      a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
+                                             round256((size_t)pl.wtiles * pl.ttiles * 4));
+    }
+  } else {
+    const int tiles = pl.wtiles * pl.ttiles;
+    a.grid = tiles < num_sms() ? tiles : num_sms();
+    a.maxfrag = 1;
+    a.split_ok = 0;
+  }
   a.wait_limit = wait_limit;
   a.status = device_status_ptr();
   if (!a.status) return cudaErrorInvalidValue;
-  const int tiles = a.wtiles * a.ttiles;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_pdl(w4a16_kernel<NT>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, st, tm_x, tm_w, a);
+  return launch_pdl(w4a16_kernel<NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_x, tm_w, a);
 }
 
 }  // namespace
@@ -373,14 +548,23 @@ bool w4a16_tc_supported(int64_t m, int64_t n, int64_t k) {
          k < (1 << 29);
 }
 
+size_t w4a16_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+  if (!w4a16_tc_supported(m, n, k)) return 0;
+  return make_plan(m, n, k).ws_bytes;
+}
+
 cudaError_t launch_w4a16_tc(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, const float *alpha,
-                            uint16_t *d, int64_t m, int64_t n, int64_t k, uint32_t wait_limit, cudaStream_t st) {
+                            uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws, size_t ws_bytes,
+                            uint32_t wait_limit, cudaStream_t st) {
   if (!w4a16_tc_supported(m, n, k)) return cudaErrorNotSupported;
-  if (m <= 16) return launch_nt<16>(x, w, wsf, alpha, d, m, n, k, wait_limit, st);
-  if (m <= 32) return launch_nt<32>(x, w, wsf, alpha, d, m, n, k, wait_limit, st);
-  if (m <= 64) return launch_nt<64>(x, w, wsf, alpha, d, m, n, k, wait_limit, st);
-  if (m <= 128) return launch_nt<128>(x, w, wsf, alpha, d, m, n, k, wait_limit, st);
-  return launch_nt<256>(x, w, wsf, alpha, d, m, n, k, wait_limit, st);
+  const Plan pl = make_plan(m, n, k);
+  switch (pl.nt) {
+    case 16: return launch_nt<16>(pl, x, w, wsf, alpha, d, m, n, k, ws, ws_bytes, wait_limit, st);
+    case 32: return launch_nt<32>(pl, x, w, wsf, alpha, d, m, n, k, ws, ws_bytes, wait_limit, st);
+    case 64: return launch_nt<64>(pl, x, w, wsf, alpha, d, m, n, k, ws, ws_bytes, wait_limit, st);
+    case 128: return launch_nt<128>(pl, x, w, wsf, alpha, d, m, n, k, ws, ws_bytes, wait_limit, st);
+    default: return launch_nt<256>(pl, x, w, wsf, alpha, d, m, n, k, ws, ws_bytes, wait_limit, st);
+  }
 }
 
 }  // namespace nvfp4

@@ -88,10 +88,14 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
                           cudaStream_t st, const float *a_row_scale = nullptr);
 
 // W4A16 on the tensor cores (weights dequantized to bf16 in shared memory).
+// With a workspace of w4a16_workspace_bytes (zero-filled once; counters left
+// at zero), up to 64 tokens are split across CTAs along K; otherwise every
+// CTA owns whole weight tiles.
 bool w4a16_tc_supported(int64_t m, int64_t n, int64_t k);
+size_t w4a16_workspace_bytes(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_w4a16_tc(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, const float *alpha,
-                            uint16_t *d, int64_t m, int64_t n, int64_t k, uint32_t wait_limit,
-                            cudaStream_t st);
+                            uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws, size_t ws_bytes,
+                            uint32_t wait_limit, cudaStream_t st);
 
 // Whole decode MLP in one persistent kernel (mlp_decode.cu).
 struct MlpDecodeParams {

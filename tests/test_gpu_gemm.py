@@ -54,10 +54,20 @@ def run_swiglu(nv, xq, xs, wdev, alpha, gs_h, m, n, k, algo):
     return host(q), lin
 
 
-def run_w4a16(nv, xbits, wdev, alpha, m, n, k, algo):
+def run_w4a16(nv, xbits, wdev, alpha, m, n, k, algo, split=False):
+    """split: pass the split-K workspace (tokens <= 64 then run split along K
+    over all SMs; without it every SM owns whole weight tiles)."""
     d = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
-    nv.bf16_fp4_gemm_ex(bf16_dev(xbits), wdev[0], wdev[1], scalar(alpha), d, m, n, k, algo=algo)
+    nbytes = nv.bf16_fp4_gemm_workspace_bytes(m, n, k, algo) if split else 0
+    ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device="cuda") if split else None
+    x = bf16_dev(xbits)
+    nv.bf16_fp4_gemm_ex(x, wdev[0], wdev[1], scalar(alpha), d, m, n, k, ws, nbytes, algo=algo)
     torch.cuda.synchronize()
+    if split and nbytes:
+        first = bf16_host(d)
+        nv.bf16_fp4_gemm_ex(x, wdev[0], wdev[1], scalar(alpha), d, m, n, k, ws, nbytes, algo=algo)
+        torch.cuda.synchronize()
+        assert np.array_equal(bf16_host(d), first), "second split call on the same workspace differs"
     return bf16_host(d)
 
 
@@ -269,16 +279,35 @@ def test_w4a16_small_shapes(lib, m, n, k, algo):
     print(f"w4a16 algo={algo} m={m} n={n} k={k}: rel err {err:.2e}")
 
 
+# split-K along K (workspace given): tiles shared by 2..5 CTAs, ragged tails
+W4A16_SPLIT = [(1, 256, 512), (5, 96, 320), (16, 1024, 256), (33, 128, 1024), (64, 384, 2048),
+               (16, 2048, 4096), (3, 160, 640)]
+
+
+@pytest.mark.parametrize("m,n,k", W4A16_SPLIT)
+def test_w4a16_split_k_small_shapes(lib, m, n, k):
+    ws = small_weights(n, k, 8)
+    xbits, x = synth.activations(4, m, k)
+    alpha = np.float32(1.0) / ws.gs
+    assert lib.bf16_fp4_gemm_workspace_bytes(m, n, k, TC) > 0      # tiles really are shared
+    got = run_w4a16(lib, xbits, ws.device_prepared(lib), alpha, m, n, k, TC, split=True)
+    ref = oracle.gemm_w4a16(x, ws.packed, ws.sf, alpha)
+    err = assert_gemm_close(got, ref)
+    print(f"w4a16 split m={m} n={n} k={k}: rel err {err:.2e}")
+
+
 @pytest.mark.parametrize("which", ["gate_up", "down"])
-@pytest.mark.parametrize("m,algo", [(1, GEMV), (16, GEMV), (1, TC), (16, TC), (128, TC), (1024, TC)])
-def test_w4a16_full_size_sampled(lib, m, which, algo):
+@pytest.mark.parametrize("m,algo,split", [(1, GEMV, False), (16, GEMV, False), (1, TC, False), (16, TC, False),
+                                          (1, TC, True), (16, TC, True), (64, TC, True), (128, TC, False),
+                                          (1024, TC, False)])
+def test_w4a16_full_size_sampled(lib, m, which, algo, split):
     ws = weights(4, which)
     if which == "gate_up":
         xbits, x = synth.activations(4, m)
     else:
         xbits, x = synth.to_bf16_bits(synth.random_matrix((m, ws.k), (23, m), scale=0.1))
     alpha = np.float32(1.0) / ws.gs
-    got = run_w4a16(lib, xbits, ws.device_prepared(lib), alpha, m, ws.n, ws.k, algo)
+    got = run_w4a16(lib, xbits, ws.device_prepared(lib), alpha, m, ws.n, ws.k, algo, split)
     cols = sample_rows(ws.n, 512, seed=m + 3)
     toks = sample_rows(m, 128, seed=m + 4)
     ref = oracle.gemm_w4a16(x[toks], ws.packed[cols], ws.sf[cols], alpha)

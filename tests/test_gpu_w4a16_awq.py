@@ -29,7 +29,11 @@ GEMV, TC = 1, 2
 def run_prescaled(nv, xbits, sbits, wdev, alpha, m, n, k, algo):
     d = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
     nbytes = nv.bf16_fp4_gemm_prescaled_workspace_bytes(m, n, k, algo)
-    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda") if nbytes else None
+    # the scaled-activation part needs no initial contents; the split-K part
+    # after it must start zero-filled
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+    if nbytes:
+        ws[:(m * k * 2 + 255) // 256 * 256].fill_(0x7F)
     x = bf16_dev(xbits)
     nv.bf16_fp4_gemm_prescaled(x, bf16_dev(sbits), wdev[0], wdev[1], scalar(alpha), d, m, n, k, ws, nbytes,
                                algo=algo)
