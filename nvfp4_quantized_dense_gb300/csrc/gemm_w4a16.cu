@@ -22,9 +22,15 @@
 // arrive, which sums the fp32 partials in K order.  Without a workspace, or
 // for more tokens, every CTA owns whole tiles.
 //
-// Roles (448 threads, one CTA per SM): warp 0 TMA producer, warp 1 TMEM owner
-// + MMA issuer, warps 2..9 converters, warps
-// 10..13 epilogue.  Bounded waits as in gemm_tc.cu.
+// Roles (512 threads, one CTA per SM): warp 0 TMA producer, warp 1 TMEM owner
+// + MMA issuer, warps 2..9 converters, warps 10..13 epilogue, warp 14 second
+// MMA issuer, warp 15 second producer.  At decode sizes a single thread that
+// loads, or issues the MMAs of, every k-block is the bound (a barrier wait
+// costs ~170 cycles even when the phase is complete, a small MMA ~50, a
+// commit ~45), so up to 128 tokens the k-blocks of the CTA's sequence
+// alternate between two producers and two issuers; each issuer accumulates
+// into its own TMEM columns and the epilogue adds the two.  Bounded waits as
+// in gemm_tc.cu.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -41,7 +47,9 @@ constexpr uint32_t WS_BYTES = 512;          // one 128x4 scale tile
 constexpr uint32_t WB_BYTES = 128 * BK * 2; // dequantized weight tile, 16 KB
 constexpr int kConvWarps = 8;               // converter warps
 constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kThreads = 64 + kConvThreads + 128;
+constexpr int kWarpMma2 = 2 + kConvWarps + 4;   // second MMA issuer
+constexpr int kWarpProd2 = kWarpMma2 + 1;       // second producer
+constexpr int kThreads = 64 + kConvThreads + 128 + 64;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kDrainPolls = 1u << 22;
 
@@ -56,15 +64,21 @@ struct Cfg {
   static constexpr bool WHOLE_KB = NT <= 64;
   static constexpr int DSTAGES = NT <= 32 ? 8 : NT == 64 ? 6 : 4;         // dequantized tiles
   static_assert(!WHOLE_KB || DSTAGES <= kConvWarps, "one converter warp per dequantized tile");
-  static constexpr int RSTAGES_FIT = (int)((220u * 1024 - DSTAGES * WB_BYTES) / RAW_BYTES);
+  static constexpr int NI = NT <= 128 ? 2 : 1;                             // MMA issuers
+  static constexpr int RSTAGES_FIT = (int)((220u * 1024 - DSTAGES * WB_BYTES) / RAW_BYTES) / NI * NI;
   static constexpr int RSTAGES = RSTAGES_FIT > 32 ? 32 : RSTAGES_FIT;   // raw k-blocks in flight
+  // issuer i takes the k-blocks j with j % NI == i: with both ring depths
+  // multiples of NI every ring barrier serves one issuer, in order
+  static_assert(RSTAGES % NI == 0 && DSTAGES % NI == 0, "ring barriers per issuer");
   static_assert(RSTAGES >= DSTAGES, "raw ring at least as deep as the dequantized one");
   static constexpr uint32_t BAR_BYTES = 1024;
   static constexpr uint32_t SMEM_BYTES = DSTAGES * WB_BYTES + RSTAGES * RAW_BYTES + BAR_BYTES + 1024;
-  static constexpr uint32_t TMEM_COLS = 2 * NT <= 32 ? 32 : 2 * NT <= 64 ? 64 : 2 * NT <= 128 ? 128 : 2 * NT <= 256 ? 256 : 512;
+  static constexpr uint32_t ACC_COLS = 2 * NI * NT;                       // two tiles x NI issuers
+  static constexpr uint32_t TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
+  static_assert(ACC_COLS <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(RSTAGES >= 4, "pipeline depth");
-  static_assert((2 * RSTAGES + 2 * DSTAGES + 5) * 8 + 16 <= BAR_BYTES, "barrier area");
+  static_assert((2 * RSTAGES + 2 * DSTAGES + 6) * 8 + 16 <= BAR_BYTES, "barrier area");
 };
 
 struct W4A16Args {
@@ -88,7 +102,7 @@ __device__ __forceinline__ void fence_proxy_async() {
 // Eight codes (one 32-bit word) times one E4M3 scale -> four bf16x2, exact:
 // E2M1 -> f16x2, times the scale in f16 (product within f16's normal range and
 // precision), widened to f32 and rounded to bf16 (no rounding happens: the
-// values have at most 5 significant bits).
+// values have at most 6 significant bits).
 __device__ __forceinline__ void dequant8(uint32_t codes, uint32_t scale_h2, uint32_t (&out)[4]) {
   uint32_t h[4];
   asm("{\n"
@@ -120,7 +134,7 @@ __device__ __forceinline__ uint32_t e4m3_to_h2(uint32_t byte) {
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 registers
     w4a16_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                  const W4A16Args p) {
   using C = Cfg<NT>;
@@ -139,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *tfull = dempty + DSTAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 2);   // drain: one per issuer
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   volatile int *last_flag = abort_flag + 1;
 
@@ -155,10 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&dempty[d], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&tfull[b], 1);
+      ptx::mbar_init(&tfull[b], C::NI);      // one commit per issuer
       ptx::mbar_init(&tempty[b], 128);
+      ptx::mbar_init(&drain[b], 1);
     }
-    ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tm_x);
@@ -185,18 +199,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (ptx::elect_one()) {
+  if (warp == 0 || warp == kWarpProd2) {
+    // ----------------------------------------------------------- producers
+    // producer p fills the raw stages of the k-blocks j with j % NI == p
+    const int prod = warp == 0 ? 0 : 1;
+    if (prod < C::NI && ptx::elect_one()) {
       const uint64_t pol_w = ptx::l2_policy_evict_first();
       const uint64_t pol_x = ptx::l2_policy_evict_last();
-      int r = 0;
+      int r = 0, j = 0;
       uint32_t ph = 0;
-      // The first RST raw stages get their weight codes and scales before
-      // the previous kernel on the stream has finished; their activation
-      // tiles follow once it has.
+      // The raw stages of the first RST k-blocks get their weight codes and
+      // scales before the previous kernel on the stream has finished; their
+      // activation tiles follow once it has.
       int pend_r[RST], pend_kb[RST], pend_tt[RST];
-      int npend = 0, c = 0;
+      int npend = 0;
       bool flushed = false;
       auto load_x = [&](int st, int kb, int tt) {
         ptx::tma_load_2d(st_x(st), &tm_x, &rfull[st], kb * (BK * 2), tt * NT, pol_x);
@@ -211,55 +227,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && !*abort_flag && fi.next(tile, kb0, kb1)) {
         const int wt = tile / p.ttiles, tt = tile - wt * p.ttiles;
-        for (int kb = kb0; kb < kb1; ++kb, ++c) {
-          if (c == RST && !flushed) flush();
-          if (!ptx::mbar_wait_bounded(&rempty[r], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
-            give_up();
-            ok = false;
-            break;
+        for (int kb = kb0; kb < kb1; ++kb, ++j) {
+          if (C::NI == 1 || (j & 1) == prod) {
+            // a stage is reused only after this producer's own earlier
+            // activation tiles are in flight
+            if (j >= RST && !flushed) flush();
+            if (!ptx::mbar_wait_bounded(&rempty[r], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&rfull[r], C::X_BYTES + WC_BYTES + WS_BYTES);
+            ptx::tma_load_2d(st_wc(r), &tm_w, &rfull[r], kb * (BK / 2), wt * 128, pol_w);
+            ptx::bulk_load(st_ws(r), p.wsf + ((size_t)wt * cp4 + kb) * 512, WS_BYTES, &rfull[r], pol_w);
+            if (j < RST) {
+              pend_r[npend] = r;
+              pend_kb[npend] = kb;
+              pend_tt[npend] = tt;
+              ++npend;
+            } else {
+              load_x(r, kb, tt);
+            }
+            issued_mask |= 1u << r;
+            issued_parity = (issued_parity & ~(1u << r)) | (ph << r);
           }
-          ptx::mbar_arrive_expect_tx(&rfull[r], C::X_BYTES + WC_BYTES + WS_BYTES);
-          ptx::tma_load_2d(st_wc(r), &tm_w, &rfull[r], kb * (BK / 2), wt * 128, pol_w);
-          ptx::bulk_load(st_ws(r), p.wsf + ((size_t)wt * cp4 + kb) * 512, WS_BYTES, &rfull[r], pol_w);
-          if (c < RST) {
-            pend_r[npend] = r;
-            pend_kb[npend] = kb;
-            pend_tt[npend] = tt;
-            ++npend;
-          } else {
-            load_x(r, kb, tt);
-          }
-          issued_mask |= 1u << r;
-          issued_parity = (issued_parity & ~(1u << r)) | (ph << r);
           if (++r == RST) { r = 0; ph ^= 1u; }
         }
       }
       if (!flushed) flush();
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kWarpMma2) {
     // ----------------------------------------------------------------- MMA
+    const int issuer = warp == 1 ? 0 : 1;
     pdl_wait();
-    if (ptx::elect_one()) {
+    if (issuer < C::NI && ptx::elect_one()) {
       // kind::f16: F32 accumulator (bits 4-5 = 1), A = B = BF16 (1), K-major,
       // N >> 3 in bits 17-22, M = 128 >> 4 in bits 24-28
       constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) | (8u << 24);
-      int r = 0, d = 0, it = 0;
-      uint32_t rph = 0, dph = 0;
+      int r = 0, d = 0, it = 0, j = 0;
+      uint32_t dph = 0;
+      auto advance = [&]() {
+        ++j;
+        if (++d == DSTAGES) { d = 0; dph ^= 1u; }
+        if (++r == RST) r = 0;
+      };
       FragIter fi{my_start, my_end, p.nkb};
       int tile, kb0, kb1;
-      for (; !*abort_flag && fi.next(tile, kb0, kb1); ++it) {
+      bool ok = true;
+      for (; ok && !*abort_flag && fi.next(tile, kb0, kb1); ++it) {
         const int ab = it & 1;
         if (!ptx::mbar_wait_bounded(&tempty[ab], (uint32_t)((it >> 1) & 1) ^ 1u, limit, kTimeoutNs, abort_flag)) {
           give_up();
           break;
         }
         ptx::tc_fence_after();
-        bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          // the converters released the tile after seeing the raw stage
-          // complete; the raw stage's wait is for the activation tile
-          if (!ptx::mbar_wait_bounded(&dfull[d], dph, limit, kTimeoutNs, abort_flag) ||
-              !ptx::mbar_wait_bounded(&rfull[r], rph, limit, kTimeoutNs, abort_flag)) {
+        const uint32_t acc = tmem + (uint32_t)((ab * C::NI + issuer) * NT);
+        bool first = true;
+        for (int kb = kb0; kb < kb1; ++kb, advance()) {
+          if (C::NI > 1 && (j & 1) != issuer) continue;
+          // the converters filled the tile after they saw the raw stage,
+          // activation tile included, complete: no wait on the stage here
+          if (!ptx::mbar_wait_bounded(&dfull[d], dph, limit, kTimeoutNs, abort_flag)) {
             give_up();
             ok = false;
             break;
@@ -267,17 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const uint32_t wb = ptx::smem_u32(st_wb(d)), xs = ptx::smem_u32(st_x(r));
 #pragma unroll
-          for (int j = 0; j < BK / 16; ++j)
-            ptx::mma_bf16(tmem + ab * NT, ptx::smem_desc(wb + 32 * j, 16, 1024, 2),
-                          ptx::smem_desc(xs + 32 * j, 16, 1024, 2), idesc, (kb != kb0) || (j != 0));
+          for (int jj = 0; jj < BK / 16; ++jj)
+            ptx::mma_bf16(acc, ptx::smem_desc(wb + 32 * jj, 16, 1024, 2),
+                          ptx::smem_desc(xs + 32 * jj, 16, 1024, 2), idesc, !first || (jj != 0));
+          first = false;
           mma_issued = true;
           ptx::tc_commit(&dempty[d]);
           ptx::tc_commit(&rempty[r]);
-          if (++d == DSTAGES) { d = 0; dph ^= 1u; }
-          if (++r == RST) { r = 0; rph ^= 1u; }
         }
         if (!ok) break;
-        ptx::tc_commit(&tfull[ab]);
+        ptx::tc_commit(&tfull[ab]);          // also when this issuer had no k-block of the tile
       }
     }
   } else if (warp < 2 + kConvWarps) {
@@ -304,21 +331,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if constexpr (C::WHOLE_KB) {
-          // the whole 128 x 64 tile: lane l takes rows l, l+32, l+64, l+96
+          // the whole 128 x 64 tile in eight steps of 16 rows; lane pair
+          // (2i, 2i+1) takes the two 32-code halves of row 16s + i, so that
+          // every load instruction reads 512 contiguous bytes.  All loads
+          // first (the compiler cannot move them past the tile stores), the
+          // scales of rows i + 16u as two 16-byte loads.
+          const int hf = lane & 1, i = lane >> 1;
+          uint4 cv[8];
 #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            const int row = lane + 32 * rr;
-            const uint4 *codes = reinterpret_cast<const uint4 *>(st_wc(r) + row * (BK / 2));
-            const uint4 c0 = codes[0], c1 = codes[1];
-            const uint32_t sfw =
-                *reinterpret_cast<const uint32_t *>(st_ws(r) + ((row & 31) << 4) + (((row >> 5) & 3) << 2));
-            const uint32_t cwd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          for (int s8 = 0; s8 < 8; ++s8)
+            cv[s8] = *reinterpret_cast<const uint4 *>(st_wc(r) + (16 * s8 + i) * (BK / 2) + hf * 16);
+          // 16-byte scale row q holds the scales of rows q, q+32, q+64, q+96
+          const uint4 sa = *reinterpret_cast<const uint4 *>(st_ws(r) + i * 16);
+          const uint4 sb = *reinterpret_cast<const uint4 *>(st_ws(r) + (16 + i) * 16);
+          const uint32_t sfs[8] = {sa.x, sb.x, sa.y, sb.y, sa.z, sb.z, sa.w, sb.w};
+#pragma unroll
+          for (int s8 = 0; s8 < 8; ++s8) {
+            const int row = 16 * s8 + i;
+            const uint32_t cwd[4] = {cv[s8].x, cv[s8].y, cv[s8].z, cv[s8].w};
             uint8_t *rowp = st_wb(d) + (row >> 3) * 1024 + (row & 7) * 128;
             const int swz = row & 7;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {       // 16-byte chunk c = elements 8c .. 8c+7
+            for (int u = 0; u < 4; ++u) {
+              const int c = 4 * hf + u;         // 16-byte chunk c = elements 8c .. 8c+7
               uint32_t o[4];
-              dequant8(cwd[c], e4m3_to_h2((sfw >> (8 * (c >> 1))) & 0xFFu), o);
+              dequant8(cwd[u], e4m3_to_h2((sfs[s8] >> (8 * (c >> 1))) & 0xFFu), o);
               *reinterpret_cast<uint4 *>(rowp + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             }
           }
@@ -352,11 +389,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - (64 + kConvThreads);
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
     const float alpha = __ldg(p.alpha);
-    constexpr int TG = NT < 32 ? NT : 32;        // tokens summed per pass of the reduction
-    int it = 0;
+    constexpr int TG = 16;                       // tokens summed per pass of the reduction
+    int it = 0, j0 = 0;                          // j0: index of the fragment's first k-block
+    // 16 accumulator columns of tile buffer ab, summed over the issuers that
+    // had a k-block of the fragment (warp-uniform)
+    auto load_acc = [&](int ab, int c, bool p0, bool p1, float (&o)[16]) {
+      uint32_t v[16], w[16];
+      const uint32_t a0 = t_row + (uint32_t)(ab * C::NI * NT + 16 * c);
+      if (p0) ptx::tmem_ld16(a0, v);
+      if (C::NI > 1 && p1) ptx::tmem_ld16(a0 + NT, w);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        o[i] = (p0 ? __uint_as_float(v[i]) : 0.0f) + ((C::NI > 1 && p1) ? __uint_as_float(w[i]) : 0.0f);
+    };
     FragIter fi{my_start, my_end, p.nkb};
     int tile, kb0, kb1;
-    for (; fi.next(tile, kb0, kb1); ++it) {
+    for (; fi.next(tile, kb0, kb1); ++it, j0 += kb1 - kb0) {
       const int ab = it & 1;
       const bool got = ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag);
       if (!got) give_up();
@@ -368,19 +417,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = min(p.m - t0, NT);
       const int64_t c_first = part.cta_of((int64_t)tile * p.nkb);
       const int64_t c_last = part.cta_of((int64_t)tile * p.nkb + p.nkb - 1);
+      const bool p0 = C::NI == 1 || (j0 & 1) == 0 || kb1 - kb0 >= 2;
+      const bool p1 = C::NI > 1 && ((j0 & 1) == 1 || kb1 - kb0 >= 2);
       if (c_last == c_first) {
         // the whole tile is this CTA's: straight to the output
 #pragma unroll 1
         for (int c = 0; c < NT / 16; ++c) {
-          uint32_t v[16];
-          ptx::tmem_ld16(t_row + ab * NT + 16 * c, v);
-          ptx::tmem_wait_ld();
+          float v[16];
+          load_acc(ab, c, p0, p1, v);
           if (n < p.n) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int tk = 16 * c + i;
               if (tk < mt) {
-                const __nv_bfloat16 o = __float2bfloat16_rn(alpha * __uint_as_float(v[i]));
+                const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v[i]);
                 p.d[(size_t)(t0 + tk) * p.n + n] = *reinterpret_cast<const uint16_t *>(&o);
               }
             }
@@ -398,12 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float *mine = slot(blockIdx.x);
 #pragma unroll 1
       for (int c = 0; c < NT / 16; ++c) {
-        uint32_t v[16];
-        ptx::tmem_ld16(t_row + ab * NT + 16 * c, v);
-        ptx::tmem_wait_ld();
+        float v[16];
+        load_acc(ab, c, p0, p1, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          if (16 * c + i < mt) mine[(16 * c + i) * 128 + row] = __uint_as_float(v[i]);
+          if (16 * c + i < mt) mine[(16 * c + i) * 128 + row] = v[i];
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&tempty[ab]);
@@ -440,17 +489,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __syncthreads();
   if (*abort_flag) {
-    if (warp == 0 && issued_mask) {
+    if ((warp == 0 || warp == kWarpProd2) && issued_mask) {
       for (int r = 0; r < RST; ++r)
         if (issued_mask & (1u << r)) {
           volatile int no_abort = 0;
           ptx::mbar_wait_bounded(&rfull[r], (issued_parity >> r) & 1u, kDrainPolls, 0, &no_abort);
         }
     }
-    if (warp == 1 && mma_issued) {
+    if ((warp == 1 || warp == kWarpMma2) && mma_issued) {
       volatile int no_abort = 0;
-      ptx::tc_commit(drain);
-      ptx::mbar_wait_bounded(drain, 0, kDrainPolls, 0, &no_abort);
+      uint64_t *dr = &drain[warp == 1 ? 0 : 1];
+      ptx::tc_commit(dr);
+      ptx::mbar_wait_bounded(dr, 0, kDrainPolls, 0, &no_abort);
     }
   }
   ptx::tc_fence_before();
