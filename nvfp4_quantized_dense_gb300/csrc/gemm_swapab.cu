@@ -63,7 +63,8 @@ struct SwapArgs {
   int *counters;        // [tiles] arrival counters
   int32_t m, n, k;
   int32_t tiles, kb_total;   // weight tiles, k-blocks per tile
-  int32_t grid, maxfrag;     // CTAs, fragment slots per CTA
+  int32_t grid, maxfrag;     // CTAs, fragment slots per CTA (split tiles)
+  int32_t whole, split_tiles;   // mixed split: whole tiles per CTA, tiles shared by CTAs
   int32_t split_ok;          // 0: no workspace, every CTA owns whole tiles
   uint32_t wait_limit;
   int *status;
@@ -71,6 +72,19 @@ struct SwapArgs {
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// A CTA's fragments: the mixed split with a workspace, whole tiles without.
+struct WorkIter {
+  bool use_mixed;
+  MixedIter mi;
+  FragIter fi;
+  __device__ __forceinline__ WorkIter(bool m, const MixedPartition &mp, int64_t cta, int64_t start, int64_t end,
+                                      int64_t kbt)
+      : use_mixed(m), mi(mp, cta), fi{start, end, kbt} {}
+  __device__ __forceinline__ bool next(int &tile, int &kb0, int &kb1) {
+    return use_mixed ? mi.next(tile, kb0, kb1) : fi.next(tile, kb0, kb1);
+  }
+};
 
 template <int MODE, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -120,8 +134,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  const Partition part{(int64_t)p.tiles * p.kb_total, p.grid, p.kb_total, p.split_ok == 0, p.tiles};
+  // With a workspace: the mixed split (the tiles shared by CTAs first, then
+  // whole tiles of its own), so that no CTA ends its run with a reduction.
+  // Without: whole tiles per CTA.
+  const MixedPartition mixed{p.kb_total, p.grid, p.whole, p.split_tiles};
+  const Partition part{(int64_t)p.tiles * p.kb_total, p.grid, p.kb_total, true, p.tiles};
   const int64_t my_start = part.start(blockIdx.x), my_end = part.start(blockIdx.x + 1);
+  auto work = [&]() { return WorkIter(p.split_ok != 0, mixed, blockIdx.x, my_start, my_end, p.kb_total); };
   const int ksteps_total = p.k >> 6;
   const int cp4 = ksteps_total;          // 512-byte scale tiles per 128-row block
   const uint32_t limit = p.wait_limit;
@@ -134,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = ptx::l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0;
-      FragIter fi{my_start, my_end, p.kb_total};
+      WorkIter fi = work();
       int tile, kb0, kb1;
       // The first STAGES stages get their weight tiles before the previous
       // kernel on the stream has finished; their activation tiles (that
@@ -187,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
-      FragIter fi{my_start, my_end, p.kb_total};
+      WorkIter fi = work();
       int tile, kb0, kb1;
       for (; !*abort_flag && fi.next(tile, kb0, kb1); ++it) {
         const int ab = it & 1;
@@ -235,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float alpha = __ldg(p.alpha);
     const int mt = min(p.m, NT);
     int it = 0;
-    FragIter fi{my_start, my_end, p.kb_total};
+    WorkIter fi = work();
     int tile, kb0, kb1;
     for (; fi.next(tile, kb0, kb1); ++it) {
       const int ab = it & 1;
@@ -260,11 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(&tempty[ab]);              // accumulator buffer free again
 
       // CTAs sharing this tile: the owners of its first and last k-block
-      const int64_t c_first = part.cta_of((int64_t)tile * p.kb_total);
-      const int64_t c_last = part.cta_of((int64_t)tile * p.kb_total + p.kb_total - 1);
+      const bool split_tile = p.split_ok != 0 && mixed.is_split(tile);
+      const int64_t c_first = split_tile ? mixed.cta_of((int64_t)tile * p.kb_total) : blockIdx.x;
+      const int64_t c_last = split_tile ? mixed.cta_of((int64_t)tile * p.kb_total + p.kb_total - 1) : blockIdx.x;
       if (c_last > c_first) {
         auto slot = [&](int64_t c) {
-          return p.partials + ((size_t)c * p.maxfrag + (size_t)(tile - part.start(c) / p.kb_total)) * NT * 128;
+          return p.partials + ((size_t)c * p.maxfrag + (size_t)(tile - mixed.start(c) / p.kb_total)) * NT * 128;
         };
         float *mine = slot(blockIdx.x);
 #pragma unroll
@@ -346,8 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct Plan {
-  int nt, tiles, kb_total, grid, maxfrag;
-  size_t ws_bytes;
+  int nt, tiles, kb_total, grid, maxfrag, whole, split_tiles;
+  size_t ws_bytes;        // workspace the mixed split needs (0: no tile shared)
+  bool split;             // mixed split (false: whole tiles per CTA, no workspace)
 };
 
 size_t counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) / 256 * 256; }
@@ -359,10 +380,22 @@ Plan make_plan(int64_t m, int64_t n, int64_t k) {
   pl.kb_total = (int)((k + BK - 1) / BK);
   const int64_t w = (int64_t)pl.tiles * pl.kb_total;
   pl.grid = (int)(w < num_sms() ? w : num_sms());
-  const int64_t per = (w + pl.grid - 1) / pl.grid;           // k-blocks per CTA, rounded up
+  // every CTA gets `whole` whole tiles; the remaining tiles are cut into one
+  // contiguous run of (tile, k-block) pairs per CTA
+  pl.whole = pl.tiles / pl.grid;
+  pl.split_tiles = pl.tiles - pl.whole * pl.grid;
+  // a shared tile counts every CTA between its first and last owner as a
+  // contributor: each CTA must own at least one shared k-block
+  if (pl.whole > 0 && pl.split_tiles > 0 && (int64_t)pl.split_tiles * pl.kb_total < pl.grid) {
+    --pl.whole;
+    pl.split_tiles += pl.grid;
+  }
+  const int64_t ws = (int64_t)pl.split_tiles * pl.kb_total;
+  const int64_t per = (ws + pl.grid - 1) / pl.grid;          // split k-blocks per CTA, rounded up
   pl.maxfrag = (int)((per + pl.kb_total - 1) / pl.kb_total + 1);
-  const bool shared_tiles = (w % pl.grid != 0) || ((w / pl.grid) % pl.kb_total != 0);
+  const bool shared_tiles = (ws % pl.grid != 0) || ((ws / pl.grid) % pl.kb_total != 0);
   pl.ws_bytes = shared_tiles ? counter_bytes(pl.tiles) + (size_t)pl.grid * pl.maxfrag * pl.nt * 128 * 4 : 0;
+  pl.split = true;
   return pl;
 }
 
@@ -390,8 +423,8 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   a.d = d;
   a.out_fp4 = out_fp4;
   a.out_sf = out_sf;
-  const bool split = pl.ws_bytes > 0 && ws != nullptr;
-  if (split) {
+  const bool split = pl.split;
+  if (split && ws != nullptr) {   // (no workspace is used when no tile is shared)
     a.counters = static_cast<int *>(ws);
     a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + counter_bytes(pl.tiles));
   }
@@ -401,6 +434,8 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   a.tiles = pl.tiles;
   a.kb_total = pl.kb_total;
   a.maxfrag = pl.maxfrag;
+  a.whole = pl.whole;
+  a.split_tiles = pl.split_tiles;
   a.split_ok = split ? 1 : 0;
   // without a workspace each CTA owns whole tiles (at most one CTA per tile)
   a.grid = split ? pl.grid : (pl.tiles < num_sms() ? pl.tiles : num_sms());
@@ -452,6 +487,7 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
   Plan pl = make_plan(m, n, k);
   if (pl.ws_bytes > 0 && (workspace == nullptr || ws_bytes < pl.ws_bytes)) {
     // not enough scratch to share tiles between CTAs: whole tiles per CTA
+    pl.split = false;
     pl.ws_bytes = 0;
     workspace = nullptr;
   }

@@ -595,6 +595,12 @@ Plan make_plan(int64_t m, int64_t hid, int64_t inter) {
   for (int g = 0; g < 2; ++g) {
     pl.whole[g] = (int)(pl.tiles[g] / grid);
     pl.split_tiles[g] = pl.tiles[g] - pl.whole[g] * (int)grid;
+    // a shared tile counts every CTA between its first and last owner as a
+    // contributor: each CTA must own at least one shared k-block
+    if (pl.whole[g] > 0 && pl.split_tiles[g] > 0 && (int64_t)pl.split_tiles[g] * pl.kbt[g] < grid) {
+      --pl.whole[g];
+      pl.split_tiles[g] += (int)grid;
+    }
     const int64_t w = (int64_t)pl.split_tiles[g] * pl.kbt[g];
     const int64_t per = (w + grid - 1) / grid;
     pl.maxfrag[g] = (int)((per + pl.kbt[g] - 1) / pl.kbt[g] + 1);

@@ -80,9 +80,11 @@ TC_SHAPES = [(128, 256, 256), (1, 256, 256), (130, 160, 320), (256, 512, 1024), 
              (384, 1024, 2048), (1000, 2304, 512), (4096, 4096, 256)]
 
 
-# swap-AB (weights as the MMA M operand): tokens padded to 16/32/64, split-K
+# swap-AB (weights as the MMA M operand): tokens padded to 16/32/64, split-K;
+# the last two have more weight tiles than SMs (whole tiles per CTA after the
+# shared ones: 160 tiles of 2 k-blocks, 306 tiles of 3 k-blocks)
 SWAP_SHAPES = [(1, 256, 256), (4, 1024, 256), (3, 96, 320), (16, 512, 2048), (17, 128, 128),
-               (33, 384, 1024), (64, 256, 512), (8, 2048, 8192)]
+               (33, 384, 1024), (64, 256, 512), (8, 2048, 8192), (1, 20480, 512), (5, 39168, 768)]
 
 
 @pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SMALL_SHAPES] +
