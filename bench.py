@@ -3,12 +3,13 @@
 
 Workload: the decode dense MLP, W4A4 NVFP4, hidden 5120, intermediate 17408
 (gate_up 34816 x 5120, down 5120 x 17408).  One step runs the MLP forward
-once for each decode batch M in {1, 2, 4, 8, 16} (31 tokens per step) as one
-nvfp4_mlp_decode launch each: quantize x -> gate_up GEMM -> SwiGLU (on the
-bf16-rounded gate_up, as silu_mul_nvfp4_quantize) + NVFP4 requantize ->
-down GEMM.  `--decode-path chain` runs the same step as four launches:
-    nvfp4_quantize(x) -> nvfp4_gemm(gate_up) -> silu_mul_nvfp4_quantize
-    -> nvfp4_gemm(down)
+once for each decode batch M in {1, 2, 4, 8, 16} (31 tokens per step) as
+three launches each (the default `--decode-path chain`):
+    nvfp4_quantize(x) -> nvfp4_gemm_swiglu_quant(gate_up; SwiGLU on the fp32
+    accumulators + NVFP4 requantize in the epilogue) -> nvfp4_gemm(down)
+both GEMMs on the weight-streaming swap-AB tensor-core kernel.
+`--decode-path fused` runs each MLP as one nvfp4_mlp_decode launch instead
+(SwiGLU on the bf16-rounded gate_up, as silu_mul_nvfp4_quantize).
 Weights are synthetic N(0, 0.02), quantized to NVFP4 on the device by the
 library before timing; x ~ N(0, 1) bf16.  Each step's launches are captured
 in a CUDA graph; four weight copies (602 MB, > 4x the 126 MB L2) rotate so the
@@ -47,8 +48,8 @@ def parse():
     p.add_argument("--workload", default="decode", choices=["decode", "prefill", "w4a16"],
                    help="decode (default line) | prefill H7168/I18432 | w4a16 H5120/I17408")
     p.add_argument("--m", type=int, default=None, help="single M for prefill / w4a16")
-    p.add_argument("--decode-path", default="fused", choices=["fused", "chain"],
-                   help="decode step as one nvfp4_mlp_decode launch (default) or the four-launch chain")
+    p.add_argument("--decode-path", default="chain", choices=["fused", "chain"],
+                   help="decode MLP as three launches (default) or one nvfp4_mlp_decode launch")
     return p.parse_args()
 
 
@@ -254,7 +255,7 @@ def run_ours(args, world, rank, local):
     tokens_per_step = sum(ms)
     mmax = max(ms)
     fused_decode = wl == "decode" and args.decode_path == "fused"
-    interleaved = wl == "prefill" or fused_decode
+    interleaved = wl in ("prefill", "decode")
 
     w_gu0 = make_weight(2 * inter, hid, interleave=interleaved)
     w_dn0 = make_weight(hid, inter)
@@ -314,42 +315,37 @@ def run_ours(args, world, rank, local):
                        [nv.bf16_fp4_gemm_workspace_bytes(m, hid, inter) for m in ms] + [0])
     ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
+    def dominant(m, wc):
+        """The step's dominant launch: the gate_up GEMM (the whole MLP when fused)."""
+        b = bufs[m]
+        (gq, gsf, _), (dq, dsf, _) = wc
+        if wl == "w4a16":
+            nv.bf16_fp4_gemm(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes)
+        elif fused_decode:
+            nv.nvfp4_mlp_decode(x_in[m], gs_x_d, gq, gsf, a_gu, gs_h_d, dq, dsf, a_dn, b["xq"], b["xs"],
+                                b["hq"], b["hs"], b["out"], m, hid, inter, True, ws, ws_bytes)
+        else:
+            nv.nvfp4_gemm_swiglu_quant(b["xq"], b["xs"], gq, gsf, a_gu, gs_h_d, b["hq"], b["hs"], m,
+                                       2 * inter, hid, ws, ws_bytes)
+
     def forward(m, wc, ev=None):
         """One MLP forward; ev = (start, end) events around the dominant kernel."""
         b = bufs[m]
         (gq, gsf, _), (dq, dsf, _) = wc
-        if wl == "w4a16":
-            if ev is not None:
-                ev[0].record()
-            nv.bf16_fp4_gemm(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes)
-            if ev is not None:
-                ev[1].record()
-            nv.silu_mul_bf16(b["gu"], m, inter, b["h16"])
-            nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
-            return
-        if fused_decode:
-            if ev is not None:
-                ev[0].record()
-            nv.nvfp4_mlp_decode(x_in[m], gs_x_d, gq, gsf, a_gu, gs_h_d, dq, dsf, a_dn, b["xq"], b["xs"],
-                                b["hq"], b["hs"], b["out"], m, hid, inter, True, ws, ws_bytes)
-            if ev is not None:
-                ev[1].record()
-            return
-        nv.nvfp4_quantize(x_in[m], m, hid, gs_x_d, b["xq"], b["xs"])
+        if wl != "w4a16" and not fused_decode:
+            nv.nvfp4_quantize(x_in[m], m, hid, gs_x_d, b["xq"], b["xs"])
         if ev is not None:
             ev[0].record()
-        if wl == "prefill":
-            nv.nvfp4_gemm_swiglu_quant(b["xq"], b["xs"], gq, gsf, a_gu, gs_h_d, b["hq"], b["hs"], m,
-                                       2 * inter, hid, ws, ws_bytes)
-        else:
-            nv.nvfp4_gemm(b["xq"], b["xs"], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes)
+        dominant(m, wc)
         if ev is not None:
             ev[1].record()
-        if wl == "decode":
-            nv.silu_mul_nvfp4_quantize(b["gu"], m, inter, gs_h_d, b["hq"], b["hs"])
-        nv.nvfp4_gemm(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
+        if wl == "w4a16":
+            nv.silu_mul_bf16(b["gu"], m, inter, b["h16"])
+            nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
+        elif not fused_decode:
+            nv.nvfp4_gemm(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
 
-    launches_per_step = sum((1 if fused_decode else {"decode": 4, "prefill": 3, "w4a16": 3}[wl]) for _ in ms)
+    launches_per_step = sum((1 if fused_decode else 3) for _ in ms)
 
     try:
         torch.cuda.Event(enable_timing=True, external=True)
@@ -423,16 +419,38 @@ def run_ours(args, world, rank, local):
                             sums[j] += events[c][j][0].elapsed_time(events[c][j][1])
         torch.cuda.synchronize()
         dom_ms = [v / args.steps for v in sums]
+    # the dominant kernel alone, REPS launches back to back in one graph
+    # (weight copies rotating), events around the replays: its per-launch time
+    # with the programmatic-launch overlap it also gets inside the step graph
+    # (the event nodes of the pass above end that overlap)
+    b2b_ms = []
+    REPS = 8
+    with torch.cuda.stream(stream):
+        for m in ms:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for r in range(REPS):
+                    dominant(m, copies[r % ncopy])
+            gr.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(3):
+                gr.replay()
+            e1.record(stream)
+            stream.synchronize()
+            b2b_ms.append(e0.elapsed_time(e1) / (3 * REPS))
+            del gr
     clk = clocks.stop()
 
     step_ms, value = aggregate(step_ms, tokens_per_step, world, device=dev)
 
     roofline = None
-    if dom_ms:
-        timing_note = ("dominant-kernel time: CUDA events around each launch on the launching stream, "
-                       f"averaged over a {args.steps}-step pass right after the headline pass")
-        per_m_us = {str(m): 1000.0 * t for m, t in zip(ms, dom_ms)}
-        tot_s = sum(dom_ms) / 1000.0
+    if b2b_ms:
+        timing_note = (f"dominant-kernel time: {REPS} launches back to back in one CUDA graph per M, CUDA "
+                       "events on the launching stream around 3 replays; isolated_us: events around each "
+                       f"launch inside the step graphs ({args.steps}-step pass, no launch overlap)")
+        per_m_us = {str(m): 1000.0 * t for m, t in zip(ms, b2b_ms)}
+        tot_s = sum(b2b_ms) / 1000.0
         if fused_decode:
             # weights (codes + scales) of both GEMMs, x in, output out
             nbytes = sum(3 * inter * hid * 9 // 16 + 2 * m * hid * 2 for m in ms)
@@ -441,9 +459,11 @@ def run_ours(args, world, rank, local):
                         "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                         "traffic": None, "algorithmic_bytes_per_step": nbytes}
         elif wl == "decode":
-            nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 9 // 16 + m * 2 * inter * 2 for m in ms)
+            # gate_up weights (codes + scales), quantized x in, NVFP4 h out
+            nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 9 // 16 + m * inter * 9 // 16 for m in ms)
             achieved = nbytes / tot_s / 1e9
-            roofline = {"bound": "hbm", "kernel": "nvfp4_gemm gate_up 34816x5120 (GEMV, M=1..16)",
+            roofline = {"bound": "hbm",
+                        "kernel": "nvfp4_gemm_swiglu_quant gate_up 34816x5120 (swap-AB tcgen05, M=1..16)",
                         "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                         "traffic": None, "algorithmic_bytes_per_step": nbytes}
         elif wl == "prefill":
@@ -459,6 +479,8 @@ def run_ours(args, world, rank, local):
                         "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                         "traffic": None}
         roofline["per_m_us"] = per_m_us
+        if dom_ms:
+            roofline["isolated_us"] = {str(m): 1000.0 * t for m, t in zip(ms, dom_ms)}
         roofline["peak_source"] = "measured" if pk else "fallback"
         roofline["timing"] = timing_note
 
