@@ -283,8 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t c_first = split_tile ? mixed.cta_of((int64_t)tile * p.kb_total) : blockIdx.x;
       const int64_t c_last = split_tile ? mixed.cta_of((int64_t)tile * p.kb_total + p.kb_total - 1) : blockIdx.x;
       if (c_last > c_first) {
+        // partial slot of contributor c: its fragment index is 0 except for
+        // c_first (every later contributor's run starts inside this tile)
+        const int f_first = tile - (int)(mixed.start(c_first) / p.kb_total);
         auto slot = [&](int64_t c) {
-          return p.partials + ((size_t)c * p.maxfrag + (size_t)(tile - mixed.start(c) / p.kb_total)) * NT * 128;
+          return p.partials + ((size_t)c * p.maxfrag + (c == c_first ? f_first : 0)) * NT * 128;
         };
         float *mine = slot(blockIdx.x);
 #pragma unroll

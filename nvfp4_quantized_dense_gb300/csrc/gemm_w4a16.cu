@@ -442,8 +442,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
       }
       // shared tile: this CTA's fp32 partial to the workspace; the last
       // contributor to arrive sums all of them in K order
+      // partial slot of contributor cc: its fragment index is 0 except for
+      // c_first (every later contributor's run starts inside this tile)
+      const int f_first = tile - (int)(part.start(c_first) / p.nkb);
       auto slot = [&](int64_t cc) {
-        return p.partials + ((size_t)cc * p.maxfrag + (size_t)(tile - part.start(cc) / p.nkb)) * NT * 128;
+        return p.partials + ((size_t)cc * p.maxfrag + (cc == c_first ? f_first : 0)) * NT * 128;
       };
       float *mine = slot(blockIdx.x);
 #pragma unroll 1

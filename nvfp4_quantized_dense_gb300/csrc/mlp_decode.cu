@@ -484,8 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t c_first = split ? pt.cta_of((int64_t)tile * G.kbt) : 0;
         const int64_t c_last = split ? pt.cta_of((int64_t)tile * G.kbt + G.kbt - 1) : 0;
         if (c_last > c_first) {
+          // partial slot of contributor c: its fragment index is 0 except for
+          // c_first (every later contributor's run starts inside this tile)
+          const int f_first = tile - (int)(pt.start(c_first) / G.kbt);
           auto slot = [&](int64_t c) {
-            return G.partials + ((size_t)c * G.maxfrag + (size_t)(tile - pt.start(c) / G.kbt)) * NT * 128;
+            return G.partials + ((size_t)c * G.maxfrag + (c == c_first ? f_first : 0)) * NT * 128;
           };
           float *mine = slot(blockIdx.x);
 #pragma unroll
