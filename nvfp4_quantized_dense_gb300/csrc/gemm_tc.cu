@@ -271,8 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
           const int slot = g & 1;
-          if (!ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag) ||
-              !ptx::mbar_wait_bounded(&sm.sf_full()[slot], (uint32_t)((g >> 1) & 1), limit, kDefaultTimeoutNs,
+          // The scale writers saw the stage's TMA data complete before they
+          // filled the scale slot: one wait covers both (a wait costs ~170
+          // cycles even on a completed phase, time the tensor pipe would
+          // spend idle behind the 1-2 MMAs it holds).
+          if (!ptx::mbar_wait_bounded(&sm.sf_full()[slot], (uint32_t)((g >> 1) & 1), limit, kDefaultTimeoutNs,
                                       abort_flag)) {
             give_up(abort_flag, p.status);
             ok = false;
