@@ -1,0 +1,114 @@
+"""Host-side work plans of the split-K kernels, restated here and checked
+against the scratch sizes the library reports (no GPU needed: without a
+device the library plans for 148 SMs; with one, for the device's count).
+
+Swap-AB GEMM (weights as the MMA's 128-row operand, 256-wide k-blocks):
+every CTA takes floor(tiles/grid) whole tiles, the other tiles are cut into
+one contiguous run of (tile, k-block) pairs per CTA, and when those shared
+tiles have fewer k-blocks than there are CTAs one round of whole tiles joins
+them.  W4A16 tensor-core GEMM (64-wide k-blocks): one contiguous run per CTA
+up to 64 tokens.  The scratch is a 256-byte-rounded counter per tile plus
+[grid][fragment slots][tokens padded][128] fp32 partials, only when a tile is
+shared.  The rule that every CTA between a shared tile's first and last owner
+contributes to it is checked on the restated partition.
+"""
+import math
+
+import pytest
+
+import nvfp4_quantized_dense_gb300 as nv
+from nvfp4_quantized_dense_gb300 import build as nvbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nvbuild.build()
+    return nv.load()
+
+
+def sm_count():
+    import torch
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(0).multi_processor_count
+    return 148
+
+
+def r256(b):
+    return (b + 255) // 256 * 256
+
+
+def swapab_plan(m, n, k, sms):
+    nt = 16 if m <= 16 else 32 if m <= 32 else 64
+    tiles, kbt = math.ceil(n / 128), math.ceil(k / 256)
+    grid = min(tiles * kbt, sms)
+    whole = tiles // grid
+    split = tiles - whole * grid
+    if whole > 0 and split > 0 and split * kbt < grid:
+        whole, split = whole - 1, split + grid
+    units = split * kbt
+    per = math.ceil(units / grid)
+    maxfrag = math.ceil(per / kbt) + 1
+    shared = units % grid != 0 or (units // grid) % kbt != 0
+    ws = r256(tiles * 4) + grid * maxfrag * nt * 128 * 4 if shared else 0
+    return dict(nt=nt, tiles=tiles, kbt=kbt, grid=grid, whole=whole, split=split, ws=ws)
+
+
+def w4a16_ws(m, n, k, sms):
+    nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128 if m <= 128 else 256
+    if nt > 64:
+        return 0
+    tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), k // 64
+    w = tiles * nkb
+    grid = min(w, sms)
+    maxfrag = math.ceil(math.ceil(w / grid) / nkb) + 1
+    shared = w % grid != 0 or (w // grid) % nkb != 0
+    return r256(tiles * 4) + grid * maxfrag * nt * 128 * 4 if shared else 0
+
+
+SWAP_CASES = [
+    (1, 34816, 5120),     # decode gate_up H5120: 272 tiles -> one whole tile per CTA + shared tiles
+    (16, 34816, 5120),
+    (1, 5120, 17408),     # decode down: 40 tiles, all shared
+    (64, 36864, 7168),    # DeepSeek-shaped gate_up
+    (8, 7168, 18432),
+    (1, 20480, 512),      # 160 tiles of 2 k-blocks: the shared k-blocks would be fewer than CTAs
+    (5, 39168, 768),
+    (33, 384, 1024), (4, 1024, 256), (17, 128, 128),
+]
+
+
+@pytest.mark.parametrize("m,n,k", SWAP_CASES)
+def test_swapab_scratch_matches_plan(lib, m, n, k):
+    pl = swapab_plan(m, n, k, sm_count())
+    assert nv.nvfp4_workspace_bytes(m, n, k, nv.ALGO_TC_SWAPAB) == pl["ws"]
+    assert nv.nvfp4_workspace_bytes(m, n, k) == pl["ws"]          # AUTO picks swap-AB up to 64 tokens
+
+
+@pytest.mark.parametrize("m,n,k", SWAP_CASES)
+@pytest.mark.parametrize("sms", [148, 152, 7])
+def test_swapab_partition_contributors_are_contiguous(m, n, k, sms):
+    pl = swapab_plan(m, n, k, sms)
+    grid, kbt, split = pl["grid"], pl["kbt"], pl["split"]
+    assert split + pl["whole"] * grid == pl["tiles"]
+    units = split * kbt
+    starts = [j * units // grid for j in range(grid + 1)]
+    owner = {}
+    for j in range(grid):
+        for u in range(starts[j], starts[j + 1]):
+            owner[u] = j
+    assert len(owner) == units
+    if units and split:
+        assert units >= grid, "a CTA without a shared k-block would break the arrival count"
+    for t in range(split):
+        cs = sorted({owner[u] for u in range(t * kbt, (t + 1) * kbt)})
+        assert cs == list(range(cs[0], cs[-1] + 1))
+        # every contributor after the first starts its run inside the tile
+        # (its partial sits in fragment slot 0)
+        for c in cs[1:]:
+            assert starts[c] // kbt == t
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 34816, 5120), (16, 34816, 5120), (16, 5120, 17408), (64, 384, 2048),
+                                   (33, 128, 1024), (5, 96, 320), (128, 34816, 5120), (1024, 34816, 5120)])
+def test_w4a16_scratch_matches_plan(lib, m, n, k):
+    assert nv.bf16_fp4_gemm_workspace_bytes(m, n, k, nv.ALGO_TC) == w4a16_ws(m, n, k, sm_count())
