@@ -293,6 +293,13 @@ def run_ours(args, world, rank, local):
     gs_h_d = scalar(gs_h) if gs_h is not None else None
     del gu_tmp
 
+    # every M's output is a row range of one buffer (read back in one copy)
+    out_all = torch.empty((sum(ms), hid), dtype=torch.bfloat16, device=dev)
+    out_rows = {}
+    r0 = 0
+    for m in ms:
+        out_rows[m] = out_all[r0:r0 + m]
+        r0 += m
     bufs = {}
     for m in ms:
         bufs[m] = dict(
@@ -302,8 +309,9 @@ def run_ours(args, world, rank, local):
             h16=torch.empty((m, inter), dtype=torch.bfloat16, device=dev),
             hq=torch.empty((m, inter // 2), dtype=torch.uint8, device=dev),
             hs=torch.empty((nv.nvfp4_sf_bytes(m, inter),), dtype=torch.uint8, device=dev),
-            out=torch.empty((m, hid), dtype=torch.bfloat16, device=dev))
-    x_in = {m: x[:m].contiguous() for m in ms}
+            out=out_rows[m])
+    # every M's input is the first M rows of one x buffer (written in one copy)
+    x_in = {m: x[:m] for m in ms}
     # one zero-filled scratch buffer (split-K partials + arrival counters),
     # sized for the largest GEMM of the chain and shared by its sequential calls
     ws_bytes = max([nv.nvfp4_workspace_bytes(m, 2 * inter, hid) for m in ms] +
@@ -315,35 +323,39 @@ def run_ours(args, world, rank, local):
                        [nv.bf16_fp4_gemm_workspace_bytes(m, hid, inter) for m in ms] + [0])
     ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
+    # the stream handle as an int: the bindings then skip looking up torch's
+    # current stream (~3 us of host time per call)
+    SH = [None]
+
     def dominant(m, wc):
         """The step's dominant launch: the gate_up GEMM (the whole MLP when fused)."""
         b = bufs[m]
         (gq, gsf, _), (dq, dsf, _) = wc
         if wl == "w4a16":
-            nv.bf16_fp4_gemm(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes)
+            nv.bf16_fp4_gemm(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes, stream=SH[0])
         elif fused_decode:
             nv.nvfp4_mlp_decode(x_in[m], gs_x_d, gq, gsf, a_gu, gs_h_d, dq, dsf, a_dn, b["xq"], b["xs"],
-                                b["hq"], b["hs"], b["out"], m, hid, inter, True, ws, ws_bytes)
+                                b["hq"], b["hs"], b["out"], m, hid, inter, True, ws, ws_bytes, stream=SH[0])
         else:
             nv.nvfp4_gemm_swiglu_quant(b["xq"], b["xs"], gq, gsf, a_gu, gs_h_d, b["hq"], b["hs"], m,
-                                       2 * inter, hid, ws, ws_bytes)
+                                       2 * inter, hid, ws, ws_bytes, stream=SH[0])
 
     def forward(m, wc, ev=None):
         """One MLP forward; ev = (start, end) events around the dominant kernel."""
         b = bufs[m]
         (gq, gsf, _), (dq, dsf, _) = wc
         if wl != "w4a16" and not fused_decode:
-            nv.nvfp4_quantize(x_in[m], m, hid, gs_x_d, b["xq"], b["xs"])
+            nv.nvfp4_quantize(x_in[m], m, hid, gs_x_d, b["xq"], b["xs"], stream=SH[0])
         if ev is not None:
             ev[0].record()
         dominant(m, wc)
         if ev is not None:
             ev[1].record()
         if wl == "w4a16":
-            nv.silu_mul_bf16(b["gu"], m, inter, b["h16"])
-            nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
+            nv.silu_mul_bf16(b["gu"], m, inter, b["h16"], stream=SH[0])
+            nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes, stream=SH[0])
         elif not fused_decode:
-            nv.nvfp4_gemm(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes)
+            nv.nvfp4_gemm(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes, stream=SH[0])
 
     launches_per_step = sum((1 if fused_decode else 3) for _ in ms)
 
@@ -354,6 +366,7 @@ def run_ours(args, world, rank, local):
         ext_ok = False
 
     stream = torch.cuda.Stream(device=dev)
+    SH[0] = stream.cuda_stream
     # Two graph sets per weight copy: plain step graphs for the headline pass
     # (an event node between kernels would end their programmatic-launch
     # overlap) and the same steps with timing events around the dominant
@@ -486,17 +499,17 @@ def run_ours(args, world, rank, local):
 
     # end to end through the API: pinned host x in, host result out, per step
     x_host = x.cpu().pin_memory()
-    outs_host = {m: torch.empty((m, hid), dtype=torch.bfloat16).pin_memory() for m in ms}
-    h2d = sum(m * hid * 2 for m in ms)
-    d2h = sum(m * hid * 2 for m in ms)
+    out_host = torch.empty((sum(ms), hid), dtype=torch.bfloat16).pin_memory()
+    h2d = x.numel() * 2
+    d2h = out_all.numel() * 2
     e2e_steps = max(3, min(args.steps, 20))
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         def e2e_step(i):
+            x.copy_(x_host, non_blocking=True)
             for m in ms:
-                x_in[m].copy_(x_host[:m], non_blocking=True)
                 forward(m, copies[i % ncopy])
-                outs_host[m].copy_(bufs[m]["out"], non_blocking=True)
+            out_host.copy_(out_all, non_blocking=True)
         for i in range(2):
             e2e_step(i)
         stream.synchronize()

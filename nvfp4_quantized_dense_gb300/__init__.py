@@ -92,10 +92,16 @@ def _ptr(x):
     return x.data_ptr()
 
 
+_torch = None
+
+
 def _stream(s):
     if s is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        global _torch
+        if _torch is None:
+            import torch
+            _torch = torch
+        return _torch.cuda.current_stream().cuda_stream
     if isinstance(s, int):
         return s
     return s.cuda_stream
