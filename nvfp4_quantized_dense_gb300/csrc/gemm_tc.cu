@@ -66,8 +66,15 @@ constexpr int kThreads = 448;           // producer, MMA, 8 epilogue warps, 4 sc
 constexpr int kCluster = 2;             // CTAs sharing one weight tile
 constexpr uint16_t kPairMask = 0x3;
 constexpr uint32_t TMEM_COLS = 512;
-// accumulator 256 columns; two scale slots of 48 columns (SFA 16 + SFB 32)
+// accumulator 256 columns; one scale slot of 48 columns (SFA 16 + SFB 32,
+// 64-column pitch) per smem stage.  With a slot per stage the stage's data
+// barrier orders everything: the producer refills stage s only after the
+// MMAs of its previous use have completed (both CTAs' commits), so a writer
+// that has seen the new data of stage s may overwrite slot s — no barrier of
+// its own for freeing the slot, and one commit per stage for the MMA issuer.
+constexpr int SF_SLOTS = STAGES;
 constexpr uint32_t ACC_COL = 0, SF_COL = 256, SF_SLOT = 64, SFB_OFF = 4 * KSTEPS;
+static_assert(SF_COL + SF_SLOTS * SF_SLOT <= 512, "TMEM columns");
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
 constexpr uint32_t kDrainPolls = 1u << 22;
 
@@ -106,8 +113,7 @@ struct Smem {
   __device__ uint64_t *tempty() const { return tfull() + 1; }
   __device__ uint64_t *drain() const { return tempty() + 1; }
   __device__ uint64_t *sf_full() const { return drain() + 1; }
-  __device__ uint64_t *sf_empty() const { return sf_full() + 2; }
-  __device__ uint32_t *tslot() const { return reinterpret_cast<uint32_t *>(sf_empty() + 2); }
+  __device__ uint32_t *tslot() const { return reinterpret_cast<uint32_t *>(sf_full() + SF_SLOTS); }
   __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(tslot() + 1); }
 };
 
@@ -154,10 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(sm.tfull(), 1);
     ptx::mbar_init(sm.tempty(), 256);
     ptx::mbar_init(sm.drain(), 1);
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&sm.sf_full()[b], 4);     // one arrival per scale-writer warp
-      ptx::mbar_init(&sm.sf_empty()[b], 1);
-    }
+    for (int b = 0; b < SF_SLOTS; ++b) ptx::mbar_init(&sm.sf_full()[b], 4);   // one arrival per scale-writer warp
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tm_a);
@@ -270,28 +273,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
-          const int slot = g & 1;
           // The scale writers saw the stage's TMA data complete before they
-          // filled the scale slot: one wait covers both (a wait costs ~170
-          // cycles even on a completed phase, time the tensor pipe would
-          // spend idle behind the 1-2 MMAs it holds).
-          if (!ptx::mbar_wait_bounded(&sm.sf_full()[slot], (uint32_t)((g >> 1) & 1), limit, kDefaultTimeoutNs,
-                                      abort_flag)) {
+          // filled its scale slot: one barrier covers both.
+          if (!ptx::mbar_wait_bounded(&sm.sf_full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
             give_up(abort_flag, p.status);
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
-          const uint32_t sf = tmem + SF_COL + slot * SF_SLOT;
+          const uint32_t sf = tmem + SF_COL + s * SF_SLOT;
           const uint32_t a_s = ptx::smem_u32(sm.a(s)), b_s = ptx::smem_u32(sm.b(s));
           for (int j = 0; j < nk; ++j)
             ptx::mma_nvfp4(tmem + ACC_COL, ptx::smem_desc(a_s + 32 * j, 16, 1024, 2),
                            ptx::smem_desc(b_s + 32 * j, 16, 1024, 2), idesc, sf + 4 * j, sf + SFB_OFF + 8 * j,
                            (kb | j) != 0);
           mma_issued = true;
-          ptx::tc_commit_mc(&sm.empty()[s], kPairMask);   // this stage is free for both producers
-          ptx::tc_commit(&sm.sf_empty()[slot]);
+          ptx::tc_commit_mc(&sm.empty()[s], kPairMask);   // this stage and its scale slot are free
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
@@ -312,10 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int pair = cluster; pair < num_pairs && !*abort_flag; pair += num_clusters) {
       bool ok = true;
       for (int kb = 0; kb < num_kb; ++kb, ++g) {
-        const int slot = g & 1;
-        if (!ptx::mbar_wait_bounded(&sm.sf_empty()[slot], (uint32_t)((g >> 1) & 1) ^ 1u, limit,
-                                    kDefaultTimeoutNs, abort_flag) ||
-            !ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
+        // the stage's data: its arrival also means the MMAs that read this
+        // scale slot last have completed (the producer refilled the stage
+        // only after they committed it)
+        if (!ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
           give_up(abort_flag, p.status);
           ok = false;
           break;
@@ -339,14 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t *d = (j < 2 ? rb0 : rb1) + 8 * (j & 1) + 4 * rb;   // column 8j + 4rb of the SFB slot
             d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
           }
-        const uint32_t sf = tmem + lane_off + SF_COL + slot * SF_SLOT;
+        const uint32_t sf = tmem + lane_off + SF_COL + s * SF_SLOT;
         ptx::tmem_st16(sf, ra);
         ptx::tmem_st16(sf + SFB_OFF, rb0);
         ptx::tmem_st16(sf + SFB_OFF + 16, rb1);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.sf_full()[slot]);
+        if (lane == 0) ptx::mbar_arrive(&sm.sf_full()[s]);
         if (++s == STAGES) { s = 0; ph ^= 1u; }
       }
       if (!ok) break;
