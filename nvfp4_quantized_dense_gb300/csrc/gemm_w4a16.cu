@@ -5,18 +5,20 @@
 // The tensor cores need both operands of a kind::f16 MMA in the same type,
 // so the weight is dequantized to bf16 in shared memory: converter warps read
 // a k-block's E2M1 codes and E4M3 scales and write E2M1 * scale -- exact in
-// bf16, at most 5 significant bits -- into a 128-byte-swizzled K-major tile
-// that the MMA reads directly.  The weight is the MMA's 128-row operand and
+// bf16, at most 6 significant bits -- into 128-byte-swizzled K-major tiles
+// (one per 64-wide sub-block) that the MMA reads directly.  The weight is the MMA's 128-row operand and
 // the tokens its N (16..256); D^T[n, t] accumulates in TMEM (two buffers) and
 // the epilogue writes D[t, n] with the 32 lanes of a warp on 32 consecutive n.
 //
-// Two rings: a deep one of raw k-blocks (4.5 KB of weight codes and scales
-// from HBM plus the k-block's activation tile), so that ~100 KB of weight
-// bytes per SM are in flight at decode sizes, and a shallow one of
-// dequantized 16 KB weight tiles.  A raw stage is released by the MMA (it
-// reads the activation tile there), a dequantized tile likewise.
+// Two rings: raw k-blocks (weight codes and scales from HBM plus the
+// k-block's activation tile) and dequantized weight tiles.  A raw stage is
+// released by the MMA (it reads the activation tile there), a dequantized
+// tile likewise.  A k-block is 128 wide up to 32 tokens (9 KB of weight
+// codes and scales, a 32 KB dequantized tile filled by a pair of converter
+// warps) and 64 wide above: at decode sizes every k-block costs each role a
+// barrier round, so wider k-blocks halve that cost per weight byte.
 //
-// Work split: as in the swap-AB kernel, the (weight tile, 64-wide k-block)
+// Work split: as in the swap-AB kernel, the (weight tile, k-block)
 // pairs are cut into one contiguous run per CTA when the caller gives a
 // workspace (tokens <= 64); a tile shared by CTAs is finished by the last to
 // arrive, which sums the fp32 partials in K order.  Without a workspace, or
@@ -41,10 +43,7 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int BK = 64;                      // K per k-block: 128 bytes of bf16 per row
-constexpr uint32_t WC_BYTES = 128 * BK / 2; // weight codes, 4 KB
-constexpr uint32_t WS_BYTES = 512;          // one 128x4 scale tile
-constexpr uint32_t WB_BYTES = 128 * BK * 2; // dequantized weight tile, 16 KB
+constexpr uint32_t SUB_WB = 128 * 64 * 2;  // dequantized 64-wide sub-block of a tile, 16 KB
 constexpr int kConvWarps = 8;               // converter warps
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kWarpMma2 = 2 + kConvWarps + 4;   // second MMA issuer
@@ -55,15 +54,27 @@ constexpr uint32_t kDrainPolls = 1u << 22;
 
 template <int NT>
 struct Cfg {
-  static constexpr uint32_t X_BYTES = NT * BK * 2;                       // NT rows x 128 B
+  // K per k-block (the unit of the work split and of every barrier round):
+  // 128 up to 32 tokens, where the barrier waits, copies, commits and MMA
+  // issues of each k-block bound the kernel; 64 above.  A k-block is SUB
+  // 64-wide sub-blocks, each one 128-byte-swizzle atom column of the
+  // dequantized tile and of the activation tile.
+  static constexpr int BK = NT <= 32 ? 128 : 64;
+  static constexpr int SUB = BK / 64;
+  static constexpr uint32_t WC_BYTES = 128 * BK / 2;                     // weight codes, 64-byte rows
+  static constexpr uint32_t WS_BYTES = SUB * 512;                        // 128x4 scale tiles
+  static constexpr uint32_t WB_BYTES = SUB * SUB_WB;                     // dequantized tile
+  static constexpr uint32_t SUB_X = NT * 128;                            // NT rows x 128 B
+  static constexpr uint32_t X_BYTES = SUB * SUB_X;
   static constexpr uint32_t RAW_BYTES = (X_BYTES + WC_BYTES + WS_BYTES + 1023) / 1024 * 1024;
-  // Up to 64 tokens each converter warp dequantizes whole k-blocks (k-block
-  // j -> warp j % DSTAGES, which owns tile j % DSTAGES): many k-blocks in
-  // flight for the weight stream.  Above, every warp takes 16 rows of every
-  // k-block: short latency per k-block for the compute-bound MMA.
+  // Up to 64 tokens the converter warps dequantize whole k-blocks, WPT warps
+  // per tile (k-block j -> tile j % DSTAGES): many k-blocks in flight for the
+  // weight stream.  Above, every warp takes 16 rows of every k-block: short
+  // latency per k-block for the compute-bound MMA.
   static constexpr bool WHOLE_KB = NT <= 64;
-  static constexpr int DSTAGES = NT <= 32 ? 8 : NT == 64 ? 6 : 4;         // dequantized tiles
-  static_assert(!WHOLE_KB || DSTAGES <= kConvWarps, "one converter warp per dequantized tile");
+  static constexpr int WPT = !WHOLE_KB ? kConvWarps : SUB == 2 ? 2 : 1;   // converter warps per tile
+  static constexpr int DSTAGES = NT <= 32 ? 4 : NT == 64 ? 6 : 4;         // dequantized tiles
+  static_assert(!WHOLE_KB || DSTAGES * WPT <= kConvWarps, "converter warps per dequantized tile");
   static constexpr int NI = NT <= 128 ? 2 : 1;                             // MMA issuers
   static constexpr int RSTAGES_FIT = (int)((220u * 1024 - DSTAGES * WB_BYTES) / RAW_BYTES) / NI * NI;
   static constexpr int RSTAGES = RSTAGES_FIT > 32 ? 32 : RSTAGES_FIT;   // raw k-blocks in flight
@@ -142,11 +153,12 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
   constexpr int DSTAGES = C::DSTAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  auto st_wb = [&](int d) { return base + d * WB_BYTES; };
-  auto st_x = [&](int r) { return base + DSTAGES * WB_BYTES + r * C::RAW_BYTES; };
+  constexpr int BK = C::BK, SUB = C::SUB;
+  auto st_wb = [&](int d) { return base + d * C::WB_BYTES; };
+  auto st_x = [&](int r) { return base + DSTAGES * C::WB_BYTES + r * C::RAW_BYTES; };
   auto st_wc = [&](int r) { return st_x(r) + C::X_BYTES; };
-  auto st_ws = [&](int r) { return st_wc(r) + WC_BYTES; };
-  uint64_t *rfull = reinterpret_cast<uint64_t *>(base + DSTAGES * WB_BYTES + RST * C::RAW_BYTES);
+  auto st_ws = [&](int r) { return st_wc(r) + C::WC_BYTES; };
+  uint64_t *rfull = reinterpret_cast<uint64_t *>(base + DSTAGES * C::WB_BYTES + RST * C::RAW_BYTES);
   uint64_t *rempty = rfull + RST;
   uint64_t *dfull = rempty + RST;
   uint64_t *dempty = dfull + DSTAGES;
@@ -165,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
       ptx::mbar_init(&rempty[r], 1);
     }
     for (int d = 0; d < DSTAGES; ++d) {
-      ptx::mbar_init(&dfull[d], C::WHOLE_KB ? 1 : kConvWarps);   // arrivals of the warps filling it
+      ptx::mbar_init(&dfull[d], C::WPT);   // arrivals of the warps filling it
       ptx::mbar_init(&dempty[d], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -189,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
 
   const int tiles = p.wtiles * p.ttiles;
   const int cp4 = p.k >> 6;              // 512-byte scale tiles per 128-row block
+  // 64-wide sub-blocks of k-block kb (the last k-block may hold fewer)
+  auto nsub_of = [&](int kb) { return min(SUB, cp4 - kb * SUB); };
   const Partition part{(int64_t)tiles * p.nkb, p.grid, p.nkb, p.split_ok == 0, tiles};
   const int64_t my_start = part.start(blockIdx.x), my_end = part.start(blockIdx.x + 1);
   const uint32_t limit = p.wait_limit;
@@ -215,7 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
       int npend = 0;
       bool flushed = false;
       auto load_x = [&](int st, int kb, int tt) {
-        ptx::tma_load_2d(st_x(st), &tm_x, &rfull[st], kb * (BK * 2), tt * NT, pol_x);
+        // one 128-byte-swizzled NT x 128 B tile per sub-block (a sub-block
+        // past K reads zeros)
+#pragma unroll
+        for (int sb = 0; sb < SUB; ++sb)
+          ptx::tma_load_2d(st_x(st) + sb * C::SUB_X, &tm_x, &rfull[st], (kb * SUB + sb) * 128, tt * NT, pol_x);
       };
       auto flush = [&]() {
         pdl_wait();
@@ -237,9 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
               ok = false;
               break;
             }
-            ptx::mbar_arrive_expect_tx(&rfull[r], C::X_BYTES + WC_BYTES + WS_BYTES);
+            const uint32_t sfb = (uint32_t)nsub_of(kb) * 512u;   // scales only of the sub-blocks K has
+            ptx::mbar_arrive_expect_tx(&rfull[r], C::X_BYTES + C::WC_BYTES + sfb);
             ptx::tma_load_2d(st_wc(r), &tm_w, &rfull[r], kb * (BK / 2), wt * 128, pol_w);
-            ptx::bulk_load(st_ws(r), p.wsf + ((size_t)wt * cp4 + kb) * 512, WS_BYTES, &rfull[r], pol_w);
+            ptx::bulk_load(st_ws(r), p.wsf + ((size_t)wt * cp4 + kb * SUB) * 512, sfb, &rfull[r], pol_w);
             if (j < RST) {
               pend_r[npend] = r;
               pend_kb[npend] = kb;
@@ -294,10 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
           }
           ptx::tc_fence_after();
           const uint32_t wb = ptx::smem_u32(st_wb(d)), xs = ptx::smem_u32(st_x(r));
+          const int nsub = nsub_of(kb);
+          for (int sb = 0; sb < nsub; ++sb)
 #pragma unroll
-          for (int jj = 0; jj < BK / 16; ++jj)
-            ptx::mma_bf16(acc, ptx::smem_desc(wb + 32 * jj, 16, 1024, 2),
-                          ptx::smem_desc(xs + 32 * jj, 16, 1024, 2), idesc, !first || (jj != 0));
+            for (int jj = 0; jj < 4; ++jj)
+              ptx::mma_bf16(acc, ptx::smem_desc(wb + sb * SUB_WB + 32 * jj, 16, 1024, 2),
+                            ptx::smem_desc(xs + sb * C::SUB_X + 32 * jj, 16, 1024, 2), idesc,
+                            !first || sb != 0 || jj != 0);
           first = false;
           mma_issued = true;
           ptx::tc_commit(&dempty[d]);
@@ -311,16 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
     // ---------------------------------------------------------- converters
     pdl_wait();
     const int cw = warp - 2;
+    // whole k-blocks: warp cw fills tile cw / WPT, rows [part*RPW, (part+1)*RPW)
+    constexpr int RPW = 128 / (C::WHOLE_KB ? C::WPT : 1);
+    const int dt = cw / C::WPT, part = cw % C::WPT;
     FragIter fi{my_start, my_end, p.nkb};
     int tile, kb0, kb1;
     int j = 0;                                  // index of the k-block in this CTA's sequence
-    bool ok = !C::WHOLE_KB || cw < DSTAGES;     // spare warps have no tile
+    bool ok = !C::WHOLE_KB || dt < DSTAGES;     // spare warps have no tile
     // A warp walks its k-blocks in order and waits for its tile's release
     // before the raw stage (RSTAGES >= DSTAGES), so no barrier parity is
     // ambiguous; no barrier joins the converter warps.
     while (ok && fi.next(tile, kb0, kb1)) {
       for (int kb = kb0; kb < kb1; ++kb, ++j) {
-        if (C::WHOLE_KB && j % DSTAGES != cw) continue;
+        if (C::WHOLE_KB && j % DSTAGES != dt) continue;
         const int r = j % RST, d = j % DSTAGES;
         const uint32_t rph = (uint32_t)((j / RST) & 1), dph = (uint32_t)((j / DSTAGES) & 1);
         bool got = ptx::mbar_wait_bounded(&dempty[d], dph ^ 1u, limit, kTimeoutNs, abort_flag);
@@ -330,37 +355,46 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
           ok = false;
           break;
         }
+        const int nsub = nsub_of(kb);
         if constexpr (C::WHOLE_KB) {
-          // the whole 128 x 64 tile in eight steps of 16 rows; lane pair
-          // (2i, 2i+1) takes the two 32-code halves of row 16s + i, so that
-          // every load instruction reads 512 contiguous bytes.  All loads
-          // first (the compiler cannot move them past the tile stores), the
-          // scales of rows i + 16u as two 16-byte loads.
+          // the warp's RPW rows of each 64-wide sub-block, in steps of 16
+          // rows; lane pair (2i, 2i+1) takes the two 32-code halves of row
+          // part*RPW + 16s + i, so that every load instruction reads 512
+          // contiguous bytes.  All loads of a sub-block first (the compiler
+          // cannot move them past the tile stores); the 16-byte scale row q
+          // holds the scales of rows q, q+32, q+64, q+96.
+          constexpr int STEPS = RPW / 16;
           const int hf = lane & 1, i = lane >> 1;
-          uint4 cv[8];
+          for (int sb = 0; sb < nsub; ++sb) {
+            uint4 cv[STEPS];
 #pragma unroll
-          for (int s8 = 0; s8 < 8; ++s8)
-            cv[s8] = *reinterpret_cast<const uint4 *>(st_wc(r) + (16 * s8 + i) * (BK / 2) + hf * 16);
-          // 16-byte scale row q holds the scales of rows q, q+32, q+64, q+96
-          const uint4 sa = *reinterpret_cast<const uint4 *>(st_ws(r) + i * 16);
-          const uint4 sb = *reinterpret_cast<const uint4 *>(st_ws(r) + (16 + i) * 16);
-          const uint32_t sfs[8] = {sa.x, sb.x, sa.y, sb.y, sa.z, sb.z, sa.w, sb.w};
+            for (int s8 = 0; s8 < STEPS; ++s8)
+              cv[s8] = *reinterpret_cast<const uint4 *>(st_wc(r) + (part * RPW + 16 * s8 + i) * (BK / 2) + sb * 32 +
+                                                        hf * 16);
+            const uint4 sa = *reinterpret_cast<const uint4 *>(st_ws(r) + sb * 512 + i * 16);
+            const uint4 sz = *reinterpret_cast<const uint4 *>(st_ws(r) + sb * 512 + (16 + i) * 16);
 #pragma unroll
-          for (int s8 = 0; s8 < 8; ++s8) {
-            const int row = 16 * s8 + i;
-            const uint32_t cwd[4] = {cv[s8].x, cv[s8].y, cv[s8].z, cv[s8].w};
-            uint8_t *rowp = st_wb(d) + (row >> 3) * 1024 + (row & 7) * 128;
-            const int swz = row & 7;
+            for (int s8 = 0; s8 < STEPS; ++s8) {
+              const int row = part * RPW + 16 * s8 + i;
+              const uint4 &sv = (s8 & 1) ? sz : sa;          // row & 31 is i or 16 + i
+              const int comp = (row >> 5) & 3;
+              const uint32_t sfw = comp == 0 ? sv.x : comp == 1 ? sv.y : comp == 2 ? sv.z : sv.w;
+              const uint32_t cwd[4] = {cv[s8].x, cv[s8].y, cv[s8].z, cv[s8].w};
+              uint8_t *rowp = st_wb(d) + sb * SUB_WB + (row >> 3) * 1024 + (row & 7) * 128;
+              const int swz = row & 7;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int c = 4 * hf + u;         // 16-byte chunk c = elements 8c .. 8c+7
-              uint32_t o[4];
-              dequant8(cwd[u], e4m3_to_h2((sfs[s8] >> (8 * (c >> 1))) & 0xFFu), o);
-              *reinterpret_cast<uint4 *>(rowp + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+              for (int u = 0; u < 4; ++u) {
+                const int c = 4 * hf + u;       // 16-byte chunk c = elements 8c .. 8c+7
+                uint32_t o[4];
+                dequant8(cwd[u], e4m3_to_h2((sfw >> (8 * (c >> 1))) & 0xFFu), o);
+                *reinterpret_cast<uint4 *>(rowp + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+              }
             }
           }
         } else {
-          // 16 rows of the tile: two lanes per row, 32 elements each
+          // 16 rows of the tile (one 64-wide sub-block: BK = 64 here): two
+          // lanes per row, 32 elements each
+          static_assert(C::WHOLE_KB || SUB == 1, "row-split converters take 64-wide k-blocks");
           const int row = 16 * cw + (lane >> 1), hf = lane & 1;
           const uint4 cv = *reinterpret_cast<const uint4 *>(st_wc(r) + row * (BK / 2) + hf * 16);
           const uint32_t sfw =
@@ -529,7 +563,8 @@ Plan make_plan(int64_t m, int64_t n, int64_t k) {
   pl.nt = pick_nt(m);
   pl.wtiles = (int)((n + 127) / 128);
   pl.ttiles = (int)((m + pl.nt - 1) / pl.nt);
-  pl.nkb = (int)(k / BK);
+  const int bk = pl.nt <= 32 ? Cfg<16>::BK : Cfg<64>::BK;   // k-block width of the token tile
+  pl.nkb = (int)((k + bk - 1) / bk);                         // the last one may be 64 wide
   const int tiles = pl.wtiles * pl.ttiles;
   pl.can_split = pl.nt <= 64;
   if (pl.can_split) {
@@ -559,8 +594,8 @@ cudaError_t launch_nt(const Plan &pl, const uint16_t *x, const uint8_t *w, const
   }
   CUtensorMap tm_x, tm_w;
   // activations bf16 [m, k]: box 128 bytes (64 elements) x NT rows, 128-byte swizzle
-  // weight codes [n, k/2]: box 32 bytes (64 codes) x 128 rows, no swizzle
-  if (!make_byte_map(&tm_x, x, m, k * 2, 128, NT, true) || !make_byte_map(&tm_w, w, n, k / 2, 32, 128, false))
+  // weight codes [n, k/2]: box BK/2 bytes x 128 rows, no swizzle
+  if (!make_byte_map(&tm_x, x, m, k * 2, 128, NT, true) || !make_byte_map(&tm_w, w, n, k / 2, C::BK / 2, 128, false))
     return cudaErrorInvalidValue;
   W4A16Args a{};
   a.wsf = wsf;

@@ -6,8 +6,9 @@ Swap-AB GEMM (weights as the MMA's 128-row operand, 256-wide k-blocks):
 every CTA takes floor(tiles/grid) whole tiles, the other tiles are cut into
 one contiguous run of (tile, k-block) pairs per CTA, and when those shared
 tiles have fewer k-blocks than there are CTAs one round of whole tiles joins
-them.  W4A16 tensor-core GEMM (64-wide k-blocks): one contiguous run per CTA
-up to 64 tokens.  The scratch is a 256-byte-rounded counter per tile plus
+them.  W4A16 tensor-core GEMM (k-blocks 128 wide up to 32 tokens, the last
+one possibly 64 wide; 64 wide above): one contiguous run per CTA up to 64
+tokens.  The scratch is a 256-byte-rounded counter per tile plus
 [grid][fragment slots][tokens padded][128] fp32 partials, only when a tile is
 shared.  The rule that every CTA between a shared tile's first and last owner
 contributes to it is checked on the restated partition.
@@ -57,7 +58,8 @@ def w4a16_ws(m, n, k, sms):
     nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128 if m <= 128 else 256
     if nt > 64:
         return 0
-    tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), k // 64
+    bk = 128 if nt <= 32 else 64            # k-block width: 128 up to 32 tokens
+    tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), math.ceil(k / bk)
     w = tiles * nkb
     grid = min(w, sms)
     maxfrag = math.ceil(math.ceil(w / grid) / nkb) + 1
