@@ -475,10 +475,15 @@ def run_ours(args, world, rank, local):
             # gate_up weights (codes + scales), quantized x in, NVFP4 h out
             nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 9 // 16 + m * inter * 9 // 16 for m in ms)
             achieved = nbytes / tot_s / 1e9
+            # traffic: DRAM bytes read + written by one launch of this kernel
+            # in an ncu capture of this bench command (summary in profiles/
+            # swapab_swiglu_gate_up_m16_h5120.md); to be set to None whenever
+            # the kernel changes before it is captured again
             roofline = {"bound": "hbm",
                         "kernel": "nvfp4_gemm_swiglu_quant gate_up 34816x5120 (swap-AB tcgen05, M=1..16)",
                         "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                        "traffic": None, "algorithmic_bytes_per_step": nbytes}
+                        "traffic": 100.42e6 + 2.94e6, "traffic_unit": "bytes per launch",
+                        "algorithmic_bytes_per_launch": nbytes / len(ms), "algorithmic_bytes_per_step": nbytes}
         elif wl == "prefill":
             flops = sum(4.0 * m * hid * inter for m in ms)
             achieved = flops / tot_s / 1e12
