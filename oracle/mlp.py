@@ -32,8 +32,10 @@ Pins (tests/test_oracle_mlp.py): brute-force triple loops on tiny shapes,
 exact integer results with power-of-two scales, silu closed forms
 (silu(0)=0, silu(x)-silu(-x)=x, limits), the fused == unfused invariant, and
 W4A16 == W4A4 when x is exactly representable, hand-worked bf16 products of
-the AWQ pre-scale and agreement with ml_dtypes' bf16 multiply.  The whole-MLP numbers have no
-external implementation to compare against: parity unpinned beyond these.
+the AWQ pre-scale and agreement with ml_dtypes' bf16 multiply.  The three MLP
+compositions are pinned by a hand-built case whose every step is exact (gates
+of +-32, power-of-two scales, permutation weights): the output is a signed,
+scaled permutation of x worked out by hand, zero where the gate is negative.
 """
 import numpy as np
 
