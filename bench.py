@@ -47,7 +47,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default="decode", choices=["decode", "prefill", "w4a16"],
                    help="decode (default line) | prefill H7168/I18432 | w4a16 H5120/I17408")
-    p.add_argument("--m", type=int, default=None, help="single M for prefill / w4a16")
+    p.add_argument("--m", type=int, default=None, help="single M (decode: instead of the 1..16 sweep)")
+    p.add_argument("--algo", default="auto", choices=["auto", "gemv", "tc", "swapab"],
+                   help="GEMM kernel family of the chain's GEMMs (auto: the library's choice by M)")
     p.add_argument("--decode-path", default="chain", choices=["fused", "chain"],
                    help="decode MLP as three launches (default) or one nvfp4_mlp_decode launch")
     return p.parse_args()
@@ -238,8 +240,11 @@ def run_ours(args, world, rank, local):
 
     wl = args.workload
     if wl == "decode":
-        hid, inter, ms, ncopy = H, I, MS, NCOPY
+        hid, inter, ms, ncopy = H, I, ((args.m,) if args.m else MS), NCOPY
         metric, workload = METRIC, WORKLOAD
+        if args.m:
+            metric = f"NVFP4 MLP tokens/s (decode H5120 I17408, M={args.m})"
+            workload = f"decode dense MLP W4A4 NVFP4, hidden 5120, intermediate 17408, M={args.m}"
     elif wl == "prefill":
         hid, inter = 7168, 18432
         ms = (args.m or 8192,)
@@ -255,6 +260,9 @@ def run_ours(args, world, rank, local):
     tokens_per_step = sum(ms)
     mmax = max(ms)
     fused_decode = wl == "decode" and args.decode_path == "fused"
+    algo = {"auto": nv.ALGO_AUTO, "gemv": nv.ALGO_GEMV, "tc": nv.ALGO_TC, "swapab": nv.ALGO_TC_SWAPAB}[args.algo]
+    if fused_decode and algo != nv.ALGO_AUTO:
+        raise SystemExit("--algo applies to the chain of separate GEMM launches, not --decode-path fused")
     interleaved = wl in ("prefill", "decode")
 
     w_gu0 = make_weight(2 * inter, hid, interleave=interleaved)
@@ -314,13 +322,13 @@ def run_ours(args, world, rank, local):
     x_in = {m: x[:m] for m in ms}
     # one zero-filled scratch buffer (split-K partials + arrival counters),
     # sized for the largest GEMM of the chain and shared by its sequential calls
-    ws_bytes = max([nv.nvfp4_workspace_bytes(m, 2 * inter, hid) for m in ms] +
-                   [nv.nvfp4_workspace_bytes(m, hid, inter) for m in ms] + [0])
+    ws_bytes = max([nv.nvfp4_workspace_bytes(m, 2 * inter, hid, algo) for m in ms] +
+                   [nv.nvfp4_workspace_bytes(m, hid, inter, algo) for m in ms] + [0])
     if fused_decode:
         ws_bytes = max(nv.nvfp4_mlp_decode_workspace_bytes(m, hid, inter) for m in ms)
     if wl == "w4a16":
-        ws_bytes = max([nv.bf16_fp4_gemm_workspace_bytes(m, 2 * inter, hid) for m in ms] +
-                       [nv.bf16_fp4_gemm_workspace_bytes(m, hid, inter) for m in ms] + [0])
+        ws_bytes = max([nv.bf16_fp4_gemm_workspace_bytes(m, 2 * inter, hid, algo) for m in ms] +
+                       [nv.bf16_fp4_gemm_workspace_bytes(m, hid, inter, algo) for m in ms] + [0])
     ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     # the stream handle as an int: the bindings then skip looking up torch's
@@ -332,13 +340,14 @@ def run_ours(args, world, rank, local):
         b = bufs[m]
         (gq, gsf, _), (dq, dsf, _) = wc
         if wl == "w4a16":
-            nv.bf16_fp4_gemm(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes, stream=SH[0])
+            nv.bf16_fp4_gemm_ex(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes, algo,
+                                stream=SH[0])
         elif fused_decode:
             nv.nvfp4_mlp_decode(x_in[m], gs_x_d, gq, gsf, a_gu, gs_h_d, dq, dsf, a_dn, b["xq"], b["xs"],
                                 b["hq"], b["hs"], b["out"], m, hid, inter, True, ws, ws_bytes, stream=SH[0])
         else:
-            nv.nvfp4_gemm_swiglu_quant(b["xq"], b["xs"], gq, gsf, a_gu, gs_h_d, b["hq"], b["hs"], m,
-                                       2 * inter, hid, ws, ws_bytes, stream=SH[0])
+            nv.nvfp4_gemm_swiglu_quant_ex(b["xq"], b["xs"], gq, gsf, a_gu, gs_h_d, b["hq"], b["hs"], m,
+                                          2 * inter, hid, ws, ws_bytes, algo, stream=SH[0])
 
     def forward(m, wc, ev=None):
         """One MLP forward; ev = (start, end) events around the dominant kernel."""
@@ -353,9 +362,11 @@ def run_ours(args, world, rank, local):
             ev[1].record()
         if wl == "w4a16":
             nv.silu_mul_bf16(b["gu"], m, inter, b["h16"], stream=SH[0])
-            nv.bf16_fp4_gemm(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes, stream=SH[0])
+            nv.bf16_fp4_gemm_ex(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes, algo,
+                                stream=SH[0])
         elif not fused_decode:
-            nv.nvfp4_gemm(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes, stream=SH[0])
+            nv.nvfp4_gemm_ex(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes, algo,
+                             stream=SH[0])
 
     launches_per_step = sum((1 if fused_decode else 3) for _ in ms)
 
@@ -475,14 +486,21 @@ def run_ours(args, world, rank, local):
             # gate_up weights (codes + scales), quantized x in, NVFP4 h out
             nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 9 // 16 + m * inter * 9 // 16 for m in ms)
             achieved = nbytes / tot_s / 1e9
-            # traffic: DRAM bytes read + written by one launch of this kernel
-            # in an ncu capture of this bench command (summary in profiles/
-            # swapab_swiglu_gate_up_m16_h5120.md); to be set to None whenever
-            # the kernel changes before it is captured again
+            family = {"auto": "swap-AB tcgen05", "swapab": "swap-AB tcgen05", "gemv": "CUDA-core GEMV",
+                      "tc": "128-token-tile tcgen05"}[args.algo]
+            if args.algo == "auto" and mmax > 64:
+                family = "128-token-tile tcgen05"
+            # traffic: DRAM bytes read + written by one launch of the swap-AB
+            # NT = 16 instance (every M <= 16) in an ncu capture of this bench
+            # command (summary in profiles/swapab_swiglu_gate_up_m16_h5120.md);
+            # to be set to None whenever the kernel changes before it is
+            # captured again
+            measured = args.algo in ("auto", "swapab") and mmax <= 16
             roofline = {"bound": "hbm",
-                        "kernel": "nvfp4_gemm_swiglu_quant gate_up 34816x5120 (swap-AB tcgen05, M=1..16)",
+                        "kernel": f"nvfp4_gemm_swiglu_quant gate_up 34816x5120 ({family}, "
+                                  f"M={','.join(map(str, ms))})",
                         "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                        "traffic": 100.42e6 + 2.94e6, "traffic_unit": "bytes per launch",
+                        "traffic": 100.42e6 + 2.94e6 if measured else None, "traffic_unit": "bytes per launch",
                         "algorithmic_bytes_per_launch": nbytes / len(ms), "algorithmic_bytes_per_step": nbytes}
         elif wl == "prefill":
             flops = sum(4.0 * m * hid * inter for m in ms)
@@ -542,7 +560,8 @@ def run_ours(args, world, rank, local):
             "config": {"workload": workload, "tokens_per_step": tokens_per_step,
                        "l2": f"{ncopy} rotating weight copies, {ncopy * weight_bytes / 1e6:.0f} MB > L2",
                        "graph": "one CUDA graph per step", "parallelism": f"replicas{world}",
-                       **({"decode_path": args.decode_path} if wl == "decode" else {})},
+                       **({"decode_path": args.decode_path} if wl == "decode" else {}),
+                       **({"algo": args.algo} if args.algo != "auto" else {})},
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "note": "direct API calls, no graph, pinned host buffers"},
