@@ -1,11 +1,9 @@
 """Host-side checks of the C ABI: the library builds, loads and exports every
 function declared in include/nvfp4mlp.h; argument validation answers before
 any launch.  No GPU needed (and no compute call is made)."""
-import ctypes
 import os
 import re
 
-import numpy as np
 import pytest
 
 import nvfp4_quantized_dense_gb300 as nv
