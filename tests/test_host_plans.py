@@ -10,8 +10,10 @@ them.  W4A16 tensor-core GEMM (k-blocks 128 wide up to 32 tokens, the last
 one possibly 64 wide; 64 wide above): one contiguous run per CTA up to 64
 tokens.  The scratch is a 256-byte-rounded counter per tile plus
 [grid][fragment slots][tokens padded][128] fp32 partials, only when a tile is
-shared.  The rule that every CTA between a shared tile's first and last owner
-contributes to it is checked on the restated partition.
+shared.  The whole-MLP decode kernel plans both of its GEMM phases the
+swap-AB way on one grid (the smaller of the SM count and either phase's
+k-block count).  The rule that every CTA between a shared tile's first and
+last owner contributes to it is checked on the restated partition.
 """
 import math
 
@@ -108,6 +110,31 @@ def test_swapab_partition_contributors_are_contiguous(m, n, k, sms):
         # (its partial sits in fragment slot 0)
         for c in cs[1:]:
             assert starts[c] // kbt == t
+
+
+def mlp_decode_ws(m, hid, inter, sms):
+    """Scratch of the whole-MLP decode kernel: sync words, h-slice counters
+    and both phases' tile counters, then each phase's fp32 partials (every
+    phase uses the swap-AB mixed partition on the same grid)."""
+    nt = 16 if m <= 16 else 32 if m <= 32 else 64
+    tiles = [2 * inter // 128, hid // 128]
+    kbt = [math.ceil(hid / 256), math.ceil(inter / 256)]
+    grid = min(tiles[0] * kbt[0], tiles[1] * kbt[1], sms)
+    ws = r256(256 + (kbt[1] + tiles[0] + tiles[1]) * 4)
+    for g in range(2):
+        whole = tiles[g] // grid
+        split = tiles[g] - whole * grid
+        if whole > 0 and split > 0 and split * kbt[g] < grid:
+            whole, split = whole - 1, split + grid
+        per = math.ceil(split * kbt[g] / grid)
+        ws += r256(grid * (math.ceil(per / kbt[g]) + 1) * nt * 128 * 4)
+    return ws
+
+
+@pytest.mark.parametrize("m,hid,inter", [(1, 5120, 17408), (16, 5120, 17408), (64, 7168, 18432), (4, 256, 512),
+                                         (33, 1024, 2048), (1, 128, 64)])
+def test_mlp_decode_scratch_matches_plan(lib, m, hid, inter):
+    assert nv.nvfp4_mlp_decode_workspace_bytes(m, hid, inter) == mlp_decode_ws(m, hid, inter, sm_count())
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 34816, 5120), (16, 34816, 5120), (16, 5120, 17408), (64, 384, 2048),
