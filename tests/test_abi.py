@@ -147,3 +147,25 @@ def test_mlp_decode_host_checks(lib):
     assert lib.nvfp4_mlp_decode(*bad) == nv.OK
     assert nv.nvfp4_mlp_decode_workspace_bytes(4, 256, 512) > 0
     assert nv.nvfp4_mlp_decode_workspace_bytes(65, 256, 512) == 0
+
+
+def test_per_token_and_masked_host_checks(lib):
+    # per-token quantize: the row-scale output is required, K % 16, layout enum
+    assert lib.nvfp4_quantize_per_token(FAKE, 4, 256, FAKE, FAKE, 0, None, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token(FAKE, 4, 100, FAKE, FAKE, 0, FAKE, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_quantize_per_token(FAKE, 4, 256, FAKE, FAKE, 5, FAKE, None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token(FAKE, -1, 256, FAKE, FAKE, 0, FAKE, None) == nv.ERR_INVALID_ARG
+    # per-token GEMMs: the row factor is required
+    assert lib.nvfp4_gemm_per_token(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None, 0, 0,
+                                    None) == nv.ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_swiglu_quant_per_token(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256,
+                                                 256, None, 0, 0, None) == nv.ERR_INVALID_ARG
+    # masked groups: masked_m required, I % 16, at most 65535 groups
+    assert lib.silu_mul_nvfp4_quantize_masked(FAKE, None, 2, 4, 256, FAKE, FAKE, FAKE,
+                                              None) == nv.ERR_INVALID_ARG
+    assert lib.silu_mul_nvfp4_quantize_masked(FAKE, FAKE, -1, 4, 256, FAKE, FAKE, FAKE,
+                                              None) == nv.ERR_INVALID_ARG
+    assert lib.silu_mul_nvfp4_quantize_masked(FAKE, FAKE, 2, 4, 24, FAKE, FAKE, FAKE,
+                                              None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.silu_mul_nvfp4_quantize_masked(FAKE, FAKE, 65536, 4, 256, FAKE, FAKE, FAKE,
+                                              None) == nv.ERR_UNSUPPORTED_SHAPE
