@@ -20,7 +20,8 @@ def lib():
 
 
 def _declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b([a-z0-9_]+)\s*\(", text)) - {"sizeof"})
 

@@ -13,7 +13,9 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "quant_block.txt")
 
 def _golden_cases():
     cases = []
-    for line in open(GOLDEN):
+    with open(GOLDEN) as f:
+        lines = f.read().splitlines()
+    for line in lines:
         if not line.strip() or line.startswith("#"):
             continue
         name, gs, xs, sf, packed = [f.strip() for f in line.split("|")]

@@ -28,7 +28,7 @@ def _worker(rank, world, port, out):
 
 def test_two_replicas_take_the_slowest_rank():
     port = 29500 + os.getpid() % 1000
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.start_processes(_worker, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
         res = dict(out)
