@@ -200,6 +200,24 @@ def test_swiglu_deepseek_decode_full_size_sampled(lib, m, algo):
     _swiglu_case(lib, 2, m, ws.n, ws.k, ws, algo, sampled_blocks=128)
 
 
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 16])
+def test_swiglu_decode_h5120_full_size_sampled(lib, m):
+    """The bench's decode step: fused gate_up + SwiGLU + requant on the
+    interleaved 34816x5120 weight (H5120/I17408) in the swap-AB launch the
+    bench times (NT = 16, mixed split-K over all SMs); 128 sampled
+    16-feature blocks."""
+    ws = weights(1, "gate_up")
+    _swiglu_case(lib, 1, m, ws.n, ws.k, ws, TC_SWAPAB, sampled_blocks=128)
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+@pytest.mark.parametrize("m", [1, 16])
+def test_w4a4_decode_full_size_sampled_tc(lib, m, which):
+    """The same decode shapes forced onto the 128-token-tile kernel (the
+    bench's --algo tc)."""
+    test_w4a4_decode_full_size_sampled(lib, m, which, TC)
+
+
 @pytest.mark.parametrize("m", [1024, 4096, 8192])
 def test_swiglu_prefill_full_size_sampled(lib, m):
     """Prefill H7168/I18432, M up to 8192, the launch the prefill chain uses:
