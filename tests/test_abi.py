@@ -170,3 +170,33 @@ def test_per_token_and_masked_host_checks(lib):
                                               None) == nv.ERR_UNSUPPORTED_SHAPE
     assert lib.silu_mul_nvfp4_quantize_masked(FAKE, FAKE, 65536, 4, 256, FAKE, FAKE, FAKE,
                                               None) == nv.ERR_UNSUPPORTED_SHAPE
+
+
+def _declared_params():
+    """{function: [C parameter type, ...]} parsed from the header."""
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(?:nvfp4_status|size_t|int|const char \*)\s+([a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        out[m.group(1)] = [re.sub(r"([\s*])[a-z0-9_]+$", r"\1", p).strip() for p in params]
+    return out
+
+
+def _ctype_kind(c_type):
+    t = c_type.replace("const ", "").strip()
+    if "*" in t or t == "nvfp4_stream_t":
+        return "ptr"
+    return {"int64_t": "i64", "size_t": "size", "uint32_t": "u32", "int": "int",
+            "nvfp4_sf_layout": "int", "nvfp4_algo": "int"}[t]
+
+
+def test_binding_signatures_match_the_header():
+    import ctypes
+    kind = {ctypes.c_void_p: "ptr", ctypes.c_int64: "i64", ctypes.c_size_t: "size", ctypes.c_int: "int",
+            ctypes.c_uint32: "u32"}
+    declared = _declared_params()
+    for fn, argtypes in nv._SIGS.items():
+        assert fn in declared, fn
+        got = ["ptr" if isinstance(a, type) and issubclass(a, ctypes._Pointer) else kind[a] for a in argtypes]
+        assert got == [_ctype_kind(t) for t in declared[fn]], fn
