@@ -55,13 +55,16 @@ def test_quantize_full_size_prefill_sampled_rows(lib):
 def test_quantize_special_blocks(lib):
     """Exact ties, SF == 0 blocks with negative zeros, saturation, outliers."""
     rows = []
-    for line in open(__file__.replace("test_gpu_elementwise.py", "golden/quant_block.txt")):
+    with open(__file__.replace("test_gpu_elementwise.py", "golden/quant_block.txt")) as f:
+        lines = f.read().splitlines()
+    for line in lines:
         if line.strip() and not line.startswith("#"):
             rows.append(np.array(line.split("|")[2].split(), dtype=np.float32))
-    x = np.concatenate(rows)[None, :]                      # 1 x 48, gs = 1
+    x = np.concatenate(rows)[None, :]                      # the golden blocks side by side
     x = np.concatenate([x, -x, x * np.float32(1e-30), x * np.float32(1e4)], axis=0).astype(np.float32)
     bits, xv = synth.to_bf16_bits(x)
-    for gs in (np.float32(1.0), np.float32(0.5), oracle.global_scale(np.abs(xv).max())):
+    # gs = fp32(0.3) puts the golden case-4 block's scale on an exact E4M3 tie
+    for gs in (np.float32(1.0), np.float32(0.5), np.float32(0.3), oracle.global_scale(np.abs(xv).max())):
         ref_q, ref_s = oracle.quantize_nvfp4(xv, gs)
         q, s = _run_quantize(lib, bits, xv.shape[0], xv.shape[1], gs, 1)
         assert np.array_equal(q, ref_q) and np.array_equal(s.reshape(ref_s.shape), ref_s)

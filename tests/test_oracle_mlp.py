@@ -271,3 +271,45 @@ def test_whole_mlp_w4a16_exact():
     np.testing.assert_allclose(out, expected, rtol=0, atol=1e-6)
     nz = expected != 0
     np.testing.assert_array_equal(out[nz], expected[nz])
+
+
+def test_silu_mul_bf16_rounds_once_from_the_exact_product():
+    """Worked by hand: silu(17) = 17 / (1 + e^-17) = 16.99999929..., times
+    1.1875 gives 20.18749916..., just below 20.1875, the midpoint between
+    the bf16 neighbours 20.125 and 20.25 (quantum 1/8 on [16, 32)): one
+    rounding gives 20.125.  Rounding to fp32 first would land exactly on the
+    midpoint (fp32 spacing there is 2^-19) and tie to the even 20.25."""
+    out = oracle.silu_mul_bf16(np.array([[17.0, 1.1875]]))
+    assert out[0, 0] == 20.125
+
+
+def _pack_e2m1_row(vals):
+    codes = [_code(v) for v in vals]
+    return np.array([codes[j] | (codes[j + 1] << 4) for j in range(0, 16, 2)], dtype=np.uint8)
+
+
+def test_fused_swiglu_takes_the_unrounded_gate_up():
+    """Worked by hand (one 16-block, scales 1.0, alpha 0.5, gs_h 1/8):
+    x = [6, 6, 4, 0.5, 0...].  Gate row 0 = [6, 6, 2, 0.5] gives
+    0.5 * 80.25 = 40.125; gate row 1 = [6, 6, 6] gives 48; up rows 0 and 1 =
+    [0, 0, 0.5] give 1.  h = silu(g) * u is 40.125 and 48 (silu(g) = g within
+    1e-16 here); the block amax 48 makes the scale 48/6 * 1/8 = 1.0, so the
+    scaled values are 5.015625 -> E2M1 6 (code 7) and 6 (code 7).  Had the
+    gate_up been rounded to bf16 first, 40.125 (a tie between 40 and 40.25)
+    would become 40, the scaled value exactly 5, and the tie would go to the
+    even 4 (code 6) -- which is what the unfused chain on a bf16 gate_up does."""
+    x = np.zeros((1, 8), dtype=np.uint8)
+    x[0] = _pack_e2m1_row([6, 6, 4, 0.5] + [0] * 12)
+    w = np.zeros((32, 8), dtype=np.uint8)
+    w[0] = _pack_e2m1_row([6, 6, 2, 0.5] + [0] * 12)
+    w[1] = _pack_e2m1_row([6, 6, 6] + [0] * 13)
+    w[16] = w[17] = _pack_e2m1_row([0, 0, 0.5] + [0] * 13)
+    one = np.full((1, 1), 0x38, dtype=np.uint8)
+    wsf = np.full((32, 1), 0x38, dtype=np.uint8)
+    hq, hs = oracle.gemm_swiglu_quant(x, one, w, wsf, np.float32(0.5), np.float32(0.125))
+    assert hs[0, 0] == 0x38
+    assert list(hq[0]) == [0x77] + [0] * 7
+    gu = oracle.gemm_w4a4(x, one, w, wsf, np.float32(0.5))          # the unfused chain's bf16 gate_up
+    assert gu[0, 0] == 40.0 and gu[0, 1] == 48.0
+    uq, us = oracle.silu_mul_quant(gu, np.float32(0.125))
+    assert us[0, 0] == 0x38 and list(uq[0]) == [0x76] + [0] * 7
