@@ -141,3 +141,40 @@ def test_mlp_decode_scratch_matches_plan(lib, m, hid, inter):
                                    (33, 128, 1024), (5, 96, 320), (128, 34816, 5120), (1024, 34816, 5120)])
 def test_w4a16_scratch_matches_plan(lib, m, n, k):
     assert nv.bf16_fp4_gemm_workspace_bytes(m, n, k, nv.ALGO_TC) == w4a16_ws(m, n, k, sm_count())
+
+
+def _random_shapes(count, seed):
+    import numpy as np
+    g = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        m = int(g.integers(1, 65))
+        n = int(g.integers(1, 400)) * 32
+        k = int(g.integers(1, 300)) * 64
+        out.append((m, n, k))
+    return out
+
+
+def test_swapab_scratch_matches_plan_random_shapes(lib):
+    """The restated plan and the library agree on 300 random decode shapes
+    (M 1..64, N multiples of 32 up to 12768, K multiples of 64 up to 19136)."""
+    sms = sm_count()
+    for m, n, k in _random_shapes(300, 11):
+        assert nv.nvfp4_workspace_bytes(m, n, k, nv.ALGO_TC_SWAPAB) == swapab_plan(m, n, k, sms)["ws"], (m, n, k)
+
+
+def test_swapab_partition_invariants_random_shapes():
+    for m, n, k in _random_shapes(300, 12):
+        for sms in (148, 152):
+            pl = swapab_plan(m, n, k, sms)
+            grid, kbt, split = pl["grid"], pl["kbt"], pl["split"]
+            assert split + pl["whole"] * grid == pl["tiles"]
+            units = split * kbt
+            if units and split:
+                assert units >= grid, (m, n, k, sms)
+
+
+def test_w4a16_scratch_matches_plan_random_shapes(lib):
+    sms = sm_count()
+    for m, n, k in _random_shapes(300, 13):
+        assert nv.bf16_fp4_gemm_workspace_bytes(m, n, k, nv.ALGO_TC) == w4a16_ws(m, n, k, sms), (m, n, k)
