@@ -84,8 +84,17 @@ def quantized_activation(wid, m, k=None):
 
 
 def sample_rows(n, count, seed=0, block=1):
-    """Sorted sample of row indices (whole blocks of `block` rows)."""
+    """Sorted sample of row indices (whole blocks of `block` rows), stratified:
+    the n // block blocks are cut into `count` equal strata and one block is
+    drawn from each, the first and the last block always included, so that a
+    sample at least as large as the number of kernel tiles touches every tile."""
     g = np.random.default_rng(seed)
     nb = n // block
-    pick = np.sort(g.choice(nb, size=min(count, nb), replace=False))
+    if count >= nb:
+        pick = np.arange(nb)
+    else:
+        edges = np.linspace(0, nb, count + 1).astype(np.int64)
+        pick = np.array([g.integers(lo, hi) for lo, hi in zip(edges[:-1], edges[1:])], dtype=np.int64)
+        pick[0], pick[-1] = 0, nb - 1
+        pick = np.unique(pick)
     return (pick[:, None] * block + np.arange(block)[None, :]).reshape(-1)

@@ -195,19 +195,20 @@ def test_swiglu_small_shapes(lib, m, n, k, algo):
 @pytest.mark.parametrize("m", [1, 8, 32, 64])
 def test_swiglu_deepseek_decode_full_size_sampled(lib, m, algo):
     """DeepSeek-V3-shaped decode, x with 1% outliers x20, interleaved
-    36864x7168 gate_up weight; 128 sampled 16-feature blocks."""
+    36864x7168 gate_up weight; 288 stratified 16-feature blocks, one in each
+    64-feature (128-row) weight tile."""
     ws = weights(2, "gate_up")
-    _swiglu_case(lib, 2, m, ws.n, ws.k, ws, algo, sampled_blocks=128)
+    _swiglu_case(lib, 2, m, ws.n, ws.k, ws, algo, sampled_blocks=288)
 
 
 @pytest.mark.parametrize("m", [1, 2, 4, 8, 16])
 def test_swiglu_decode_h5120_full_size_sampled(lib, m):
     """The bench's decode step: fused gate_up + SwiGLU + requant on the
     interleaved 34816x5120 weight (H5120/I17408) in the swap-AB launch the
-    bench times (NT = 16, mixed split-K over all SMs); 128 sampled
-    16-feature blocks."""
+    bench times (NT = 16, mixed split-K over all SMs); 272 stratified
+    16-feature blocks, one in each 64-feature (128-row) weight tile."""
     ws = weights(1, "gate_up")
-    _swiglu_case(lib, 1, m, ws.n, ws.k, ws, TC_SWAPAB, sampled_blocks=128)
+    _swiglu_case(lib, 1, m, ws.n, ws.k, ws, TC_SWAPAB, sampled_blocks=272)
 
 
 @pytest.mark.parametrize("which", ["gate_up", "down"])
@@ -221,9 +222,10 @@ def test_w4a4_decode_full_size_sampled_tc(lib, m, which):
 @pytest.mark.parametrize("m", [1024, 4096, 8192])
 def test_swiglu_prefill_full_size_sampled(lib, m):
     """Prefill H7168/I18432, M up to 8192, the launch the prefill chain uses:
-    256 sampled tokens x 32 sampled 16-feature blocks."""
+    256 stratified tokens x 144 stratified 16-feature blocks (one in each
+    128-feature span of the 256-row weight tiles)."""
     ws = weights(3, "gate_up")
-    _swiglu_case(lib, 3, m, ws.n, ws.k, ws, 0, sampled_blocks=32, sampled_tokens=256)
+    _swiglu_case(lib, 3, m, ws.n, ws.k, ws, 0, sampled_blocks=144, sampled_tokens=256)
 
 
 @pytest.mark.parametrize("m", [1024, 8192])
