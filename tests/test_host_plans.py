@@ -13,7 +13,10 @@ tokens.  The scratch is a 256-byte-rounded counter per tile plus
 shared.  The whole-MLP decode kernel plans both of its GEMM phases the
 swap-AB way on one grid (the smaller of the SM count and either phase's
 k-block count).  The rule that every CTA between a shared tile's first and
-last owner contributes to it is checked on the restated partition.
+last owner contributes to it is checked on the restated partition, and so is
+the kernels' reduction bookkeeping: the walk of each CTA (its run, then its
+whole tiles), the first/last owner formula and each contributor's partial
+slot, written out as the kernels compute them.
 """
 import math
 
@@ -178,3 +181,91 @@ def test_w4a16_scratch_matches_plan_random_shapes(lib):
     sms = sm_count()
     for m, n, k in _random_shapes(300, 13):
         assert nv.bf16_fp4_gemm_workspace_bytes(m, n, k, nv.ALGO_TC) == w4a16_ws(m, n, k, sms), (m, n, k)
+
+
+def _mixed_fragments(kbt, grid, whole, split_tiles, j):
+    """The fragments CTA j walks under the swap-AB mixed partition: its run of
+    the split units (start(j) = floor(j * U / grid)), then its whole tiles
+    split_tiles + j*whole + [0, whole)."""
+    units = split_tiles * kbt
+    x, end = j * units // grid, (j + 1) * units // grid
+    out = []
+    while x < end:
+        tile = x // kbt
+        kb0 = x - tile * kbt
+        kb1 = min(kbt, kb0 + (end - x))
+        out.append((tile, kb0, kb1))
+        x += kb1 - kb0
+    for t in range(split_tiles + j * whole, split_tiles + (j + 1) * whole):
+        out.append((t, 0, kbt))
+    return out
+
+
+@pytest.mark.parametrize("m,n,k", SWAP_CASES + [(1, 5120, 17408), (16, 36864, 7168), (64, 7168, 18432)])
+@pytest.mark.parametrize("sms", [148, 152, 7])
+def test_swapab_reduction_bookkeeping(m, n, k, sms):
+    """Every (tile, k-block) is covered once; for a shared tile the owner of
+    its first and last k-block (cta_of = ((x + 1) * grid - 1) // U, the
+    inverse of start) bracket exactly the CTAs that hold a fragment of it;
+    each contributor's partial slot (f_first for the first owner, 0 for the
+    others) is its fragment's index in its own walk, below maxfrag."""
+    pl = swapab_plan(m, n, k, sms)
+    grid, kbt, whole, split = pl["grid"], pl["kbt"], pl["whole"], pl["split"]
+    units = split * kbt
+    maxfrag = (math.ceil(math.ceil(units / grid) / kbt) + 1) if units else 1
+    seen = {}
+    holders = {}
+    for j in range(grid):
+        for f, (tile, kb0, kb1) in enumerate(_mixed_fragments(kbt, grid, whole, split, j)):
+            for kb in range(kb0, kb1):
+                assert (tile, kb) not in seen
+                seen[(tile, kb)] = j
+            if tile < split:
+                holders.setdefault(tile, []).append((j, f))
+    assert len(seen) == pl["tiles"] * kbt
+    cta_of = lambda x: ((x + 1) * grid - 1) // units
+    start = lambda j: j * units // grid
+    for tile, hs in holders.items():
+        c_first, c_last = cta_of(tile * kbt), cta_of(tile * kbt + kbt - 1)
+        assert [c for c, _ in hs] == list(range(c_first, c_last + 1))
+        f_first = tile - start(c_first) // kbt
+        for c, f in hs:
+            slot = f_first if c == c_first else 0
+            assert slot == f and slot < maxfrag, (tile, c, f, slot)
+
+
+def test_swapab_reduction_bookkeeping_random_shapes():
+    for m, n, k in _random_shapes(150, 14):
+        for sms in (148, 152):
+            test_swapab_reduction_bookkeeping(m, n, k, sms)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 34816, 5120), (16, 34816, 5120), (16, 5120, 17408), (64, 384, 2048),
+                                   (33, 128, 1024), (5, 96, 320), (64, 7168, 18432)])
+@pytest.mark.parametrize("sms", [148, 152, 7])
+def test_w4a16_reduction_bookkeeping(m, n, k, sms):
+    """The W4A16 split-K (one contiguous run per CTA over all tiles, up to 64
+    tokens) keeps the same invariants as the swap-AB mixed split with no
+    whole tiles."""
+    nt = 16 if m <= 16 else 32 if m <= 32 else 64
+    bk = 128 if nt <= 32 else 64
+    tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), math.ceil(k / bk)
+    grid = min(tiles * nkb, sms)
+    units = tiles * nkb
+    maxfrag = math.ceil(math.ceil(units / grid) / nkb) + 1
+    seen, holders = set(), {}
+    for j in range(grid):
+        frags = _mixed_fragments(nkb, grid, 0, tiles, j)
+        assert frags, "every CTA owns at least one k-block"
+        for f, (tile, kb0, kb1) in enumerate(frags):
+            for kb in range(kb0, kb1):
+                assert (tile, kb) not in seen
+                seen.add((tile, kb))
+            holders.setdefault(tile, []).append((j, f))
+    assert len(seen) == units
+    for tile, hs in holders.items():
+        c_first, c_last = ((tile * nkb + 1) * grid - 1) // units, ((tile * nkb + nkb) * grid - 1) // units
+        assert [c for c, _ in hs] == list(range(c_first, c_last + 1))
+        f_first = tile - (c_first * units // grid) // nkb
+        for c, f in hs:
+            assert (f_first if c == c_first else 0) == f < maxfrag
