@@ -269,3 +269,46 @@ def test_w4a16_reduction_bookkeeping(m, n, k, sms):
         f_first = tile - (c_first * units // grid) // nkb
         for c, f in hs:
             assert (f_first if c == c_first else 0) == f < maxfrag
+
+
+def _kwalk(kbt, early, u0, u1):
+    """The whole-MLP kernel's walk of the units [u0, u1) of one fragment,
+    written out as the kernel steps it: the early units (u with
+    floor((u+1)*early/kbt) > floor(u*early/kbt)) first, then the others;
+    early unit number e is k-block e, the others follow after `early`."""
+    out = []
+    for pass_ in (0, 1):
+        eb = u0 * early // kbt
+        r = u0 * early - eb * kbt
+        for u in range(u0, u1):
+            is_early = r + early >= kbt
+            e = eb
+            if is_early:
+                eb += 1
+                r += early - kbt
+            else:
+                r += early
+            if is_early == (pass_ == 0):
+                out.append(e if is_early else early + (u - e))
+    return out
+
+
+@pytest.mark.parametrize("kbt", [1, 2, 3, 20, 28, 68, 72])
+def test_mlp_decode_kwalk_is_a_permutation_of_every_fragment_split(kbt):
+    """Whatever contiguous pieces a tile's units are cut into, the pieces'
+    walks visit every k-block exactly once, early k-blocks (0..early-1) before
+    the others within each piece."""
+    import numpy as np
+    g = np.random.default_rng(kbt)
+    for early in range(0, kbt + 1):
+        assert sorted(_kwalk(kbt, early, 0, kbt)) == list(range(kbt))
+        for _ in range(5):
+            cuts = sorted(set(int(c) for c in g.integers(1, kbt, size=3))) if kbt > 1 else []
+            bounds = [0] + cuts + [kbt]
+            seen = []
+            for a, b in zip(bounds[:-1], bounds[1:]):
+                walk = _kwalk(kbt, early, a, b)
+                n_early = sum(1 for kb in walk if kb < early)
+                assert all(kb < early for kb in walk[:n_early]) and all(kb >= early for kb in walk[n_early:])
+                seen += walk
+            assert sorted(seen) == list(range(kbt)), (kbt, early, bounds)
