@@ -48,8 +48,9 @@ def parse():
     p.add_argument("--workload", default="decode", choices=["decode", "prefill", "w4a16"],
                    help="decode (default line) | prefill H7168/I18432 | w4a16 H5120/I17408")
     p.add_argument("--m", type=int, default=None, help="single M (decode: instead of the 1..16 sweep)")
-    p.add_argument("--algo", default="auto", choices=["auto", "gemv", "tc", "swapab"],
-                   help="GEMM kernel family of the chain's GEMMs (auto: the library's choice by M)")
+    p.add_argument("--algo", default="auto", choices=["auto", "gemv", "tc", "tc1sm", "swapab"],
+                   help="GEMM kernel family of the chain's GEMMs (auto: the library's choice by M; "
+                        "tc: CTA pairs with 2-SM MMAs; tc1sm: one CTA per tile)")
     p.add_argument("--decode-path", default="chain", choices=["fused", "chain"],
                    help="decode MLP as three launches (default) or one nvfp4_mlp_decode launch")
     return p.parse_args()
@@ -283,7 +284,8 @@ def run_ours(args, world, rank, local):
     tokens_per_step = sum(ms)
     mmax = max(ms)
     fused_decode = wl == "decode" and args.decode_path == "fused"
-    algo = {"auto": nv.ALGO_AUTO, "gemv": nv.ALGO_GEMV, "tc": nv.ALGO_TC, "swapab": nv.ALGO_TC_SWAPAB}[args.algo]
+    algo = {"auto": nv.ALGO_AUTO, "gemv": nv.ALGO_GEMV, "tc": nv.ALGO_TC, "tc1sm": nv.ALGO_TC_1SM,
+            "swapab": nv.ALGO_TC_SWAPAB}[args.algo]
     if fused_decode and algo != nv.ALGO_AUTO:
         raise SystemExit("--algo applies to the chain of separate GEMM launches, not --decode-path fused")
     interleaved = wl in ("prefill", "decode")
@@ -510,7 +512,7 @@ def run_ours(args, world, rank, local):
             nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 9 // 16 + m * inter * 9 // 16 for m in ms)
             achieved = nbytes / tot_s / 1e9
             family = {"auto": "swap-AB tcgen05", "swapab": "swap-AB tcgen05", "gemv": "CUDA-core GEMV",
-                      "tc": "128-token-tile tcgen05"}[args.algo]
+                      "tc": "128-token-tile tcgen05, CTA pairs", "tc1sm": "128-token-tile tcgen05"}[args.algo]
             if args.algo == "auto" and mmax > 64:
                 family = "128-token-tile tcgen05"
             # traffic: DRAM bytes read + written by one launch of the swap-AB

@@ -87,9 +87,11 @@ typedef enum {
  * tcgen05 tensor-core kernels above that. */
 typedef enum {
   NVFP4_ALGO_AUTO = 0,
-  NVFP4_ALGO_GEMV = 1,     /* CUDA-core split-row GEMV (any M, meant for M <= 16) */
-  NVFP4_ALGO_TC = 2,       /* tcgen05 block-scaled MMA, accumulators in TMEM      */
-  NVFP4_ALGO_TC_SWAPAB = 3 /* tcgen05 with weights as the MMA M operand (small M) */
+  NVFP4_ALGO_GEMV = 1,      /* CUDA-core split-row GEMV (any M, meant for M <= 16)  */
+  NVFP4_ALGO_TC = 2,        /* tcgen05 block-scaled MMA, accumulators in TMEM: CTA
+                               pairs issuing 2-SM MMAs (256 x 256 per pair)        */
+  NVFP4_ALGO_TC_SWAPAB = 3, /* tcgen05 with weights as the MMA M operand (small M)  */
+  NVFP4_ALGO_TC_1SM = 4     /* as NVFP4_ALGO_TC with one CTA per 128 x 256 tile    */
 } nvfp4_algo;
 
 /* Human-readable name of a status code (static storage). */
@@ -326,6 +328,9 @@ size_t bf16_fp4_gemm_prescaled_workspace_bytes(int64_t m, int64_t n, int64_t k, 
  * inter % 64 == 0, 16-byte aligned buffers.  The kernel's CTAs wait on each
  * other: it is launched with at most one CTA per SM, and a kernel that the
  * caller runs concurrently on another stream can delay it but not block it.
+ * Before launching, the call checks that the device can hold the whole grid
+ * at once (occupancy per SM x SM count) and returns
+ * NVFP4_ERR_UNSUPPORTED_SHAPE, launching nothing, when it cannot.
  * Tolerances as the separate calls. */
 nvfp4_status nvfp4_mlp_decode(const uint16_t *x, const float *x_global_scale,
                               const uint8_t *w_gate_up_int, const uint8_t *w_gate_up_int_sf,

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libnvfp4mlp.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_ARCH, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(6)
 SF_SWIZZLED_128x4, SF_LINEAR = 0, 1
-ALGO_AUTO, ALGO_GEMV, ALGO_TC, ALGO_TC_SWAPAB = 0, 1, 2, 3
+ALGO_AUTO, ALGO_GEMV, ALGO_TC, ALGO_TC_SWAPAB, ALGO_TC_1SM = 0, 1, 2, 3, 4
 
 _lib = None
 

@@ -42,7 +42,7 @@ nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVF
 // above, the CUDA-core GEMV where neither applies.
 nvfp4_algo pick_algo(TcMode mode, int64_t m, int64_t n, int64_t k) {
   if (m <= 64 && swapab_supported(mode, m, n, k)) return NVFP4_ALGO_TC_SWAPAB;
-  if (m > 16 && tc_supported(mode, false, m, n, k)) return NVFP4_ALGO_TC;
+  if (m > 16 && tc_supported(mode, m, n, k)) return NVFP4_ALGO_TC;
   return NVFP4_ALGO_GEMV;
 }
 
@@ -55,6 +55,8 @@ nvfp4_status check_gemm_shape(int64_t m, int64_t n, int64_t k) {
 }
 
 }  // namespace
+
+uint32_t nvfp4::wait_limit() { return g_wait_limit.load(); }
 
 extern "C" {
 
@@ -145,7 +147,7 @@ nvfp4_status gemm_impl(const uint8_t *a_fp4, const uint8_t *a_sf, const float *a
   if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
   if (!aligned16(a_fp4) || !aligned16(a_sf) || !aligned16(b_fp4) || !aligned16(b_sf) || !aligned16(d))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
+  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_1SM) return NVFP4_ERR_INVALID_ARG;
   if (nvfp4_status s = check_arch()) return s;
   if (m == 0) return NVFP4_OK;
   const cudaStream_t st = (cudaStream_t)stream;
@@ -159,8 +161,8 @@ nvfp4_status gemm_impl(const uint8_t *a_fp4, const uint8_t *a_sf, const float *a
                                    nullptr, m, n, k, workspace, ws_bytes, g_wait_limit.load(), st,
                                    a_row_scale));
   }
-  if (!tc_supported(TC_W4A4, false, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  return from_cuda(launch_tc(TC_W4A4, false, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
+  if (!tc_supported(TC_W4A4, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A4, algo == NVFP4_ALGO_TC, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr,
                              nullptr, m, n, k, g_wait_limit.load(), st, a_row_scale));
 }
 
@@ -176,7 +178,7 @@ nvfp4_status swiglu_impl(const uint8_t *a_fp4, const uint8_t *a_sf, const float 
   if (!aligned16(a_fp4) || !aligned16(a_sf) || !aligned16(w_int_fp4) || !aligned16(w_int_sf) ||
       !aligned16(out_fp4) || !aligned16(out_sf))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
+  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_1SM) return NVFP4_ERR_INVALID_ARG;
   if (nvfp4_status s = check_arch()) return s;
   if (m == 0) return NVFP4_OK;
   const cudaStream_t st = (cudaStream_t)stream;
@@ -190,8 +192,8 @@ nvfp4_status swiglu_impl(const uint8_t *a_fp4, const uint8_t *a_sf, const float 
                                    out_global_scale, nullptr, out_fp4, out_sf, m, n, k, workspace,
                                    ws_bytes, g_wait_limit.load(), st, a_row_scale));
   }
-  if (!tc_supported(TC_W4A4_SWIGLU, false, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  return from_cuda(launch_tc(TC_W4A4_SWIGLU, false, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
+  if (!tc_supported(TC_W4A4_SWIGLU, m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_tc(TC_W4A4_SWIGLU, algo == NVFP4_ALGO_TC, a_fp4, a_sf, w_int_fp4, w_int_sf, alpha,
                              out_global_scale, nullptr, out_fp4, out_sf, m, n, k, g_wait_limit.load(),
                              st, a_row_scale));
 }
@@ -282,12 +284,13 @@ nvfp4_status w4a16_impl(const uint16_t *a, const uint16_t *pre_scale, const uint
   if (!aligned16(a) || !aligned16(b_fp4) || !aligned16(b_sf) || !aligned16(d))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (pre_scale && !aligned16(pre_scale)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_SWAPAB) return NVFP4_ERR_INVALID_ARG;
+  if (algo < NVFP4_ALGO_AUTO || algo > NVFP4_ALGO_TC_1SM) return NVFP4_ERR_INVALID_ARG;
   if (nvfp4_status s = check_arch()) return s;
   if (m == 0) return NVFP4_OK;
   const cudaStream_t st = (cudaStream_t)stream;
   // The W4A16 tensor-core kernel always has the weight as the MMA's 128-row
-  // operand, so NVFP4_ALGO_TC and NVFP4_ALGO_TC_SWAPAB name the same kernel.
+  // operand and one CTA per weight tile, so NVFP4_ALGO_TC, NVFP4_ALGO_TC_SWAPAB
+  // and NVFP4_ALGO_TC_1SM name the same kernel.
   if (algo == NVFP4_ALGO_AUTO)
     algo = w4a16_tc_supported(m, n, k) ? NVFP4_ALGO_TC : NVFP4_ALGO_GEMV;
   if (algo == NVFP4_ALGO_GEMV)
@@ -382,7 +385,10 @@ nvfp4_status nvfp4_mlp_decode(const uint16_t *x, const float *x_global_scale, co
   q.workspace = workspace;
   q.ws_bytes = ws_bytes;
   q.wait_limit = g_wait_limit.load();
-  return from_cuda(launch_mlp_decode(q, (cudaStream_t)stream));
+  const cudaError_t e = launch_mlp_decode(q, (cudaStream_t)stream);
+  // the device cannot hold every CTA at once (they wait on each other)
+  if (e == cudaErrorCooperativeLaunchTooLarge) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(e);
 }
 
 size_t nvfp4_mlp_decode_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {

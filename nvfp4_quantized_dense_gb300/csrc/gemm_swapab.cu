@@ -408,13 +408,12 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
                       uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k, void *ws,
                       uint32_t wait_limit, cudaStream_t st, const float *rs) {
   using C = Cfg<NT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(swapab_kernel<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the shared-memory limit is a setting of each device's context
+  static PerDeviceOnce smem_attr;
+  if (cudaError_t e = smem_attr.run([] {
+        return cudaFuncSetAttribute(swapab_kernel<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+      }))
+    return e;
   CUtensorMap tm_w, tm_x;
   if (!make_byte_map(&tm_w, w, n, k / 2, 128, 128, true) || !make_byte_map(&tm_x, x, m, k / 2, 128, NT, true))
     return cudaErrorInvalidValue;

@@ -585,13 +585,12 @@ cudaError_t launch_nt(const Plan &pl, const uint16_t *x, const uint8_t *w, const
                       uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws, size_t ws_bytes, uint32_t wait_limit,
                       cudaStream_t st) {
   using C = Cfg<NT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(w4a16_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the shared-memory limit is a setting of each device's context
+  static PerDeviceOnce smem_attr;
+  if (cudaError_t e = smem_attr.run([] {
+        return cudaFuncSetAttribute(w4a16_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+      }))
+    return e;
   CUtensorMap tm_x, tm_w;
   // activations bf16 [m, k]: box 128 bytes (64 elements) x NT rows, 128-byte swizzle
   // weight codes [n, k/2]: box BK/2 bytes x 128 rows, no swizzle

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "nvfp4mlp.h"
 
 namespace nvfp4 {
@@ -26,6 +28,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// Runs `set()` (a per-context setting such as a kernel's dynamic shared-memory
+// limit) once on each device, with that device current; two host threads
+// racing on the first call may both run it, which is harmless for settings.
+struct PerDeviceOnce {
+  std::atomic<uint8_t> done[64] = {};
+  template <class F>
+  cudaError_t run(F set) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t e = set();
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
+  }
+};
+
+// Poll limit of the kernels' bounded waits set through nvfp4_set_wait_limit
+// (0 = the kernels' wall-clock default).
+uint32_t wait_limit();
 
 cudaError_t launch_quantize(const uint16_t *x, int64_t m, int64_t k, const float *gs,
                             uint8_t *out_fp4, uint8_t *out_sf, bool swizzled, cudaStream_t st);
@@ -56,14 +78,15 @@ cudaError_t launch_gemv(GemvMode mode, const void *a, const uint8_t *a_sf, const
                         cudaStream_t st, const float *a_row_scale = nullptr,
                         const uint16_t *pre_scale = nullptr);
 
-// tcgen05 tensor-core family.
+// tcgen05 tensor-core family.  launch_tc: prefill-sized M, 128 x 256 output
+// tiles; pair = 2-SM MMAs by CTA pairs (cta_group::2), else one CTA per tile.
 enum TcMode { TC_W4A4 = 0, TC_W4A4_SWIGLU = 1, TC_W4A16 = 2 };
-cudaError_t launch_tc(TcMode mode, bool swap_ab, const void *a, const uint8_t *a_sf,
+cudaError_t launch_tc(TcMode mode, bool pair, const void *a, const uint8_t *a_sf,
                       const uint8_t *b, const uint8_t *b_sf, const float *alpha,
                       const float *out_gs, uint16_t *d, uint8_t *out_fp4, uint8_t *out_sf,
                       int64_t m, int64_t n, int64_t k, uint32_t wait_limit, cudaStream_t st,
                       const float *a_row_scale = nullptr);
-bool tc_supported(TcMode mode, bool swap_ab, int64_t m, int64_t n, int64_t k);
+bool tc_supported(TcMode mode, int64_t m, int64_t n, int64_t k);
 
 // Device status word of the current device (set by kernels that give up a
 // bounded wait); reads it into *out and clears it.  Synchronous.

@@ -616,13 +616,20 @@ Plan make_plan(int64_t m, int64_t hid, int64_t inter) {
 template <int NT>
 cudaError_t launch_nt(const Plan &pl, const MlpDecodeParams &q, cudaStream_t st) {
   using C = Cfg<NT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mlp_decode_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the shared-memory limit is a setting of each device's context
+  static PerDeviceOnce smem_attr;
+  if (cudaError_t e = smem_attr.run([] {
+        return cudaFuncSetAttribute(mlp_decode_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
+      }))
+    return e;
+  // The CTAs wait on each other, so all of them must be resident at once:
+  // refuse up front (rather than time out) when the device cannot hold the
+  // grid, e.g. when other work or a partition leaves fewer SMs to this kernel.
+  int per_sm = 0;
+  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mlp_decode_kernel<NT>, kThreads,
+                                                                    C::SMEM_BYTES))
+    return e;
+  if ((int64_t)per_sm * num_sms() < pl.grid) return cudaErrorCooperativeLaunchTooLarge;
   const int64_t m = q.m, hid = q.hidden, inter = q.inter;
   CUtensorMap tm_wgu, tm_xq, tm_wdn, tm_h;
   // codes [rows, K/2] bytes; box 128 bytes of K x (128 weight rows | NT token rows), 128-byte swizzle

@@ -81,7 +81,7 @@ extern "C" nvfp4_status nvfp4_gemm_decode_noalloc(const uint8_t *a_fp4, const ui
     if (cudaMemsetAsync(scratch, 0, counter_bytes, st) != cudaSuccess) return NVFP4_ERR_CUDA;
   }
   return launch_swapab(TC_W4A4, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr, nullptr, m, n,
-                       k, scratch, kStaticScratchBytes, 0, st) == cudaSuccess
+                       k, scratch, kStaticScratchBytes, wait_limit(), st) == cudaSuccess
              ? NVFP4_OK
              : NVFP4_ERR_CUDA;
 }

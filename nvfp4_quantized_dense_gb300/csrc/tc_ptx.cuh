@@ -188,25 +188,39 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 2-D tiled TMA load delivered to the same shared-memory offset of every CTA
-// in cta_mask; each destination CTA's mbarrier at `bar`'s offset receives the
-// bytes that land in it.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *tm, uint64_t *bar, int32_t x,
-                                               int32_t y, uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
-      : "memory");
+// Address of the same shared-memory variable in CTA `rank` of the cluster
+// (a shared::cluster address).
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
 }
 
-// Contiguous bulk copy delivered to every CTA in cta_mask (see tma_load_2d_mc).
-__device__ __forceinline__ void bulk_load_mc(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                             uint16_t cta_mask, uint64_t policy) {
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address).
+// The release is at CTA scope: what the arrival publishes to the other CTA
+// is either TMEM traffic (ordered by the tcgen05 fences around the arrive and
+// the wait) or async-proxy copies (ordered by their own completion), so no
+// cluster-wide memory fence is needed -- and one per pipeline stage would
+// serialize the pipeline.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Store a word into another CTA's shared memory (relaxed, cluster scope).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// 2-D tiled TMA load into this CTA's shared memory whose completion is
+// signalled on an mbarrier of the CTA pair's other CTA (bar_cluster is a
+// shared::cluster address): the load form for the two halves of a 2-SM MMA
+// operand, both counted on the issuing CTA's barrier.
+__device__ __forceinline__ void tma_load_2d_to_pair_bar(void *dst, const CUtensorMap *tm, uint32_t bar_cluster,
+                                                        int32_t x, int32_t y, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4, %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
 
@@ -288,14 +302,45 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
                : "memory");
 }
 
-// As tc_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
-// cta_mask.
-__device__ __forceinline__ void tc_commit_mc(uint64_t *bar, uint16_t cta_mask) {
+// ------------------------------------------------- tcgen05, CTA pair (2-SM)
+// The same operations for an MMA shared by the two CTAs of a cluster pair
+// (cta_group::2): TMEM is allocated and freed collectively by one warp of
+// each CTA, the MMA is issued by one thread of the pair's even CTA and reads
+// A (one 128-row half per CTA) and B (one half of N per CTA) from both CTAs'
+// shared memory at the same offsets, and writes each CTA's 128 accumulator
+// lanes in that CTA's TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_nvfp4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n"
+      "}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
+}
+
+// Arrive on the mbarrier at shared::cluster address `bar_cluster` (this CTA's
+// or the pair's other CTA's) once every pair MMA issued so far by this thread
+// has completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar_cluster) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_cluster)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }

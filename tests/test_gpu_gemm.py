@@ -22,7 +22,7 @@ from tolerance import assert_gemm_close, check_requant
 
 pytestmark = pytest.mark.gpu
 
-GEMV, TC, TC_SWAPAB = 1, 2, 3
+GEMV, TC, TC_SWAPAB, TC_1SM = 1, 2, 3, 4
 
 
 def workspace(nv, m, n, k, algo):
@@ -74,10 +74,12 @@ def run_w4a16(nv, xbits, wdev, alpha, m, n, k, algo, split=False):
 # ---------------------------------------------------------------- W4A4 GEMM
 SMALL_SHAPES = [(4, 1024, 256), (1, 256, 512), (3, 96, 320), (16, 512, 256), (17, 128, 128),
                 (130, 160, 320)]
-# tensor-core tiles are 128 x 256 x 256: cover exact tiles, ragged M / N / K
-# tails, several k-blocks and more tiles than SMs (persistent loop)
+# tensor-core tiles are 128 x 256 x 256 per CTA (a CTA pair takes 256 x 256):
+# cover exact tiles, an odd number of 128-row tiles (the pair's second CTA
+# past M), ragged M / N / K tails, several k-blocks, a weight tile whose
+# second 128-row half is past N, and more tiles than SMs (persistent loop)
 TC_SHAPES = [(128, 256, 256), (1, 256, 256), (130, 160, 320), (256, 512, 1024), (200, 96, 576),
-             (384, 1024, 2048), (1000, 2304, 512), (4096, 4096, 256)]
+             (384, 1024, 2048), (1000, 2304, 512), (4096, 4096, 256), (640, 384, 1280), (257, 128, 64)]
 
 
 # swap-AB (weights as the MMA M operand): tokens padded to 16/32/64, split-K;
@@ -89,6 +91,7 @@ SWAP_SHAPES = [(1, 256, 256), (4, 1024, 256), (3, 96, 320), (16, 512, 2048), (17
 
 @pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SMALL_SHAPES] +
                          [(m, n, k, TC) for m, n, k in TC_SHAPES] +
+                         [(m, n, k, TC_1SM) for m, n, k in TC_SHAPES] +
                          [(m, n, k, TC_SWAPAB) for m, n, k in SWAP_SHAPES])
 def test_w4a4_small_shapes(lib, m, n, k, algo):
     ws = small_weights(n, k, 3)
@@ -121,7 +124,7 @@ def test_w4a4_decode_full_size_sampled(lib, m, which, algo):
     print(f"decode {which} m={m} algo={algo}: rel err {err:.2e}")
 
 
-@pytest.mark.parametrize("algo", [GEMV, TC, TC_SWAPAB])
+@pytest.mark.parametrize("algo", [GEMV, TC, TC_SWAPAB, TC_1SM])
 def test_w4a4_is_deterministic(lib, algo):
     m, n, k = 16, 1024, 4096
     ws = small_weights(n, k, 4)
@@ -177,7 +180,8 @@ def _swiglu_case(nv, wid, m, n, k, ws, algo, sampled_blocks=None, sampled_tokens
 
 
 SWIGLU_GEMV = [(4, 1024, 256), (1, 256, 512), (3, 128, 320), (16, 384, 256), (130, 256, 128)]
-SWIGLU_TC = [(128, 256, 256), (4, 1024, 256), (130, 384, 320), (256, 1024, 1024), (700, 2304, 512)]
+SWIGLU_TC = [(128, 256, 256), (4, 1024, 256), (130, 384, 320), (256, 1024, 1024), (700, 2304, 512),
+             (384, 640, 1280)]
 
 
 SWIGLU_SWAP = [(1, 256, 256), (4, 1024, 256), (3, 128, 320), (16, 384, 4096), (40, 256, 512),
@@ -186,6 +190,7 @@ SWIGLU_SWAP = [(1, 256, 256), (4, 1024, 256), (3, 128, 320), (16, 384, 4096), (4
 
 @pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SWIGLU_GEMV] +
                          [(m, n, k, TC) for m, n, k in SWIGLU_TC] +
+                         [(m, n, k, TC_1SM) for m, n, k in SWIGLU_TC] +
                          [(m, n, k, TC_SWAPAB) for m, n, k in SWIGLU_SWAP])
 def test_swiglu_small_shapes(lib, m, n, k, algo):
     _swiglu_case(lib, 0, m, n, k, small_weights(n, k, 6), algo)
@@ -219,13 +224,14 @@ def test_w4a4_decode_full_size_sampled_tc(lib, m, which):
     test_w4a4_decode_full_size_sampled(lib, m, which, TC)
 
 
-@pytest.mark.parametrize("m", [1024, 4096, 8192])
-def test_swiglu_prefill_full_size_sampled(lib, m):
-    """Prefill H7168/I18432, M up to 8192, the launch the prefill chain uses:
-    256 stratified tokens x 144 stratified 16-feature blocks (one in each
-    128-feature span of the 256-row weight tiles)."""
+@pytest.mark.parametrize("m,algo", [(1024, 0), (4096, 0), (8192, 0), (1024, TC_1SM)])
+def test_swiglu_prefill_full_size_sampled(lib, m, algo):
+    """Prefill H7168/I18432, M up to 8192, the launch the prefill chain uses
+    (AUTO: CTA pairs with 2-SM MMAs): 256 stratified tokens x 144 stratified
+    16-feature blocks (one in each 128-feature span of the 256-row weight
+    tiles)."""
     ws = weights(3, "gate_up")
-    _swiglu_case(lib, 3, m, ws.n, ws.k, ws, 0, sampled_blocks=144, sampled_tokens=256)
+    _swiglu_case(lib, 3, m, ws.n, ws.k, ws, algo, sampled_blocks=144, sampled_tokens=256)
 
 
 @pytest.mark.parametrize("m", [1024, 8192])
@@ -249,7 +255,8 @@ def quantize_rows(x, gs):
     return quantize_big(x, gs)
 
 
-def test_tc_bounded_wait_gives_up_cleanly(lib):
+@pytest.mark.parametrize("algo", [TC, TC_1SM])
+def test_tc_bounded_wait_gives_up_cleanly(lib, algo):
     """A wait limit of one poll makes the pipeline waits run out: the kernel
     must record NVFP4_ERR_DEVICE_TIMEOUT and return, leaving the context
     usable for the next (normal) call."""
@@ -260,12 +267,12 @@ def test_tc_bounded_wait_gives_up_cleanly(lib):
     assert lib.nvfp4_get_device_status() == 0
     lib.nvfp4_set_wait_limit(1)
     try:
-        run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, TC)
+        run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, algo)
     finally:
         lib.nvfp4_set_wait_limit(0)
     assert lib.nvfp4_get_device_status() == lib.ERR_DEVICE_TIMEOUT
     assert lib.nvfp4_get_device_status() == 0          # read clears it
-    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, TC)
+    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, n, k, algo)
     assert_gemm_close(got, oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha))
 
 

@@ -47,10 +47,41 @@ def test_noalloc_matches_workspace_entry_point(lib, m, n, k):
 
 
 def test_noalloc_rejects_too_much_scratch(lib):
-    """A split plan larger than the fixed array is refused before launch."""
-    m, n, k = 64, 65536, 65536
+    """A split plan larger than the fixed array is refused before launch.
+    The operands are real device buffers of the stated shape, so a launch
+    that should not happen would compute on valid memory rather than fault."""
+    m, n, k = 64, 256, 65536
     need = lib.nvfp4_workspace_bytes(m, n, k, TC_SWAPAB)
     assert need > (8 << 20)
+    a = torch.zeros((m, k // 2), dtype=torch.uint8, device="cuda")
+    a_sf = torch.zeros((lib.nvfp4_sf_bytes(m, k),), dtype=torch.uint8, device="cuda")
+    w = torch.zeros((n, k // 2), dtype=torch.uint8, device="cuda")
+    w_sf = torch.zeros((lib.nvfp4_sf_bytes(n, k),), dtype=torch.uint8, device="cuda")
+    out = torch.zeros((m, n), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(lib.Nvfp4Error) as e:
-        lib.nvfp4_gemm_decode_noalloc(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, m, n, k)
+        lib.nvfp4_gemm_decode_noalloc(a, a_sf, w, w_sf, scalar(1.0), out, m, n, k)
     assert e.value.status == lib.ERR_UNSUPPORTED_SHAPE
+
+
+def test_noalloc_bounded_wait_gives_up_cleanly(lib):
+    """The wait limit set through nvfp4_set_wait_limit applies to this entry
+    point too: with one poll the kernel gives up, reports the timeout, and the
+    next normal call (which clears the array's counters again) is right."""
+    m, n, k = 16, 2048, 8192
+    ws = small_weights(n, k, 13)
+    w, w_sf = ws.device_prepared(lib)
+    _, _, gs_x, xq, xs = quantized_activation(0, m, k)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    a, a_sf = dev(xq), dev(oracle.sf_swizzle_128x4(xs))
+    out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    assert lib.nvfp4_get_device_status() == 0
+    lib.nvfp4_set_wait_limit(1)
+    try:
+        lib.nvfp4_gemm_decode_noalloc(a, a_sf, w, w_sf, scalar(alpha), out, m, n, k)
+    finally:
+        lib.nvfp4_set_wait_limit(0)
+    assert lib.nvfp4_get_device_status() == lib.ERR_DEVICE_TIMEOUT
+    lib.nvfp4_gemm_decode_noalloc(a, a_sf, w, w_sf, scalar(alpha), out, m, n, k)
+    torch.cuda.synchronize()
+    assert lib.nvfp4_get_device_status() == 0
+    assert_gemm_close(bf16_host(out), oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha))
