@@ -1,22 +1,32 @@
 #!/usr/bin/env python
 """Benchmark of the NVFP4 dense-MLP hot path on one GB300 (or N replicas).
 
-Workload: the decode dense MLP, W4A4 NVFP4, hidden 5120, intermediate 17408
-(gate_up 34816 x 5120, down 5120 x 17408).  One step runs the MLP forward
-once for each decode batch M in {1, 2, 4, 8, 16} (31 tokens per step) as
-three launches each (the default `--decode-path chain`):
+One step runs the MLP forward once for every batch size of the four
+synthetic workloads, which together span M = 1..8192:
+  decode   W4A4 H5120 / I17408,  M in 1, 2, 4, 8, 16
+  decode   W4A4 H7168 / I18432,  M in 1, 8, 32, 64 (x with 1 % outliers x20)
+  prefill  W4A4 H7168 / I18432,  M in 1024, 4096, 8192
+  W4A16    bf16 x NVFP4, H5120 / I17408, M in 1, 16, 128, 1024
+(14617 tokens per step).  A W4A4 forward is three launches:
     nvfp4_quantize(x) -> nvfp4_gemm_swiglu_quant(gate_up; SwiGLU on the fp32
     accumulators + NVFP4 requantize in the epilogue) -> nvfp4_gemm(down)
-both GEMMs on the weight-streaming swap-AB tensor-core kernel.
-`--decode-path fused` runs each MLP as one nvfp4_mlp_decode launch instead
-(SwiGLU on the bf16-rounded gate_up, as silu_mul_nvfp4_quantize).
-Weights are synthetic N(0, 0.02), quantized to NVFP4 on the device by the
-library before timing; x ~ N(0, 1) bf16.  Each step's launches are captured
-in a CUDA graph; four weight copies (602 MB, > 4x the 126 MB L2) rotate so the
-weight stream comes from HBM every step.
+with the library choosing the kernel by M (weight-streaming tensor-core
+kernels up to 64 tokens, 2-SM CTA-pair tensor-core kernels above); a W4A16
+forward is bf16_fp4_gemm(gate_up) -> silu_mul_bf16 -> bf16_fp4_gemm(down).
+Each workload's forwards are one CUDA graph; weight copies rotate so that the
+weight stream comes from HBM every step (more copies than fit in L2).
 
-Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on
-the host cores instead (the slow baseline arm).
+Weights: synthetic N(0, 0.02) fp32 draws of the shared input generator
+(`synth`), rounded to bf16 on the device and quantized to NVFP4 by the
+library (timing does not depend on the values); x ~ N(0, 1) bf16.
+
+Prints one JSON line (rank 0): the whole-step throughput, a roofline record
+for the step's dominant kernel, and one sub-record per workload (median and
+p10/p90 over >= 100 graph replays, per-M chain and GEMM times with their
+roofline fractions), the elementwise kernels against HBM, an end-to-end
+number through the C ABI with host copies, and the CPU oracle on a bounded
+sample.  `--impl reference` times the CPU oracle instead (the slow baseline
+arm).
 """
 import argparse
 import json
@@ -30,29 +40,36 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-H, I = 5120, 17408
-MS = (1, 2, 4, 8, 16)
-TOKENS_PER_STEP = sum(MS)
-NCOPY = 4
-METRIC = "NVFP4 MLP tokens/s (decode H5120 I17408, M in 1,2,4,8,16)"
-WORKLOAD = "decode dense MLP W4A4 NVFP4, hidden 5120, intermediate 17408, M sweep 1/2/4/8/16"
+# (key, synth workload id, title)
+WORKLOADS = [
+    ("decode_h5120", 1, "decode dense MLP W4A4 NVFP4, hidden 5120, intermediate 17408, M 1/2/4/8/16"),
+    ("decode_h7168", 2, "decode dense MLP W4A4 NVFP4, DeepSeek-V3-shaped hidden 7168, intermediate 18432, "
+                        "M 1/8/32/64, x with 1% outliers x20"),
+    ("prefill_h7168", 3, "prefill dense MLP W4A4 NVFP4, hidden 7168, intermediate 18432, M 1024/4096/8192"),
+    ("w4a16_h5120", 4, "W4A16 dense MLP (bf16 x NVFP4 weights), hidden 5120, intermediate 17408, M 1/16/128/1024"),
+]
+METRIC = "NVFP4 MLP tokens/s (M=1..8192 over the decode, prefill and W4A16 workloads)"
+NCOPY = 4          # rotating weight copies per weight family (> L2 in total)
+REPLAYS = 100      # per-workload graph replays for median / p10 / p90
+REPS = 8           # back-to-back launches per per-M timing graph
+
+# CPU oracle sample: one forward per workload at these M on 1/SLICE of the
+# intermediate size (the oracle's cost is linear in I)
+SLICE = 8
+ORACLE_M = {1: 16, 2: 64, 3: 256, 4: 128}
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", default="decode", choices=["decode", "prefill", "w4a16"],
-                   help="decode (default line) | prefill H7168/I18432 | w4a16 H5120/I17408")
-    p.add_argument("--m", type=int, default=None, help="single M (decode: instead of the 1..16 sweep)")
+    p.add_argument("--only", default=None, help="comma-separated workload keys (default: all four)")
     p.add_argument("--algo", default="auto", choices=["auto", "gemv", "tc", "tc1sm", "swapab"],
-                   help="GEMM kernel family of the chain's GEMMs (auto: the library's choice by M; "
-                        "tc: CTA pairs with 2-SM MMAs; tc1sm: one CTA per tile)")
-    p.add_argument("--decode-path", default="chain", choices=["fused", "chain"],
-                   help="decode MLP as three launches (default) or one nvfp4_mlp_decode launch")
+                   help="W4A4 GEMM kernel family (auto: the library's choice by M; tc: CTA pairs with 2-SM "
+                        "MMAs; tc1sm: one CTA per tile)")
     return p.parse_args()
 
 
@@ -76,41 +93,67 @@ def dist_setup():
     return world, rank, local
 
 
+def selected(args):
+    keys = args.only.split(",") if args.only else [w[0] for w in WORKLOADS]
+    out = [w for w in WORKLOADS if w[0] in keys]
+    if not out:
+        raise SystemExit(f"--only: no workload among {keys}")
+    return out
+
+
 # --------------------------------------------------------------- oracle leg
-# The CPU oracle's cost is linear in the intermediate size I (both GEMMs) and
-# dominated by them, so a bounded sample runs the decode MLP on a slice of I:
-# the first I/SLICE gate rows and as many up rows, and the matching I/SLICE
-# input columns of down_proj (same H, same weight and activation recipe).
-# Its tokens/s is scaled back to the whole MLP: tokens * (1/SLICE) / seconds.
-SLICE = 8
-
-
 class OracleSampler:
-    def __init__(self):
+    """The CPU oracle on a bounded sample of the benchmark's workloads: one
+    MLP forward per workload at ORACLE_M[wid] tokens on the first I/SLICE
+    intermediate features (gate and up rows, and the matching down_proj
+    input columns), same H and value recipe.  Token equivalents = M / SLICE."""
+
+    def __init__(self, wids):
         import numpy as np
         import oracle
         import synth
         self.np, self.oracle, self.synth = np, oracle, synth
-        self.isl = I // SLICE
-        wgu = synth.weight(1, "gate_up", rows=2 * self.isl)     # [gate slice; up slice]
-        wdn = synth.weight(1, "down", cols=self.isl)
-        self.gs_gu = oracle.global_scale(np.abs(wgu).max())
-        self.gs_dn = oracle.global_scale(np.abs(wdn).max())
-        self.gu = oracle.quantize_nvfp4(wgu, self.gs_gu)
-        self.dn = oracle.quantize_nvfp4(wdn, self.gs_dn)
+        self.w = {}
+        for fam in sorted({synth.WEIGHT_SOURCE.get(w, w) for w in wids}):
+            isl = synth.WORKLOADS[fam].inter // SLICE
+            wgu = synth.weight(fam, "gate_up", rows=2 * isl)       # [gate slice; up slice]
+            wdn = synth.weight(fam, "down", cols=isl)
+            gs_gu = oracle.global_scale(np.abs(wgu).max())
+            gs_dn = oracle.global_scale(np.abs(wdn).max())
+            self.w[fam] = (gs_gu, oracle.quantize_nvfp4(wgu, gs_gu), gs_dn, oracle.quantize_nvfp4(wdn, gs_dn))
+        self.wids = list(wids)
 
-    def forward(self, m):
-        """One timed oracle MLP forward (unfused chain) at M = m on the slice;
-        returns (whole-MLP token equivalents, seconds)."""
-        np, oracle = self.np, self.oracle
-        _, x = self.synth.activations(1, m)
-        gs_x = oracle.global_scale(np.abs(x).max())
-        a_gu = np.float32(1.0) / (gs_x * self.gs_gu)
-        gs_h = np.float32(448.0 * 6.0 / 8.0)
-        a_dn = np.float32(1.0) / (gs_h * self.gs_dn)
+    def forward(self, wid):
+        """One timed oracle forward of workload `wid`; returns (token
+        equivalents, seconds)."""
+        np, oracle, synth = self.np, self.oracle, self.synth
+        m = ORACLE_M[wid]
+        gs_gu, gu, gs_dn, dn = self.w[synth.WEIGHT_SOURCE.get(wid, wid)]
+        _, x = synth.activations(wid, m)
         t0 = time.perf_counter()
-        oracle.mlp_w4a4_unfused(x, gs_x, self.gu, a_gu, gs_h, self.dn, a_dn)
+        if synth.WORKLOADS[wid].mode == "w4a16":
+            oracle.mlp_w4a16(x, gu, np.float32(1.0) / gs_gu, dn, np.float32(1.0) / gs_dn)
+        else:
+            gs_x = oracle.global_scale(np.abs(x).max())
+            a_gu = np.float32(1.0) / (gs_x * gs_gu)
+            gs_h = np.float32(448.0 * 6.0 / 8.0)
+            a_dn = np.float32(1.0) / (gs_h * gs_dn)
+            fwd = oracle.mlp_w4a4_fused if synth.WORKLOADS[wid].fused else oracle.mlp_w4a4_unfused
+            fwd(x, gs_x, gu, a_gu, gs_h, dn, a_dn)
         return m / SLICE, time.perf_counter() - t0
+
+    def sample(self):
+        tokens, secs = 0.0, 0.0
+        for wid in self.wids:
+            t, s = self.forward(wid)
+            tokens += t
+            secs += s
+        return tokens, secs
+
+    def describe(self):
+        ms = ", ".join(f"M={ORACLE_M[w]} ({self.synth.WORKLOADS[w].name})" for w in self.wids)
+        return (f"CPU oracle (NumPy float64), one MLP forward per workload on the first 1/{SLICE} of the "
+                f"intermediate features: {ms}; tokens counted as M/{SLICE}")
 
     @staticmethod
     def threads():
@@ -124,40 +167,28 @@ class OracleSampler:
         return n
 
 
-def oracle_sample(ms):
-    """The CPU baseline beside a GPU run: one oracle forward per M in `ms`.
-    Returns (token equivalents, seconds, threads)."""
-    smp = OracleSampler()
-    tokens, secs = 0.0, 0.0
-    for m in ms:
-        t, s = smp.forward(m)
-        tokens += t
-        secs += s
-    return tokens, secs, smp.threads()
-
-
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    smp = OracleSampler()
+    wls = selected(args)
+    smp = OracleSampler([w[1] for w in wls])
     for _ in range(args.warmup):
-        smp.forward(16)
+        smp.sample()
     tokens, secs = 0.0, 0.0
     for _ in range(args.steps):
-        t, s = smp.forward(16)
+        t, s = smp.sample()
         tokens += t
         secs += s
     value = tokens / secs
-    sample = (f"CPU oracle (NumPy float64), per step one decode MLP forward at M=16 on a 1/{SLICE} slice of "
-              f"the intermediate size (I {I // SLICE} of {I}, H {H}); tokens/s scaled to the whole MLP")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "step": f"M=16 forward on 1/{SLICE} of I (bounded sample)"},
+        "config": {"workload": "; ".join(w[2] for w in wls),
+                   "step": "bounded sample: " + smp.describe()},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": smp.threads(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": smp.describe()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -197,8 +228,15 @@ class Clocks:
         self.out.close()
         rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
         os.unlink(self.path)
-        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if len(r) >= 9 and num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if len(r) >= 9 and num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if len(r) >= 9 and num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         for r in rows:
@@ -207,9 +245,11 @@ class Clocks:
             for nm, v in zip(names, r[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(nm)
+        loaded = [s for s, p in zip(sm, pw) if p is not None and p > 300.0] if len(pw) == len(sm) else []
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(rows)}
+                "sm_mhz_under_load": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
 
 
 def peaks():
@@ -219,11 +259,18 @@ def peaks():
         return None
 
 
+def pct(vals, q):
+    s = sorted(vals)
+    i = min(len(s) - 1, max(0, int(round(q * (len(s) - 1)))))
+    return s[i]
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
 
     import nvfp4_quantized_dense_gb300 as nv
+    import synth
 
     nv.load()
     torch.cuda.set_device(local)
@@ -232,214 +279,229 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1234 + rank)
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    bf16_peak = pk["bf16_tflops"] if pk else 1900.0
+    fp4_peak = bf16_peak * 6.0        # dense FP4 : dense BF16 = 13.5 : 2.25 (nominal)
+    peak_src = "measured" if pk else "fallback"
+    algo = {"auto": nv.ALGO_AUTO, "gemv": nv.ALGO_GEMV, "tc": nv.ALGO_TC, "tc1sm": nv.ALGO_TC_1SM,
+            "swapab": nv.ALGO_TC_SWAPAB}[args.algo]
+    wls = selected(args)
 
     def scalar(v):
         return torch.tensor([np.float32(v)], dtype=torch.float32, device=dev)
 
+    def gscale_np(a):
+        return np.float32(np.float32(448.0 * 6.0) / np.float32(np.abs(a).max()))
+
     def gscale(t):
         return np.float32(np.float32(448.0 * 6.0) / np.float32(t.abs().max().float().item()))
 
-    def make_weight(rows, cols, interleave=False):
-        w = (torch.randn(rows, cols, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
-        gs = gscale(w)
+    # ---------------------------------------------------------------- weights
+    def make_weight(fam, which, layout):
+        """(codes, swizzled scales, gs) of one synth weight on the device;
+        layout 'interleaved' (the fused gate_up kernel's) or 'plain'."""
+        w32 = synth.weight(fam, which)
+        gs = gscale_np(w32)
+        rows, cols = w32.shape
+        wb = torch.from_numpy(w32).to(dev).to(torch.bfloat16)
+        del w32
         q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
         s_lin = torch.empty((rows * cols // 16,), dtype=torch.uint8, device=dev)
-        nv.nvfp4_quantize(w, rows, cols, scalar(gs), q, s_lin, nv.SF_LINEAR)
+        nv.nvfp4_quantize(wb, rows, cols, scalar(gs), q, s_lin, nv.SF_LINEAR)
+        del wb
         s = torch.empty((nv.nvfp4_sf_bytes(rows, cols),), dtype=torch.uint8, device=dev)
-        if interleave:
+        if layout == "interleaved":
             qi = torch.empty_like(q)
             nv.nvfp4_prepare_gate_up_interleaved(q, s_lin, rows, cols, qi, s)
             q = qi
         else:
             nv.nvfp4_prepare_weights(q, s_lin, rows, cols, q, s)
-        del w, s_lin
         return q, s, gs
 
-    pk = peaks()
-    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
-    bf16_peak = pk["bf16_tflops"] if pk else 1900.0
-    fp4_peak = bf16_peak * 6.0        # dense FP4 : dense BF16 = 13.5 : 2.25 (nominal)
+    need = {}     # family -> set of (which, layout)
+    for _, wid, _ in wls:
+        fam = synth.WEIGHT_SOURCE.get(wid, wid)
+        w = synth.WORKLOADS[wid]
+        st = need.setdefault(fam, set())
+        st.add(("down", "plain"))
+        if w.mode == "w4a16":
+            st.add(("gate_up", "plain"))
+        else:
+            st.add(("gate_up", "interleaved"))
+            if wid == 1:
+                st.add(("gate_up", "plain"))      # the unfused chain (silu_mul_nvfp4_quantize)
+    weights = {}     # (fam, which, layout) -> list of NCOPY (q, s, gs)
+    for fam, st in need.items():
+        for which, layout in sorted(st):
+            base = make_weight(fam, which, layout)
+            weights[(fam, which, layout)] = [base] + [(base[0].clone(), base[1].clone(), base[2])
+                                                      for _ in range(NCOPY - 1)]
+    torch.cuda.synchronize()
+    weight_bytes = sum(c[0].numel() + c[1].numel() for v in weights.values() for c in v)
 
-    wl = args.workload
-    if wl == "decode":
-        hid, inter, ms, ncopy = H, I, ((args.m,) if args.m else MS), NCOPY
-        metric, workload = METRIC, WORKLOAD
-        if args.m:
-            metric = f"NVFP4 MLP tokens/s (decode H5120 I17408, M={args.m})"
-            workload = f"decode dense MLP W4A4 NVFP4, hidden 5120, intermediate 17408, M={args.m}"
-    elif wl == "prefill":
-        hid, inter = 7168, 18432
-        ms = (args.m or 8192,)
-        ncopy = 2
-        metric = f"NVFP4 MLP tokens/s (prefill H7168 I18432, M={ms[0]})"
-        workload = f"prefill dense MLP W4A4 NVFP4 (fused gate_up+SwiGLU+requant), hidden 7168, intermediate 18432, M={ms[0]}"
-    else:
-        hid, inter = H, I
-        ms = (args.m,) if args.m else (1, 16, 128, 1024)
-        ncopy = NCOPY
-        metric = f"W4A16 MLP tokens/s (H5120 I17408, M in {','.join(map(str, ms))})"
-        workload = f"W4A16 dense MLP (bf16 x NVFP4), hidden 5120, intermediate 17408, M in {ms}"
-    tokens_per_step = sum(ms)
-    mmax = max(ms)
-    fused_decode = wl == "decode" and args.decode_path == "fused"
-    algo = {"auto": nv.ALGO_AUTO, "gemv": nv.ALGO_GEMV, "tc": nv.ALGO_TC, "tc1sm": nv.ALGO_TC_1SM,
-            "swapab": nv.ALGO_TC_SWAPAB}[args.algo]
-    if fused_decode and algo != nv.ALGO_AUTO:
-        raise SystemExit("--algo applies to the chain of separate GEMM launches, not --decode-path fused")
-    interleaved = wl in ("prefill", "decode")
+    # ------------------------------------------------------------ workloads
+    SH = [None]       # the timing stream's handle (an int: no torch stream lookup per call)
 
-    w_gu0 = make_weight(2 * inter, hid, interleave=interleaved)
-    w_dn0 = make_weight(hid, inter)
-    copies = [(w_gu0, w_dn0)]
-    for _ in range(ncopy - 1):
-        copies.append(((w_gu0[0].clone(), w_gu0[1].clone(), w_gu0[2]),
-                       (w_dn0[0].clone(), w_dn0[1].clone(), w_dn0[2])))
-    weight_bytes = sum(t.numel() for t in (w_gu0[0], w_gu0[1], w_dn0[0], w_dn0[1]))
+    class W:
+        pass
 
-    x = torch.randn(mmax, hid, generator=gen, device=dev).to(torch.bfloat16)
-    gs_x = gscale(x)
-    # calibrate the static down_proj input scale once from one gate_up pass
-    mc = min(mmax, 1024)
-    gu_tmp = torch.empty((mc, 2 * inter), dtype=torch.bfloat16, device=dev)
-    if wl == "w4a16":
-        nv.bf16_fp4_gemm(x[:mc].contiguous(), w_gu0[0], w_gu0[1], scalar(np.float32(1.0) / w_gu0[2]),
-                         gu_tmp, mc, 2 * inter, hid)
-        gs_h, a_gu = None, scalar(np.float32(1.0) / w_gu0[2])
-        a_dn = scalar(np.float32(1.0) / w_dn0[2])
-    else:
-        xq = torch.empty((mc, hid // 2), dtype=torch.uint8, device=dev)
-        xs = torch.empty((nv.nvfp4_sf_bytes(mc, hid),), dtype=torch.uint8, device=dev)
-        nv.nvfp4_quantize(x[:mc].contiguous(), mc, hid, scalar(gs_x), xq, xs)
-        a_gu = scalar(np.float32(1.0) / (gs_x * w_gu0[2]))
-        nv.nvfp4_gemm(xq, xs, w_gu0[0], w_gu0[1], a_gu, gu_tmp, mc, 2 * inter, hid)
-        gf = gu_tmp.float()
-        if interleaved:       # interleaved rows: blocks of 128 = [64 up ; 64 gate]
-            gf = gf.view(mc, 2 * inter // 128, 2, 64)
+    items = []
+    ws_bytes = 16
+    for key, wid, title in wls:
+        spec = synth.WORKLOADS[wid]
+        fam = synth.WEIGHT_SOURCE.get(wid, wid)
+        it = W()
+        it.key, it.wid, it.title, it.spec = key, wid, title, spec
+        it.hid, it.inter, it.ms = spec.hidden, spec.inter, tuple(spec.ms)
+        it.w4a16 = spec.mode == "w4a16"
+        it.gu = weights[(fam, "gate_up", "plain" if it.w4a16 else "interleaved")]
+        it.gu_plain = weights.get((fam, "gate_up", "plain")) if wid == 1 else None
+        it.dn = weights[(fam, "down", "plain")]
+        mmax = max(it.ms)
+        xbits, _ = synth.activations(wid, mmax)
+        it.x = torch.from_numpy(xbits.view(np.int16)).to(dev).view(torch.bfloat16)
+        it.gs_x = gscale(it.x)
+        hid, inter = it.hid, it.inter
+        # calibrate the static down_proj input scale once from one gate_up pass
+        mc = min(mmax, 1024)
+        gu_tmp = torch.empty((mc, 2 * inter), dtype=torch.bfloat16, device=dev)
+        gq, gsf, ggs = it.gu[0]
+        if it.w4a16:
+            it.a_gu = scalar(np.float32(1.0) / ggs)
+            it.a_dn = scalar(np.float32(1.0) / it.dn[0][2])
+            it.gs_h = None
+        else:
+            xq = torch.empty((mc, hid // 2), dtype=torch.uint8, device=dev)
+            xs = torch.empty((nv.nvfp4_sf_bytes(mc, hid),), dtype=torch.uint8, device=dev)
+            nv.nvfp4_quantize(it.x[:mc].contiguous(), mc, hid, scalar(it.gs_x), xq, xs)
+            it.a_gu = scalar(np.float32(1.0) / (it.gs_x * ggs))
+            nv.nvfp4_gemm(xq, xs, gq, gsf, it.a_gu, gu_tmp, mc, 2 * inter, hid)
+            gf = gu_tmp.float().view(mc, 2 * inter // 128, 2, 64)      # interleaved: [64 up ; 64 gate]
             u, g = gf[:, :, 0, :].reshape(mc, inter), gf[:, :, 1, :].reshape(mc, inter)
-        else:
-            g, u = gf[:, :inter], gf[:, inter:]
-        gs_h = gscale(g * torch.sigmoid(g) * u)
-        a_dn = scalar(np.float32(1.0) / (gs_h * w_dn0[2]))
-    gs_x_d = scalar(gs_x)
-    gs_h_d = scalar(gs_h) if gs_h is not None else None
-    del gu_tmp
+            gs_h = gscale(g * torch.sigmoid(g) * u)
+            it.gs_h = scalar(gs_h)
+            it.a_dn = scalar(np.float32(1.0) / (gs_h * it.dn[0][2]))
+            if it.gu_plain is not None:
+                it.a_gu_plain = scalar(np.float32(1.0) / (it.gs_x * it.gu_plain[0][2]))
+        it.gs_x_d = scalar(it.gs_x)
+        del gu_tmp
+        it.out = torch.empty((sum(it.ms), hid), dtype=torch.bfloat16, device=dev)
+        it.bufs = {}
+        r0 = 0
+        for m in it.ms:
+            bf16_mid = it.w4a16 or it.gu_plain is not None    # a bf16 gate_up result is materialized
+            it.bufs[m] = dict(
+                x=it.x[:m], out=it.out[r0:r0 + m],
+                xq=torch.empty((m, hid // 2), dtype=torch.uint8, device=dev),
+                xs=torch.empty((nv.nvfp4_sf_bytes(m, hid),), dtype=torch.uint8, device=dev),
+                gu=torch.empty((m, 2 * inter), dtype=torch.bfloat16, device=dev) if bf16_mid else None,
+                h16=torch.empty((m, inter), dtype=torch.bfloat16, device=dev) if it.w4a16 else None,
+                hq=torch.empty((m, inter // 2), dtype=torch.uint8, device=dev),
+                hs=torch.empty((nv.nvfp4_sf_bytes(m, inter),), dtype=torch.uint8, device=dev))
+            r0 += m
+            if it.w4a16:
+                ws_bytes = max(ws_bytes, nv.bf16_fp4_gemm_workspace_bytes(m, 2 * inter, hid, algo),
+                               nv.bf16_fp4_gemm_workspace_bytes(m, hid, inter, algo))
+            else:
+                ws_bytes = max(ws_bytes, nv.nvfp4_workspace_bytes(m, 2 * inter, hid, algo),
+                               nv.nvfp4_workspace_bytes(m, hid, inter, algo))
+        items.append(it)
+    # one zero-filled scratch (split-K partials + arrival counters) shared by
+    # every GEMM of the step: they run in stream order
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
 
-    # every M's output is a row range of one buffer (read back in one copy)
-    out_all = torch.empty((sum(ms), hid), dtype=torch.bfloat16, device=dev)
-    out_rows = {}
-    r0 = 0
-    for m in ms:
-        out_rows[m] = out_all[r0:r0 + m]
-        r0 += m
-    bufs = {}
-    for m in ms:
-        bufs[m] = dict(
-            xq=torch.empty((m, hid // 2), dtype=torch.uint8, device=dev),
-            xs=torch.empty((nv.nvfp4_sf_bytes(m, hid),), dtype=torch.uint8, device=dev),
-            gu=torch.empty((m, 2 * inter), dtype=torch.bfloat16, device=dev),
-            h16=torch.empty((m, inter), dtype=torch.bfloat16, device=dev),
-            hq=torch.empty((m, inter // 2), dtype=torch.uint8, device=dev),
-            hs=torch.empty((nv.nvfp4_sf_bytes(m, inter),), dtype=torch.uint8, device=dev),
-            out=out_rows[m])
-    # every M's input is the first M rows of one x buffer (written in one copy)
-    x_in = {m: x[:m] for m in ms}
-    # one zero-filled scratch buffer (split-K partials + arrival counters),
-    # sized for the largest GEMM of the chain and shared by its sequential calls
-    ws_bytes = max([nv.nvfp4_workspace_bytes(m, 2 * inter, hid, algo) for m in ms] +
-                   [nv.nvfp4_workspace_bytes(m, hid, inter, algo) for m in ms] + [0])
-    if fused_decode:
-        ws_bytes = max(nv.nvfp4_mlp_decode_workspace_bytes(m, hid, inter) for m in ms)
-    if wl == "w4a16":
-        ws_bytes = max([nv.bf16_fp4_gemm_workspace_bytes(m, 2 * inter, hid, algo) for m in ms] +
-                       [nv.bf16_fp4_gemm_workspace_bytes(m, hid, inter, algo) for m in ms] + [0])
-    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-
-    # the stream handle as an int: the bindings then skip looking up torch's
-    # current stream (~3 us of host time per call)
-    SH = [None]
-
-    def dominant(m, wc):
-        """The step's dominant launch: the gate_up GEMM (the whole MLP when fused)."""
-        b = bufs[m]
-        (gq, gsf, _), (dq, dsf, _) = wc
-        if wl == "w4a16":
-            nv.bf16_fp4_gemm_ex(x_in[m], gq, gsf, a_gu, b["gu"], m, 2 * inter, hid, ws, ws_bytes, algo,
+    def gate_up(it, m, c):
+        b = it.bufs[m]
+        gq, gsf, _ = it.gu[c]
+        if it.w4a16:
+            nv.bf16_fp4_gemm_ex(b["x"], gq, gsf, it.a_gu, b["gu"], m, 2 * it.inter, it.hid, ws, ws_bytes, algo,
                                 stream=SH[0])
-        elif fused_decode:
-            nv.nvfp4_mlp_decode(x_in[m], gs_x_d, gq, gsf, a_gu, gs_h_d, dq, dsf, a_dn, b["xq"], b["xs"],
-                                b["hq"], b["hs"], b["out"], m, hid, inter, True, ws, ws_bytes, stream=SH[0])
         else:
-            nv.nvfp4_gemm_swiglu_quant_ex(b["xq"], b["xs"], gq, gsf, a_gu, gs_h_d, b["hq"], b["hs"], m,
-                                          2 * inter, hid, ws, ws_bytes, algo, stream=SH[0])
+            nv.nvfp4_gemm_swiglu_quant_ex(b["xq"], b["xs"], gq, gsf, it.a_gu, it.gs_h, b["hq"], b["hs"], m,
+                                          2 * it.inter, it.hid, ws, ws_bytes, algo, stream=SH[0])
 
-    def forward(m, wc, ev=None):
-        """One MLP forward; ev = (start, end) events around the dominant kernel."""
-        b = bufs[m]
-        (gq, gsf, _), (dq, dsf, _) = wc
-        if wl != "w4a16" and not fused_decode:
-            nv.nvfp4_quantize(x_in[m], m, hid, gs_x_d, b["xq"], b["xs"], stream=SH[0])
-        if ev is not None:
-            ev[0].record()
-        dominant(m, wc)
-        if ev is not None:
-            ev[1].record()
-        if wl == "w4a16":
-            nv.silu_mul_bf16(b["gu"], m, inter, b["h16"], stream=SH[0])
-            nv.bf16_fp4_gemm_ex(b["h16"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes, algo,
+    def down(it, m, c):
+        b = it.bufs[m]
+        dq, dsf, _ = it.dn[c]
+        if it.w4a16:
+            nv.bf16_fp4_gemm_ex(b["h16"], dq, dsf, it.a_dn, b["out"], m, it.hid, it.inter, ws, ws_bytes, algo,
                                 stream=SH[0])
-        elif not fused_decode:
-            nv.nvfp4_gemm_ex(b["hq"], b["hs"], dq, dsf, a_dn, b["out"], m, hid, inter, ws, ws_bytes, algo,
-                             stream=SH[0])
+        else:
+            nv.nvfp4_gemm_ex(b["hq"], b["hs"], dq, dsf, it.a_dn, b["out"], m, it.hid, it.inter, ws, ws_bytes,
+                             algo, stream=SH[0])
 
-    launches_per_step = sum((1 if fused_decode else 3) for _ in ms)
+    def forward(it, m, c):
+        b = it.bufs[m]
+        if not it.w4a16:
+            nv.nvfp4_quantize(b["x"], m, it.hid, it.gs_x_d, b["xq"], b["xs"], stream=SH[0])
+        gate_up(it, m, c)
+        if it.w4a16:
+            nv.silu_mul_bf16(b["gu"], m, it.inter, b["h16"], stream=SH[0])
+        down(it, m, c)
 
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        ext_ok = True
-    except TypeError:
-        ext_ok = False
+    def forward_unfused(it, m, c):
+        """The unfused decode chain: gate_up GEMM to bf16 on the plain weight,
+        then silu_mul_nvfp4_quantize, then down_proj."""
+        b = it.bufs[m]
+        gq, gsf, _ = it.gu_plain[c]
+        nv.nvfp4_quantize(b["x"], m, it.hid, it.gs_x_d, b["xq"], b["xs"], stream=SH[0])
+        nv.nvfp4_gemm_ex(b["xq"], b["xs"], gq, gsf, it.a_gu_plain, b["gu"], m, 2 * it.inter, it.hid, ws, ws_bytes,
+                         algo, stream=SH[0])
+        nv.silu_mul_nvfp4_quantize(b["gu"], m, it.inter, it.gs_h, b["hq"], b["hs"], stream=SH[0])
+        down(it, m, c)
+
+    def launches(it):
+        return len(it.ms) * 3
 
     stream = torch.cuda.Stream(device=dev)
     SH[0] = stream.cuda_stream
-    # Two graph sets per weight copy: plain step graphs for the headline pass
-    # (an event node between kernels would end their programmatic-launch
-    # overlap) and the same steps with timing events around the dominant
-    # kernel for the roofline pass that follows.
-    graphs, probe_graphs, events = [], [], []
+
+    def graph_of(fn):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            fn()
+        return gr
+
+    def time_graph(gr, reps=3):
+        """Mean ms of one replay of `gr` over `reps` replays (after one warm)."""
+        with torch.cuda.stream(stream):
+            gr.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / reps
+
     with torch.cuda.stream(stream):
-        for m in ms:                      # warm the kernels outside capture
-            forward(m, copies[0])
+        for it in items:                      # warm every kernel outside capture
+            for m in it.ms:
+                forward(it, m, 0)
         torch.cuda.synchronize()
-        for c in range(ncopy):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
-                for m in ms:
-                    forward(m, copies[c])
-            graphs.append(gr)
-            if ext_ok:
-                evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                        torch.cuda.Event(enable_timing=True, external=True)) for _ in ms]
-                pg = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(pg, stream=stream):
-                    for j, m in enumerate(ms):
-                        forward(m, copies[c], evs[j])
-                probe_graphs.append(pg)
-                events.append(evs)
+        graphs = {it.key: [graph_of(lambda it=it, c=c: [forward(it, m, c) for m in it.ms]) for c in range(NCOPY)]
+                  for it in items}
     torch.cuda.synchronize()
+    tokens_per_step = sum(sum(it.ms) for it in items)
+    launches_per_step = sum(launches(it) for it in items)
+
+    def step(i):
+        for it in items:
+            graphs[it.key][i % NCOPY].replay()
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    for i in range(args.warmup):
-        with torch.cuda.stream(stream):
-            graphs[i % ncopy].replay()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
     torch.cuda.synchronize()
 
     clocks = Clocks(local)
     clocks.start()
+    # ------------------------------------------------------ headline (timed)
     barrier()
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
@@ -447,117 +509,161 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         t_start.record()
         for i in range(args.steps):
-            graphs[i % ncopy].replay()
+            step(i)
         t_end.record()
     torch.cuda.synchronize()
     barrier()
     step_ms = t_start.elapsed_time(t_end) / args.steps
-    # roofline pass: the same number of steps with the instrumented graphs
-    dom_ms = None
-    if ext_ok:
-        sums = [0.0] * len(ms)
+
+    # -------------------------------------- per-workload replay distributions
+    per = {}
+    for it in items:
+        times = []
         with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                probe_graphs[i % ncopy].replay()
-                # each graph's event nodes keep only their latest replay: read
-                # them once every copy has been replayed (and at the end)
-                if i % ncopy == ncopy - 1 or i == args.steps - 1:
-                    stream.synchronize()
-                    for c in range(i % ncopy + 1):
-                        for j in range(len(ms)):
-                            sums[j] += events[c][j][0].elapsed_time(events[c][j][1])
-        torch.cuda.synchronize()
-        dom_ms = [v / args.steps for v in sums]
-    # the dominant kernel alone, REPS launches back to back in one graph
-    # (weight copies rotating), events around the replays: its per-launch time
-    # with the programmatic-launch overlap it also gets inside the step graph
-    # (the event nodes of the pass above end that overlap)
-    b2b_ms = []
-    REPS = 8
-    with torch.cuda.stream(stream):
-        for m in ms:
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
-                for r in range(REPS):
-                    dominant(m, copies[r % ncopy])
-            gr.replay()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(3):
-                gr.replay()
-            e1.record(stream)
-            stream.synchronize()
-            b2b_ms.append(e0.elapsed_time(e1) / (3 * REPS))
-            del gr
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(REPLAYS)]
+            for i, (a, b) in enumerate(evs):
+                a.record(stream)
+                graphs[it.key][i % NCOPY].replay()
+                b.record(stream)
+        stream.synchronize()
+        times = [a.elapsed_time(b) for a, b in evs]
+        med = statistics.median(times)
+        per[it.key] = {"workload": it.title, "tokens": sum(it.ms), "replays": REPLAYS,
+                       "ms_median": med, "ms_p10": pct(times, 0.1), "ms_p90": pct(times, 0.9),
+                       "tokens_per_s": sum(it.ms) / (med / 1000.0)}
+
+    # --------------------- per M: whole forward and each GEMM, back to back
+    def per_launch_ms(fn):
+        gr = graph_of(lambda: [fn(r % NCOPY) for r in range(REPS)])
+        t = time_graph(gr) / REPS
+        del gr
+        return t
+
+    w_bytes = {}      # per weight tensor: codes + scales
+    for it in items:
+        hid, inter = it.hid, it.inter
+        gu_w = 2 * inter * hid * 9 // 16
+        dn_w = inter * hid * 9 // 16
+        rec = per[it.key]
+        rec["per_m"] = {}
+        for m in it.ms:
+            t_fwd = per_launch_ms(lambda c, it=it, m=m: forward(it, m, c))
+            t_gu = per_launch_ms(lambda c, it=it, m=m: gate_up(it, m, c))
+            t_dn = per_launch_ms(lambda c, it=it, m=m: down(it, m, c))
+            r = {"forward_us": 1000 * t_fwd, "gate_up_us": 1000 * t_gu, "down_us": 1000 * t_dn,
+                 "tokens_per_s": m / (t_fwd / 1000.0)}
+            if it.w4a16:
+                gu_b = gu_w + m * hid * 2 + m * 2 * inter * 2
+                dn_b = dn_w + m * inter * 2 + m * hid * 2
+                gu_f, dn_f = 2.0 * m * hid * 2 * inter, 2.0 * m * inter * hid
+            else:
+                gu_b = gu_w + m * hid * 9 // 16 + m * inter * 9 // 16
+                dn_b = dn_w + m * inter * 9 // 16 + m * hid * 2
+                gu_f, dn_f = 4.0 * m * hid * inter, 2.0 * m * inter * hid
+            if m <= 64:          # weight-streaming: HBM-bound on the weight bytes
+                r["gate_up_hbm_frac"] = gu_b / (t_gu / 1000) / 1e9 / hbm_peak
+                r["down_hbm_frac"] = dn_b / (t_dn / 1000) / 1e9 / hbm_peak
+                r["path_hbm_frac"] = (gu_w + dn_w) / (t_fwd / 1000) / 1e9 / hbm_peak
+            else:                # compute-bound: tensor peak of the contraction's dtype
+                pkk = bf16_peak if it.w4a16 else fp4_peak
+                r["gate_up_tensor_frac"] = gu_f / (t_gu / 1000) / 1e12 / pkk
+                r["down_tensor_frac"] = dn_f / (t_dn / 1000) / 1e12 / pkk
+                r["gate_up_tflops"] = gu_f / (t_gu / 1000) / 1e12
+            rec["per_m"][str(m)] = r
+        if it.wid == 1 and it.gu_plain is not None:
+            rec["unfused_chain_forward_us"] = {
+                str(m): 1000 * per_launch_ms(lambda c, it=it, m=m: forward_unfused(it, m, c)) for m in it.ms}
+        w_bytes[it.key] = gu_w + dn_w
+
+    # ------------------------------------------------- elementwise kernels
+    elementwise = {}
+    big = next((it for it in items if it.wid == 3), None)
+    if big is not None:
+        m, k = max(big.ms), big.hid
+        xs2 = [big.x[:m], torch.empty_like(big.x[:m]).copy_(big.x[:m])]    # 2 x 117 MB > L2
+        b = big.bufs[m]
+        t = per_launch_ms(lambda c: nv.nvfp4_quantize(xs2[c % 2], m, k, big.gs_x_d, b["xq"], b["xs"],
+                                                      stream=SH[0]))
+        nb = m * k * 2 + m * k // 2 + m * k // 16
+        elementwise["nvfp4_quantize"] = {"shape": f"[{m}, {k}]", "us": 1000 * t, "bytes": nb,
+                                         "gbs": nb / (t / 1000) / 1e9, "hbm_frac": nb / (t / 1000) / 1e9 / hbm_peak}
+        del xs2
+    dec = next((it for it in items if it.wid in (1, 4)), None)
+    if dec is not None:
+        inter = dec.inter
+        for m in (16, 1024):
+            gus = [torch.randn((m, 2 * inter), device=dev).to(torch.bfloat16) for _ in range(2)]
+            hq = torch.empty((m, inter // 2), dtype=torch.uint8, device=dev)
+            hs = torch.empty((nv.nvfp4_sf_bytes(m, inter),), dtype=torch.uint8, device=dev)
+            h16 = torch.empty((m, inter), dtype=torch.bfloat16, device=dev)
+            gsd = scalar(64.0)
+            t = per_launch_ms(lambda c: nv.silu_mul_nvfp4_quantize(gus[c % 2], m, inter, gsd, hq, hs,
+                                                                   stream=SH[0]))
+            nb = m * 2 * inter * 2 + m * inter // 2 + m * inter // 16
+            elementwise[f"silu_mul_nvfp4_quantize_m{m}"] = {
+                "shape": f"[{m}, {2 * inter}]", "us": 1000 * t, "bytes": nb, "gbs": nb / (t / 1000) / 1e9,
+                "hbm_frac": nb / (t / 1000) / 1e9 / hbm_peak}
+            t = per_launch_ms(lambda c: nv.silu_mul_bf16(gus[c % 2], m, inter, h16, stream=SH[0]))
+            nb = m * 2 * inter * 2 + m * inter * 2
+            elementwise[f"silu_mul_bf16_m{m}"] = {
+                "shape": f"[{m}, {2 * inter}]", "us": 1000 * t, "bytes": nb, "gbs": nb / (t / 1000) / 1e9,
+                "hbm_frac": nb / (t / 1000) / 1e9 / hbm_peak}
+            del gus
     clk = clocks.stop()
 
     step_ms, value = aggregate(step_ms, tokens_per_step, world, device=dev)
 
+    # roofline of the step's dominant kernel: the GEMM with the largest share
+    # of the step time
+    dom = None
+    for it in items:
+        for m in it.ms:
+            r = per[it.key]["per_m"][str(m)]
+            for which in ("gate_up", "down"):
+                t = r[f"{which}_us"]
+                if dom is None or t > dom[0]:
+                    dom = (t, it, m, which)
     roofline = None
-    if b2b_ms:
-        timing_note = (f"dominant-kernel time: {REPS} launches back to back in one CUDA graph per M, CUDA "
-                       "events on the launching stream around 3 replays; isolated_us: events around each "
-                       f"launch inside the step graphs ({args.steps}-step pass, no launch overlap)")
-        per_m_us = {str(m): 1000.0 * t for m, t in zip(ms, b2b_ms)}
-        tot_s = sum(b2b_ms) / 1000.0
-        if fused_decode:
-            # weights (codes + scales) of both GEMMs, x in, output out
-            nbytes = sum(3 * inter * hid * 9 // 16 + 2 * m * hid * 2 for m in ms)
-            achieved = nbytes / tot_s / 1e9
-            roofline = {"bound": "hbm", "kernel": "nvfp4_mlp_decode (whole decode MLP, one launch, M=1..16)",
-                        "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                        "traffic": None, "algorithmic_bytes_per_step": nbytes}
-        elif wl == "decode":
-            # gate_up weights (codes + scales), quantized x in, NVFP4 h out
-            nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 9 // 16 + m * inter * 9 // 16 for m in ms)
-            achieved = nbytes / tot_s / 1e9
-            family = {"auto": "swap-AB tcgen05", "swapab": "swap-AB tcgen05", "gemv": "CUDA-core GEMV",
-                      "tc": "128-token-tile tcgen05, CTA pairs", "tc1sm": "128-token-tile tcgen05"}[args.algo]
-            if args.algo == "auto" and mmax > 64:
-                family = "128-token-tile tcgen05"
-            # traffic: DRAM bytes read + written by one launch of the swap-AB
-            # NT = 16 instance (every M <= 16) in an ncu capture of this bench
-            # command (summary in profiles/swapab_swiglu_gate_up_m16_h5120.md);
-            # to be set to None whenever the kernel changes before it is
-            # captured again
-            measured = args.algo in ("auto", "swapab") and mmax <= 16
-            roofline = {"bound": "hbm",
-                        "kernel": f"nvfp4_gemm_swiglu_quant gate_up 34816x5120 ({family}, "
-                                  f"M={','.join(map(str, ms))})",
-                        "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                        "traffic": 100.42e6 + 2.94e6 if measured else None, "traffic_unit": "bytes per launch",
-                        "algorithmic_bytes_per_launch": nbytes / len(ms), "algorithmic_bytes_per_step": nbytes}
-        elif wl == "prefill":
-            flops = sum(4.0 * m * hid * inter for m in ms)
-            achieved = flops / tot_s / 1e12
-            roofline = {"bound": "tensor", "kernel": "nvfp4_gemm_swiglu_quant gate_up 36864x7168 (tcgen05)",
-                        "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
-                        "traffic": None, "peak_note": "measured bf16 burst x 6 (nominal fp4:bf16)"}
+    if dom is not None:
+        t_us, it, m, which = dom
+        r = per[it.key]["per_m"][str(m)]
+        if m > 64:
+            flops = (4.0 if which == "gate_up" else 2.0) * m * it.hid * it.inter
+            pkk = bf16_peak if it.w4a16 else fp4_peak
+            achieved = flops / (t_us / 1e6) / 1e12
+            roofline = {"bound": "tensor", "achieved": achieved, "peak": pkk, "unit": "TFLOP/s",
+                        "frac": achieved / pkk, "traffic": None,
+                        "algorithmic_flops_per_launch": flops,
+                        "peak_note": ("measured bf16 burst" if it.w4a16 else
+                                      "measured bf16 burst x 6 (nominal fp4 : bf16)") + f" ({peak_src})"}
         else:
-            nbytes = sum(2 * inter * hid * 9 // 16 + m * hid * 2 + m * 2 * inter * 2 for m in ms)
-            achieved = nbytes / tot_s / 1e9
-            roofline = {"bound": "hbm", "kernel": "bf16_fp4_gemm gate_up 34816x5120",
-                        "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                        "traffic": None}
-        roofline["per_m_us"] = per_m_us
-        if dom_ms:
-            roofline["isolated_us"] = {str(m): 1000.0 * t for m, t in zip(ms, dom_ms)}
-        roofline["peak_source"] = "measured" if pk else "fallback"
-        roofline["timing"] = timing_note
+            nb = r[f"{which}_hbm_frac"] * hbm_peak * 1e9 * (t_us / 1e6)
+            achieved = nb / (t_us / 1e6) / 1e9
+            roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": achieved / hbm_peak, "traffic": None, "algorithmic_bytes_per_launch": nb,
+                        "peak_note": f"measured copy bandwidth ({peak_src})"}
+        fused = not it.w4a16 and which == "gate_up"
+        roofline["kernel"] = (f"{'nvfp4_gemm_swiglu_quant' if fused else ('bf16_fp4_gemm' if it.w4a16 else 'nvfp4_gemm')} "
+                              f"{which} ({it.key}, M={m})")
+        roofline["us_per_launch"] = t_us
+        roofline["timing"] = (f"{REPS} launches back to back in one CUDA graph (weight copies rotating), CUDA "
+                              "events on the launching stream around 3 replays")
 
-    # end to end through the API: pinned host x in, host result out, per step
-    x_host = x.cpu().pin_memory()
-    out_host = torch.empty((sum(ms), hid), dtype=torch.bfloat16).pin_memory()
-    h2d = x.numel() * 2
-    d2h = out_all.numel() * 2
+    # ------------------------------- end to end through the C ABI (no graph)
+    x_host = {it.key: it.x.cpu().pin_memory() for it in items}
+    out_host = {it.key: torch.empty(it.out.shape, dtype=torch.bfloat16).pin_memory() for it in items}
+    h2d = sum(it.x.numel() * 2 for it in items)
+    d2h = sum(it.out.numel() * 2 for it in items)
     e2e_steps = max(3, min(args.steps, 20))
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         def e2e_step(i):
-            x.copy_(x_host, non_blocking=True)
-            for m in ms:
-                forward(m, copies[i % ncopy])
-            out_host.copy_(out_all, non_blocking=True)
+            for it in items:
+                it.x.copy_(x_host[it.key], non_blocking=True)
+                for m in it.ms:
+                    forward(it, m, i % NCOPY)
+                out_host[it.key].copy_(it.out, non_blocking=True)
         for i in range(2):
             e2e_step(i)
         stream.synchronize()
@@ -569,28 +675,35 @@ def run_ours(args, world, rank, local):
     e2e_value = world * tokens_per_step / e2e_s
 
     cpu = None
-    if rank == 0 and wl == "decode" and not args.no_cpu_baseline:
-        tokens, secs, threads = oracle_sample((1, 16))
-        cpu = {"value": tokens / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"CPU oracle (NumPy float64) decode MLP forward at M=1 and M=16 on a 1/{SLICE} "
-                         f"slice of I (I {I // SLICE} of {I}, H {H}), weights pre-quantized; tokens/s "
-                         "scaled to the whole MLP"}
+    if rank == 0 and not args.no_cpu_baseline:
+        smp = OracleSampler([it.wid for it in items])
+        tokens, secs = 0.0, 0.0
+        for _ in range(2):
+            t, s = smp.sample()
+            tokens += t
+            secs += s
+        cpu = {"value": tokens / secs, "unit": "tokens/s", "cores": smp.threads(), "kind": "oracle",
+               "sample": smp.describe() + "; two passes"}
 
     if rank == 0:
         line = {
-            "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16 x nvfp4 (fp32 accumulate)" if wl == "w4a16" else "nvfp4 (e2m1 x ue4m3, fp32 accumulate)",
+            "dtype": "nvfp4 (e2m1 x ue4m3, fp32 accumulate); bf16 x nvfp4 in the W4A16 workload",
             "data": "synthetic",
-            "config": {"workload": workload, "tokens_per_step": tokens_per_step,
-                       "l2": f"{ncopy} rotating weight copies, {ncopy * weight_bytes / 1e6:.0f} MB > L2",
-                       "graph": "one CUDA graph per step", "parallelism": f"replicas{world}",
-                       **({"decode_path": args.decode_path} if wl == "decode" else {}),
-                       **({"algo": args.algo} if args.algo != "auto" else {})},
-            "roofline": roofline, "cpu_baseline": cpu, "clocks": clk,
+            "config": {"workload": "; ".join(it.title for it in items), "tokens_per_step": tokens_per_step,
+                       "step": "one MLP forward per (workload, M), one CUDA graph per workload",
+                       "l2": f"{NCOPY} rotating weight copies per weight family, {weight_bytes / 1e6:.0f} MB > L2",
+                       "weights": "synth N(0, 0.02) fp32 draws, rounded to bf16 and quantized to NVFP4 on the "
+                                  "device by the library",
+                       "parallelism": f"replicas{world}", **({"algo": args.algo} if args.algo != "auto" else {})},
+            "roofline": roofline, "per_workload": per, "elementwise": elementwise,
+            "cpu_baseline": cpu, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "note": "direct API calls, no graph, pinned host buffers"},
+                    "d2h_bytes_per_step": d2h,
+                    "note": "direct API calls, no graph, pinned host buffers; x of every workload in, every "
+                            "output out, each step"},
             "gpu_launches": launches_per_step * args.steps,
         }
         print(json.dumps(line), flush=True)
