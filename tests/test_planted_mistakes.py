@@ -1,20 +1,22 @@
 """Planted-mistake check of the oracle's pins and of the parity acceptance
-rules (run by hand, not by pytest):
-
-    python tests/oracle_mutants.py
+rules.
 
 Each entry plants one plausible mistake in a temporary copy of ``oracle/``
 or of ``tests/tolerance.py`` and runs the CPU pins (``tests/test_oracle_*.py``
 and ``tests/test_tolerance_rules.py``) against it; every mistake must make
 them fail.  Entries marked equivalent change nothing observable (e.g. a clamp the
 next step repeats) and are listed to record that they were considered.
-Exit status 1 if any non-equivalent mistake survives.
+
+Under pytest the mistakes run in parallel (one process each); by hand,
+``python tests/test_planted_mistakes.py`` prints the table and exits 1 if any
+non-equivalent mistake survives.
 """
 import os
 import shutil
 import subprocess
 import sys
 import tempfile
+from concurrent.futures import ThreadPoolExecutor
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -115,21 +117,33 @@ def run_one(fname, old, new):
             f.write(src.replace(old, new))
         tests = sorted(os.path.join("tests", t) for t in os.listdir(os.path.join(tmp, "tests"))
                        if t.startswith("test_oracle") or t == "test_tolerance_rules.py")
+        env = dict(os.environ, PYTHONPATH=tmp, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
         r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *tests],
-                           cwd=tmp, capture_output=True, text=True, env=dict(os.environ, PYTHONPATH=tmp))
+                           cwd=tmp, capture_output=True, text=True, env=env)
         return "caught" if r.returncode != 0 else "survived"
     finally:
         shutil.rmtree(tmp)
 
 
+def run_all():
+    """[(mutant, outcome, as expected)] for every planted mistake."""
+    workers = max(1, min(16, os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        outcomes = list(ex.map(lambda mu: run_one(mu[0], mu[1], mu[2]), MUTANTS))
+    return [(mu, res, (res == "survived") if mu[4] else (res == "caught")) for mu, res in zip(MUTANTS, outcomes)]
+
+
+def test_every_planted_mistake_is_caught():
+    results = run_all()
+    unexpected = [f"{mu[0]}: {mu[3]} -> {res}" for mu, res, ok in results if not ok]
+    assert not unexpected, "planted mistakes not caught as expected:\n" + "\n".join(unexpected)
+
+
 def main():
-    bad = 0
-    for fname, old, new, what, equivalent in MUTANTS:
-        res = run_one(fname, old, new)
-        ok = (res == "survived") if equivalent else (res == "caught")
-        bad += not ok
-        print(f"{'ok ' if ok else 'BAD'} {fname:18s} {what:55s} {res}{' (equivalent)' if equivalent else ''}",
-              flush=True)
+    results = run_all()
+    for (fname, _, _, what, equivalent), res, ok in results:
+        print(f"{'ok ' if ok else 'BAD'} {fname:18s} {what:55s} {res}{' (equivalent)' if equivalent else ''}")
+    bad = sum(not ok for _, _, ok in results)
     print(f"{len(MUTANTS)} planted mistakes, {bad} unexpected")
     return 1 if bad else 0
 
