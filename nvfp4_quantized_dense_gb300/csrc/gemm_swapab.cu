@@ -4,7 +4,14 @@
 // roofline, so the kernel is a deep TMA pipeline (6-8 stages of 16 KB weight
 // tiles per SM) feeding one MMA issuer.
 //
-// Work split: the (128-row weight tile, 256-wide k-block) pairs are laid out
+// Work split, when there are at least twice as many SMs as weight tiles and
+// C of them per tile fill at least 90 % of the SMs: clusters of C CTAs, one
+// tile per cluster, the tile's
+// k-blocks cut into C contiguous runs; the cluster's other CTAs publish their
+// fp32 partial tiles in their own shared memory and its first CTA adds them
+// in K order through distributed shared memory and runs the epilogue -- no
+// workspace and no global round trip after the last MMA.
+// Otherwise: the (128-row weight tile, 256-wide k-block) pairs are laid out
 // tile-major and cut into one contiguous, equal run per CTA, so every SM
 // streams the same number of weight bytes.  A CTA's run crosses tile
 // boundaries; each piece of a tile it covers is a fragment.  A tile covered by
@@ -19,6 +26,9 @@
 // Roles per CTA (192 threads, one CTA per SM): warp 0 TMA producer,
 // warp 1 TMEM owner + MMA issuer (double-buffered accumulators), warps 2..5
 // epilogue (TMEM lane = weight row).  Bounded waits as in gemm_tc.cu.
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "splitk.cuh"
@@ -66,6 +76,7 @@ struct SwapArgs {
   int32_t grid, maxfrag;     // CTAs, fragment slots per CTA (split tiles)
   int32_t whole, split_tiles;   // mixed split: whole tiles per CTA, tiles shared by CTAs
   int32_t split_ok;          // 0: no workspace, every CTA owns whole tiles
+  int32_t cl;                // > 1: clusters of cl CTAs, one tile each, reduced in shared memory
   uint32_t wait_limit;
   int *status;
   const float *rs;      // optional per-token activation dequant factor [M]
@@ -100,7 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + ACC_BUFS;
   uint64_t *drain = tempty + ACC_BUFS;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *parts = drain + 1;           // cluster split: [0] partials published, [1] partials read
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(parts + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   volatile int *last_flag = abort_flag + 1;
   auto st_w = [&](int s) { return base + s * C::STAGE_BYTES; };
@@ -120,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tempty[b], 128);
     }
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(&parts[0], 128 * (p.cl > 1 ? p.cl - 1 : 1));   // every epilogue thread of the others
+    ptx::mbar_init(&parts[1], 128);                               // every epilogue thread of the first CTA
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tm_w);
@@ -130,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if (p.cl > 1) ptx::cluster_sync();   // every CTA's barriers exist before any remote arrival
+  else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tslot;
 
@@ -139,7 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Without: whole tiles per CTA.
   const MixedPartition mixed{p.kb_total, p.grid, p.whole, p.split_tiles};
   const Partition part{(int64_t)p.tiles * p.kb_total, p.grid, p.kb_total, true, p.tiles};
-  const int64_t my_start = part.start(blockIdx.x), my_end = part.start(blockIdx.x + 1);
+  int64_t my_start = part.start(blockIdx.x), my_end = part.start(blockIdx.x + 1);
+  if (p.cl > 1) {   // cluster split: tile blockIdx / cl, this CTA's run of its k-blocks
+    const int64_t tile = blockIdx.x / p.cl, j = blockIdx.x % p.cl;
+    my_start = tile * p.kb_total + p.kb_total * j / p.cl;
+    my_end = tile * p.kb_total + p.kb_total * (j + 1) / p.cl;
+  }
   auto work = [&]() { return WorkIter(p.split_ok != 0, mixed, blockIdx.x, my_start, my_end, p.kb_total); };
   const int ksteps_total = p.k >> 6;
   const int cp4 = ksteps_total;          // 512-byte scale tiles per 128-row block
@@ -302,6 +322,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (et == 0) p.counters[tile] = 0;
       }
 
+      if (p.cl > 1) {
+        // the cluster's other CTAs publish their partials (row r, pitch
+        // PITCH, in their own staging buffer); the first CTA adds them in
+        // rank order -- K order -- and runs the epilogue
+        const uint32_t crank = blockIdx.x % p.cl;
+        bool ok = true;
+        if (crank != 0) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            if (t < mt) s_out[r * C::PITCH + t] = v[t];
+          ptx::mbar_arrive_remote_release_cluster(ptx::map_to_cta(ptx::smem_u32(&parts[0]), 0));
+          ok = ptx::mbar_wait_bounded(&parts[1], 0, limit, kTimeoutNs, abort_flag);    // read by the first CTA
+        } else {
+          ok = ptx::mbar_wait_bounded_acq_cluster(&parts[0], 0, limit, kTimeoutNs, abort_flag);
+          if (ok) {
+            for (int c = 1; c < p.cl; ++c) {
+              const uint32_t src = ptx::map_to_cta(ptx::smem_u32(s_out + r * C::PITCH), (uint32_t)c);
+#pragma unroll
+              for (int t = 0; t < NT; ++t)
+                if (t < mt) v[t] += ptx::ld_cluster_f32(src + 4u * t);
+            }
+            for (int c = 1; c < p.cl; ++c) ptx::mbar_arrive_remote(ptx::map_to_cta(ptx::smem_u32(&parts[1]), (uint32_t)c));
+          }
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+        }
+        if (ptx::bar_any(1, 128, !ok)) break;
+        if (crank != 0) continue;
+      }
+
       const int n = tile * 128 + r;
       if constexpr (MODE == TC_W4A4) {
         if (n < p.n) {
@@ -364,15 +416,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (p.cl > 1) ptx::cluster_sync();   // no CTA leaves while the first CTA may still read its partials
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 struct Plan {
   int nt, tiles, kb_total, grid, maxfrag, whole, split_tiles;
+  int cl;                 // > 1: cluster split (one tile per cluster of cl CTAs)
   size_t ws_bytes;        // workspace the mixed split needs (0: no tile shared)
   bool split;             // mixed split (false: whole tiles per CTA, no workspace)
 };
+
+// Clusters of cl CTAs of the NT instance the device holds at once (both
+// modes use the same resources); without a device, as many as the SMs allow.
+int max_clusters(int nt, int cl) {
+  static std::atomic<int> cache[64][3][9];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms() / cl;
+  const int ni = nt == 16 ? 0 : nt == 32 ? 1 : 2;
+  int v = cache[dev][ni][cl].load(std::memory_order_relaxed);
+  if (v) return v;
+  auto query = [&](auto kernel, uint32_t smem) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(cl * (num_sms() / cl));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    return cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess ? n : 0;
+  };
+  v = ni == 0 ? query(swapab_kernel<TC_W4A4, 16>, Cfg<16>::SMEM_BYTES)
+      : ni == 1 ? query(swapab_kernel<TC_W4A4, 32>, Cfg<32>::SMEM_BYTES)
+                : query(swapab_kernel<TC_W4A4, 64>, Cfg<64>::SMEM_BYTES);
+  if (v <= 0) v = 1;
+  cache[dev][ni][cl].store(v, std::memory_order_relaxed);
+  return v;
+}
 
 size_t counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) / 256 * 256; }
 
@@ -381,8 +469,28 @@ Plan make_plan(int64_t m, int64_t n, int64_t k) {
   pl.nt = m <= 16 ? 16 : m <= 32 ? 32 : 64;
   pl.tiles = (int)((n + 127) / 128);
   pl.kb_total = (int)((k + BK - 1) / BK);
+  const int sms = num_sms();
+  // Cluster split when the tiles are at most half the SMs: cl CTAs per tile
+  // (at most 8, the portable cluster size, and at most one per k-block),
+  // provided the clusters keep at least 90 % of the SMs busy and all fit at
+  // once.  The weight stream is spread over every SM either way: with fewer
+  // CTAs streaming (40 tiles x 3 = 120 of 152 SMs for the H5120 down_proj)
+  // the cluster split measured slower than the global one, whose reduction
+  // costs two global round trips after the last MMA.
+  for (int cl = std::min(std::min(8, sms / std::max(pl.tiles, 1)), pl.kb_total);
+       cl >= 2 && (int64_t)pl.tiles * cl * 10 >= (int64_t)sms * 9; --cl) {
+    if (max_clusters(pl.nt, cl) >= pl.tiles) {
+      pl.cl = cl;
+      pl.grid = pl.tiles * cl;
+      pl.maxfrag = 1;
+      pl.ws_bytes = 0;
+      pl.split = false;
+      return pl;
+    }
+  }
+  pl.cl = 1;
   const int64_t w = (int64_t)pl.tiles * pl.kb_total;
-  pl.grid = (int)(w < num_sms() ? w : num_sms());
+  pl.grid = (int)(w < sms ? w : sms);
   // every CTA gets `whole` whole tiles; the remaining tiles are cut into one
   // contiguous run of (tile, k-block) pairs per CTA
   pl.whole = pl.tiles / pl.grid;
@@ -439,13 +547,30 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   a.whole = pl.whole;
   a.split_tiles = pl.split_tiles;
   a.split_ok = split ? 1 : 0;
+  a.cl = pl.cl;
   // without a workspace each CTA owns whole tiles (at most one CTA per tile)
-  a.grid = split ? pl.grid : (pl.tiles < num_sms() ? pl.tiles : num_sms());
+  a.grid = pl.cl > 1 ? pl.grid : split ? pl.grid : (pl.tiles < num_sms() ? pl.tiles : num_sms());
   a.wait_limit = wait_limit;
   a.status = device_status_ptr();
   a.rs = rs;
   if (!a.status) return cudaErrorInvalidValue;
-  return launch_pdl(swapab_kernel<MODE, NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_w, tm_x, a);
+  if (pl.cl <= 1)
+    return launch_pdl(swapab_kernel<MODE, NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_w, tm_x, a);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = pl.cl;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, swapab_kernel<MODE, NT>, tm_w, tm_x, a);
 }
 
 template <int MODE>

@@ -206,6 +206,49 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive on an mbarrier of any CTA of the cluster with a release at cluster
+// scope: this thread's earlier shared-memory writes become visible to the
+// CTA that acquires the phase (for data read through distributed shared
+// memory; it costs a cluster-wide fence, so it is not for pipeline stages).
+__device__ __forceinline__ void mbar_arrive_remote_release_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Bounded wait (as mbar_wait_bounded) with a cluster-scope acquire: pairs
+// with mbar_arrive_remote_release_cluster.
+__device__ __forceinline__ bool mbar_wait_bounded_acq_cluster(uint64_t *bar, uint32_t parity, uint32_t limit,
+                                                              uint64_t timeout_ns, volatile int *abort) {
+  uint64_t t0 = 0;
+  for (uint32_t polls = 1;; ++polls) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (limit) {
+      if (polls >= limit) return false;
+    } else if ((polls & 255u) == 0) {
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > timeout_ns) return false;
+    }
+  }
+}
+
+// Load a float from another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
 // Store a word into another CTA's shared memory (relaxed, cluster scope).
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");

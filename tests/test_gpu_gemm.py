@@ -83,10 +83,13 @@ TC_SHAPES = [(128, 256, 256), (1, 256, 256), (130, 160, 320), (256, 512, 1024), 
 
 
 # swap-AB (weights as the MMA M operand): tokens padded to 16/32/64, split-K;
-# the last two have more weight tiles than SMs (whole tiles per CTA after the
-# shared ones: 160 tiles of 2 k-blocks, 306 tiles of 3 k-blocks)
+# (1, 20480, 512) and (5, 39168, 768) have more weight tiles than SMs (whole
+# tiles per CTA after the shared ones: 160 tiles of 2 k-blocks, 306 tiles of
+# 3 k-blocks); (3, 2560, 2048) and (40, 6144, 1280) take the cluster split
+# (one tile per cluster: 20 tiles x 7 CTAs, 48 x 3 with 64-token tiles)
 SWAP_SHAPES = [(1, 256, 256), (4, 1024, 256), (3, 96, 320), (16, 512, 2048), (17, 128, 128),
-               (33, 384, 1024), (64, 256, 512), (8, 2048, 8192), (1, 20480, 512), (5, 39168, 768)]
+               (33, 384, 1024), (64, 256, 512), (8, 2048, 8192), (1, 20480, 512), (5, 39168, 768),
+               (3, 2560, 2048), (16, 4864, 512), (40, 6144, 1280)]
 
 
 @pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SMALL_SHAPES] +
@@ -184,8 +187,9 @@ SWIGLU_TC = [(128, 256, 256), (4, 1024, 256), (130, 384, 320), (256, 1024, 1024)
              (384, 640, 1280)]
 
 
+# (33, 3072, 2048) takes the cluster split (24 tiles x 6 CTAs)
 SWIGLU_SWAP = [(1, 256, 256), (4, 1024, 256), (3, 128, 320), (16, 384, 4096), (40, 256, 512),
-               (64, 1024, 1024)]
+               (64, 1024, 1024), (16, 4096, 1024), (33, 3072, 2048)]
 
 
 @pytest.mark.parametrize("m,n,k,algo", [(m, n, k, GEMV) for m, n, k in SWIGLU_GEMV] +
@@ -214,6 +218,22 @@ def test_swiglu_decode_h5120_full_size_sampled(lib, m):
     16-feature blocks, one in each 64-feature (128-row) weight tile."""
     ws = weights(1, "gate_up")
     _swiglu_case(lib, 1, m, ws.n, ws.k, ws, TC_SWAPAB, sampled_blocks=272)
+
+
+@pytest.mark.parametrize("m", [1, 64])
+def test_w4a4_deepseek_down_full_size_sampled(lib, m):
+    """DeepSeek-V3-shaped decode down_proj 7168 x 18432 (56 weight tiles, all
+    shared by CTAs along K) on an oracle-made NVFP4 h, in the launch the
+    decode chain uses; 512 sampled output columns."""
+    ws = weights(2, "down")
+    hf = synth.random_matrix((m, ws.k), (22, m), scale=0.05)
+    gs_x = oracle.global_scale(np.abs(hf).max())
+    xq, xs = oracle.quantize_nvfp4(hf, gs_x)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    got = run_w4a4(lib, xq, xs, ws.device_prepared(lib), alpha, m, ws.n, ws.k, 0)
+    cols = sample_rows(ws.n, 512, seed=m)
+    err = assert_gemm_close(got[:, cols], oracle.gemm_w4a4(xq, xs, ws.packed[cols], ws.sf[cols], alpha))
+    print(f"deepseek down m={m}: rel err {err:.2e}")
 
 
 @pytest.mark.parametrize("which", ["gate_up", "down"])

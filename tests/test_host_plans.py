@@ -43,9 +43,25 @@ def r256(b):
     return (b + 255) // 256 * 256
 
 
-def swapab_plan(m, n, k, sms):
+def swapab_cluster(tiles, kbt, sms):
+    """Cluster size of the cluster split (1: not used): at most 8 CTAs per
+    tile and one per k-block, at least 90 % of the SMs busy, every cluster
+    resident at once (without a device: as many as the SMs allow)."""
+    cl = min(8, sms // max(tiles, 1), kbt)
+    while cl >= 2 and tiles * cl * 10 >= sms * 9:
+        if sms // cl >= tiles:
+            return cl
+        cl -= 1
+    return 1
+
+
+def swapab_plan(m, n, k, sms, clusters=True):
+    """clusters=False: the split the kernel uses when no cluster split fits."""
     nt = 16 if m <= 16 else 32 if m <= 32 else 64
     tiles, kbt = math.ceil(n / 128), math.ceil(k / 256)
+    cl = swapab_cluster(tiles, kbt, sms) if clusters else 1
+    if cl > 1:
+        return dict(nt=nt, tiles=tiles, kbt=kbt, grid=tiles * cl, whole=0, split=0, ws=0, cl=cl)
     grid = min(tiles * kbt, sms)
     whole = tiles // grid
     split = tiles - whole * grid
@@ -56,7 +72,7 @@ def swapab_plan(m, n, k, sms):
     maxfrag = math.ceil(per / kbt) + 1
     shared = units % grid != 0 or (units // grid) % kbt != 0
     ws = r256(tiles * 4) + grid * maxfrag * nt * 128 * 4 if shared else 0
-    return dict(nt=nt, tiles=tiles, kbt=kbt, grid=grid, whole=whole, split=split, ws=ws)
+    return dict(nt=nt, tiles=tiles, kbt=kbt, grid=grid, whole=whole, split=split, ws=ws, cl=1)
 
 
 def w4a16_ws(m, n, k, sms):
@@ -75,7 +91,10 @@ def w4a16_ws(m, n, k, sms):
 SWAP_CASES = [
     (1, 34816, 5120),     # decode gate_up H5120: 272 tiles -> one whole tile per CTA + shared tiles
     (16, 34816, 5120),
-    (1, 5120, 17408),     # decode down: 40 tiles, all shared
+    (1, 5120, 17408),     # decode down: 40 tiles, all shared (clusters of 3 would leave 32 SMs idle)
+    (16, 7168, 18432),    # DeepSeek-shaped down: 56 tiles, all shared
+    (3, 2560, 2048),      # 20 tiles -> clusters of 7 CTAs, one tile each
+    (40, 6144, 1280),     # 48 tiles -> clusters of 3
     (64, 36864, 7168),    # DeepSeek-shaped gate_up
     (8, 7168, 18432),
     (1, 20480, 512),      # 160 tiles of 2 k-blocks: the shared k-blocks would be fewer than CTAs
@@ -95,6 +114,14 @@ def test_swapab_scratch_matches_plan(lib, m, n, k):
 @pytest.mark.parametrize("sms", [148, 152, 7])
 def test_swapab_partition_contributors_are_contiguous(m, n, k, sms):
     pl = swapab_plan(m, n, k, sms)
+    if pl["cl"] > 1:
+        # cluster split: the cl CTAs of tile t cover its k-blocks in order,
+        # each at least one, as the kernel cuts them (j * kbt / cl)
+        cl, kbt = pl["cl"], pl["kbt"]
+        assert 2 <= cl <= 8 and pl["grid"] == pl["tiles"] * cl <= sms and 10 * pl["grid"] >= 9 * sms
+        cuts = [kbt * j // cl for j in range(cl + 1)]
+        assert cuts[0] == 0 and cuts[-1] == kbt and all(b > a for a, b in zip(cuts, cuts[1:]))
+        return
     grid, kbt, split = pl["grid"], pl["kbt"], pl["split"]
     assert split + pl["whole"] * grid == pl["tiles"]
     units = split * kbt
@@ -169,7 +196,7 @@ def test_swapab_scratch_matches_plan_random_shapes(lib):
 def test_swapab_partition_invariants_random_shapes():
     for m, n, k in _random_shapes(300, 12):
         for sms in (148, 152):
-            pl = swapab_plan(m, n, k, sms)
+            pl = swapab_plan(m, n, k, sms, clusters=False)
             grid, kbt, split = pl["grid"], pl["kbt"], pl["split"]
             assert split + pl["whole"] * grid == pl["tiles"]
             units = split * kbt
@@ -209,7 +236,7 @@ def test_swapab_reduction_bookkeeping(m, n, k, sms):
     inverse of start) bracket exactly the CTAs that hold a fragment of it;
     each contributor's partial slot (f_first for the first owner, 0 for the
     others) is its fragment's index in its own walk, below maxfrag."""
-    pl = swapab_plan(m, n, k, sms)
+    pl = swapab_plan(m, n, k, sms, clusters=False)
     grid, kbt, whole, split = pl["grid"], pl["kbt"], pl["whole"], pl["split"]
     units = split * kbt
     maxfrag = (math.ceil(math.ceil(units / grid) / kbt) + 1) if units else 1
