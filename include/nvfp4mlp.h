@@ -107,11 +107,14 @@ size_t nvfp4_sf_bytes(int64_t rows, int64_t k, nvfp4_sf_layout layout);
 
 /* Scratch bytes the GEMM entry points want for (m, n, k) with `algo` (AUTO
  * resolves as the GEMM would).  Non-zero only for the weight-streaming
- * tensor-core kernel (NVFP4_ALGO_TC_SWAPAB, AUTO for m <= 64), which splits K
- * across CTAs: fp32 partial tiles plus one arrival counter per 128-row weight
- * tile.  The workspace must be zero-filled once before its first use; every
- * complete call leaves the counters at zero again, so one buffer serves a
- * whole sequence of calls on one stream (not concurrent calls).  After a call
+ * tensor-core kernel (NVFP4_ALGO_TC_SWAPAB, AUTO for m <= 64) when it splits K
+ * across CTAs: a fixed 64 KiB area of arrival counters followed by fp32
+ * partial tiles.  Every workspace of this library (this one, the W4A16
+ * GEMM's, nvfp4_mlp_decode's) has that layout, so calls of different shapes
+ * and entry points may share one buffer sized for the largest of them.  The
+ * workspace must be zero-filled once before its first use; every complete
+ * call leaves the counters at zero again, so one buffer serves a whole
+ * sequence of calls on one stream (not concurrent calls).  After a call
  * that reported NVFP4_ERR_DEVICE_TIMEOUT, zero it again.  A smaller or NULL
  * workspace is not an error: the kernel then runs one CTA per weight tile
  * without splitting K. */
@@ -242,10 +245,11 @@ nvfp4_status nvfp4_gemm_swiglu_quant_per_token(const uint8_t *a_fp4, const uint8
  *   workspace  optional DEVICE scratch (nullptr / 0 allowed): with
  *              bf16_fp4_gemm_workspace_bytes(m, n, k, algo) bytes, 16-byte
  *              aligned and zero-filled once before first use, the tensor-core
- *              path splits up to 64 tokens along K over all SMs (the
- *              counters are left at zero after every complete call; calls
- *              sharing it must be stream-ordered); with less, every SM owns
- *              whole 128-row weight tiles.  The result does not depend on it.
+ *              path splits the work along K over all SMs -- up to 64 tokens
+ *              always, above when whole 128-row weight tiles would leave SMs
+ *              idle (the counters are left at zero after every complete call;
+ *              calls sharing it must be stream-ordered); with less, every SM
+ *              owns whole weight tiles.  The result does not depend on it.
  * Requires k % 64 == 0, n % 32 == 0. */
 nvfp4_status bf16_fp4_gemm(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
                            const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,

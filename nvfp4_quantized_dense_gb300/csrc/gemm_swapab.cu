@@ -462,7 +462,6 @@ int max_clusters(int nt, int cl) {
   return v;
 }
 
-size_t counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) / 256 * 256; }
 
 Plan make_plan(int64_t m, int64_t n, int64_t k) {
   Plan pl{};
@@ -505,7 +504,8 @@ Plan make_plan(int64_t m, int64_t n, int64_t k) {
   const int64_t per = (ws + pl.grid - 1) / pl.grid;          // split k-blocks per CTA, rounded up
   pl.maxfrag = (int)((per + pl.kb_total - 1) / pl.kb_total + 1);
   const bool shared_tiles = (ws % pl.grid != 0) || ((ws / pl.grid) % pl.kb_total != 0);
-  pl.ws_bytes = shared_tiles ? counter_bytes(pl.tiles) + (size_t)pl.grid * pl.maxfrag * pl.nt * 128 * 4 : 0;
+  // counters: one per shared tile (tiles [0, split_tiles), fewer than twice the grid)
+  pl.ws_bytes = shared_tiles ? kCounterArea + (size_t)pl.grid * pl.maxfrag * pl.nt * 128 * 4 : 0;
   pl.split = true;
   return pl;
 }
@@ -536,7 +536,7 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   const bool split = pl.split;
   if (split && ws != nullptr) {   // (no workspace is used when no tile is shared)
     a.counters = static_cast<int *>(ws);
-    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + counter_bytes(pl.tiles));
+    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kCounterArea);
   }
   a.m = (int32_t)m;
   a.n = (int32_t)n;

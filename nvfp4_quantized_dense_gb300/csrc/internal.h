@@ -45,6 +45,15 @@ struct PerDeviceOnce {
   }
 };
 
+// Every split-K workspace starts with a fixed area of arrival counters (and
+// other words that must start at zero); a kernel's fp32 partials follow it.
+// Calls of different shapes may share one workspace in stream order: their
+// counters all live in this area, which no kernel's partials overlap, and
+// every complete call leaves them at zero.  A kernel that would need more
+// counter slots than the area holds does not split.
+constexpr size_t kCounterArea = 64 * 1024;
+constexpr int64_t kCounterSlots = (int64_t)(kCounterArea / 4);
+
 // Poll limit of the kernels' bounded waits set through nvfp4_set_wait_limit
 // (0 = the kernels' wall-clock default).
 uint32_t wait_limit();
@@ -112,8 +121,9 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
 
 // W4A16 on the tensor cores (weights dequantized to bf16 in shared memory).
 // With a workspace of w4a16_workspace_bytes (zero-filled once; counters left
-// at zero), up to 64 tokens are split across CTAs along K; otherwise every
-// CTA owns whole weight tiles.
+// at zero), the work is split across CTAs along K -- up to 64 tokens always,
+// above when whole weight tiles would leave SMs idle; otherwise every CTA
+// owns whole tiles.
 bool w4a16_tc_supported(int64_t m, int64_t n, int64_t k);
 size_t w4a16_workspace_bytes(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_w4a16_tc(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, const float *alpha,

@@ -593,7 +593,7 @@ Plan make_plan(int64_t m, int64_t hid, int64_t inter) {
   if (w1 < grid) grid = w1;
   pl.grid = (int)grid;
   // sync words, then the h slice counters, then the split-K tile counters
-  pl.counter_bytes = round256(256 + (size_t)(pl.kbt[1] + pl.tiles[0] + pl.tiles[1]) * 4);
+  pl.counter_bytes = kCounterArea;   // sync words, h-slice counters and tile counters fit in it
   pl.ws_bytes = pl.counter_bytes;
   for (int g = 0; g < 2; ++g) {
     pl.whole[g] = (int)(pl.tiles[g] / grid);
@@ -688,8 +688,12 @@ cudaError_t launch_nt(const Plan &pl, const MlpDecodeParams &q, cudaStream_t st)
 }  // namespace
 
 bool mlp_decode_supported(int64_t m, int64_t hidden, int64_t inter) {
-  return m >= 1 && m <= 64 && hidden >= 128 && hidden % 128 == 0 && inter >= 64 && inter % 64 == 0 &&
-         hidden < (1 << 24) && inter < (1 << 24);
+  if (!(m >= 1 && m <= 64 && hidden >= 128 && hidden % 128 == 0 && inter >= 64 && inter % 64 == 0 &&
+        hidden < (1 << 24) && inter < (1 << 24)))
+    return false;
+  // sync words, then one counter per down_proj k-block (h slice) and per tile of both GEMMs
+  const int64_t words = 64 + (inter + BK - 1) / BK + 2 * inter / 128 + hidden / 128;
+  return words <= kCounterSlots;
 }
 
 size_t mlp_decode_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {

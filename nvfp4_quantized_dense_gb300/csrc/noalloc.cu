@@ -77,7 +77,10 @@ extern "C" nvfp4_status nvfp4_gemm_decode_noalloc(const uint8_t *a_fp4, const ui
   // The array keeps whatever the previous call left; the arrival counters at
   // its start must begin at zero.
   if (need > 0) {
-    const size_t counter_bytes = ((size_t)((n + 127) / 128) * 4 + 255) / 256 * 256;
+    // (the kernel's counters: one per 128-row weight tile at most, at the
+    // front of the counter area)
+    const size_t used = ((size_t)((n + 127) / 128) * 4 + 255) / 256 * 256;
+    const size_t counter_bytes = used < kCounterArea ? used : kCounterArea;
     if (cudaMemsetAsync(scratch, 0, counter_bytes, st) != cudaSuccess) return NVFP4_ERR_CUDA;
   }
   return launch_swapab(TC_W4A4, a_fp4, a_sf, b_fp4, b_sf, alpha, nullptr, d, nullptr, nullptr, m, n,

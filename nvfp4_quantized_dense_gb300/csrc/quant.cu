@@ -132,8 +132,11 @@ __global__ void __launch_bounds__(kTileThreads) silu_mul_quantize_kernel(
     float g[16], u[16], h[16];
     load16_bf16(gate_up + row * 2 * inter + col * 16, g);
     load16_bf16(gate_up + row * 2 * inter + inter + col * 16, u);
+    // the fast exponential and division, as the fused GEMM epilogues: h is
+    // within ~1e-6 relative of the correctly rounded one, far inside the
+    // requantize tolerance, and the kernel stays bound by HBM, not the ALUs
 #pragma unroll
-    for (int i = 0; i < 16; ++i) h[i] = silu_mul(g[i], u[i]);
+    for (int i = 0; i < 16; ++i) h[i] = silu_mul_fast(g[i], u[i]);
     uint32_t lo, hi;
     sf = quantize_block16(h, gs, lo, hi);
     *reinterpret_cast<uint2 *>(out_fp4 + row * (inter >> 1) + col * 8) = make_uint2(lo, hi);

@@ -328,9 +328,11 @@ def test_w4a16_small_shapes(lib, m, n, k, algo):
     print(f"w4a16 algo={algo} m={m} n={n} k={k}: rel err {err:.2e}")
 
 
-# split-K along K (workspace given): tiles shared by 2..5 CTAs, ragged tails
+# split-K along K (workspace given): tiles shared by 2..5 CTAs, ragged tails;
+# the last three are 128- and 256-token tiles with too few weight tiles for
+# whole tiles per CTA (128- and 256-token tiles, several token tiles)
 W4A16_SPLIT = [(1, 256, 512), (5, 96, 320), (16, 1024, 256), (33, 128, 1024), (64, 384, 2048),
-               (16, 2048, 4096), (3, 160, 640)]
+               (16, 2048, 4096), (3, 160, 640), (100, 640, 2048), (128, 1024, 1024), (300, 768, 512)]
 
 
 @pytest.mark.parametrize("m,n,k", W4A16_SPLIT)
@@ -348,7 +350,7 @@ def test_w4a16_split_k_small_shapes(lib, m, n, k):
 @pytest.mark.parametrize("which", ["gate_up", "down"])
 @pytest.mark.parametrize("m,algo,split", [(1, GEMV, False), (16, GEMV, False), (1, TC, False), (16, TC, False),
                                           (1, TC, True), (16, TC, True), (64, TC, True), (128, TC, False),
-                                          (1024, TC, False)])
+                                          (1024, TC, False), (128, TC, True), (1024, TC, True)])
 def test_w4a16_full_size_sampled(lib, m, which, algo, split):
     ws = weights(4, which)
     if which == "gate_up":

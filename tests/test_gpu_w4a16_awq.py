@@ -129,8 +129,9 @@ def test_prescaled_argument_errors(lib):
     x2 = torch.zeros((m2, k), dtype=torch.bfloat16, device="cuda")
     d2 = torch.empty((m2, n), dtype=torch.bfloat16, device="cuda")
     need = lib.bf16_fp4_gemm_prescaled_workspace_bytes(m2, n, k, TC)
-    assert need == m2 * k * 2
-    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    xs_bytes = (m2 * k * 2 + 255) // 256 * 256           # the scaled activations come first
+    assert need == xs_bytes + lib.bf16_fp4_gemm_workspace_bytes(m2, n, k, TC)
+    small = torch.empty(xs_bytes - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(lib.Nvfp4Error) as e:
-        lib.bf16_fp4_gemm_prescaled(x2, s[:k], w, sfo, a, d2, m2, n, k, small, need - 16, algo=TC)
+        lib.bf16_fp4_gemm_prescaled(x2, s[:k], w, sfo, a, d2, m2, n, k, small, xs_bytes - 16, algo=TC)
     assert e.value.status == lib.ERR_INVALID_ARG

@@ -2,13 +2,17 @@
 against the scratch sizes the library reports (no GPU needed: without a
 device the library plans for 148 SMs; with one, for the device's count).
 
-Swap-AB GEMM (weights as the MMA's 128-row operand, 256-wide k-blocks):
+Every workspace starts with a fixed 64 KiB area holding the arrival counters
+(no kernel's partials overlap it, so GEMMs of different shapes may share a
+workspace).  Swap-AB GEMM (weights as the MMA's 128-row operand, 256-wide
+k-blocks):
 every CTA takes floor(tiles/grid) whole tiles, the other tiles are cut into
 one contiguous run of (tile, k-block) pairs per CTA, and when those shared
 tiles have fewer k-blocks than there are CTAs one round of whole tiles joins
 them.  W4A16 tensor-core GEMM (k-blocks 128 wide up to 32 tokens, the last
 one possibly 64 wide; 64 wide above): one contiguous run per CTA up to 64
-tokens.  The scratch is a 256-byte-rounded counter per tile plus
+tokens, and above when whole tiles would leave SMs idle.  The scratch is the
+counter area plus
 [grid][fragment slots][tokens padded][128] fp32 partials, only when a tile is
 shared.  The whole-MLP decode kernel plans both of its GEMM phases the
 swap-AB way on one grid (the smaller of the SM count and either phase's
@@ -37,6 +41,11 @@ def sm_count():
     if torch.cuda.is_available():
         return torch.cuda.get_device_properties(0).multi_processor_count
     return 148
+
+
+# Every split-K workspace starts with a fixed 64 KiB counter area that no
+# kernel's partials overlap, so calls of different shapes can share one.
+COUNTER_AREA = 64 * 1024
 
 
 def r256(b):
@@ -71,21 +80,24 @@ def swapab_plan(m, n, k, sms, clusters=True):
     per = math.ceil(units / grid)
     maxfrag = math.ceil(per / kbt) + 1
     shared = units % grid != 0 or (units // grid) % kbt != 0
-    ws = r256(tiles * 4) + grid * maxfrag * nt * 128 * 4 if shared else 0
+    ws = COUNTER_AREA + grid * maxfrag * nt * 128 * 4 if shared else 0
     return dict(nt=nt, tiles=tiles, kbt=kbt, grid=grid, whole=whole, split=split, ws=ws, cl=1)
 
 
 def w4a16_ws(m, n, k, sms):
     nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128 if m <= 128 else 256
-    if nt > 64:
-        return 0
     bk = 128 if nt <= 32 else 64            # k-block width: 128 up to 32 tokens
     tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), math.ceil(k / bk)
+    rounds = math.ceil(tiles / sms)
+    if nt > 64 and tiles * 100 >= rounds * sms * 80:    # whole tiles fill the rounds
+        return 0
     w = tiles * nkb
     grid = min(w, sms)
     maxfrag = math.ceil(math.ceil(w / grid) / nkb) + 1
     shared = w % grid != 0 or (w // grid) % nkb != 0
-    return r256(tiles * 4) + grid * maxfrag * nt * 128 * 4 if shared else 0
+    if tiles > COUNTER_AREA // 4:
+        return 0
+    return COUNTER_AREA + grid * maxfrag * nt * 128 * 4 if shared else 0
 
 
 SWAP_CASES = [
@@ -150,7 +162,8 @@ def mlp_decode_ws(m, hid, inter, sms):
     tiles = [2 * inter // 128, hid // 128]
     kbt = [math.ceil(hid / 256), math.ceil(inter / 256)]
     grid = min(tiles[0] * kbt[0], tiles[1] * kbt[1], sms)
-    ws = r256(256 + (kbt[1] + tiles[0] + tiles[1]) * 4)
+    assert 256 + (kbt[1] + tiles[0] + tiles[1]) * 4 <= COUNTER_AREA
+    ws = COUNTER_AREA
     for g in range(2):
         whole = tiles[g] // grid
         split = tiles[g] - whole * grid
@@ -168,7 +181,8 @@ def test_mlp_decode_scratch_matches_plan(lib, m, hid, inter):
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 34816, 5120), (16, 34816, 5120), (16, 5120, 17408), (64, 384, 2048),
-                                   (33, 128, 1024), (5, 96, 320), (128, 34816, 5120), (1024, 34816, 5120)])
+                                   (33, 128, 1024), (5, 96, 320), (128, 34816, 5120), (1024, 34816, 5120),
+                                   (128, 5120, 17408), (1024, 5120, 17408), (300, 4096, 512)])
 def test_w4a16_scratch_matches_plan(lib, m, n, k):
     assert nv.bf16_fp4_gemm_workspace_bytes(m, n, k, nv.ALGO_TC) == w4a16_ws(m, n, k, sm_count())
 
@@ -268,13 +282,13 @@ def test_swapab_reduction_bookkeeping_random_shapes():
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 34816, 5120), (16, 34816, 5120), (16, 5120, 17408), (64, 384, 2048),
-                                   (33, 128, 1024), (5, 96, 320), (64, 7168, 18432)])
+                                   (33, 128, 1024), (5, 96, 320), (64, 7168, 18432), (128, 5120, 17408),
+                                   (1024, 5120, 17408)])
 @pytest.mark.parametrize("sms", [148, 152, 7])
 def test_w4a16_reduction_bookkeeping(m, n, k, sms):
-    """The W4A16 split-K (one contiguous run per CTA over all tiles, up to 64
-    tokens) keeps the same invariants as the swap-AB mixed split with no
-    whole tiles."""
-    nt = 16 if m <= 16 else 32 if m <= 32 else 64
+    """The W4A16 split-K (one contiguous run per CTA over all tiles) keeps
+    the same invariants as the swap-AB mixed split with no whole tiles."""
+    nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128 if m <= 128 else 256
     bk = 128 if nt <= 32 else 64
     tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), math.ceil(k / bk)
     grid = min(tiles * nkb, sms)
