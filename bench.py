@@ -67,6 +67,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--only", default=None, help="comma-separated workload keys (default: all four)")
+    p.add_argument("--m", type=int, default=None, help="one batch size instead of each workload's M list")
     p.add_argument("--algo", default="auto", choices=["auto", "gemv", "tc", "tc1sm", "swapab"],
                    help="W4A4 GEMM kernel family (auto: the library's choice by M; tc: CTA pairs with 2-SM "
                         "MMAs; tc1sm: one CTA per tile)")
@@ -353,7 +354,7 @@ def run_ours(args, world, rank, local):
         fam = synth.WEIGHT_SOURCE.get(wid, wid)
         it = W()
         it.key, it.wid, it.title, it.spec = key, wid, title, spec
-        it.hid, it.inter, it.ms = spec.hidden, spec.inter, tuple(spec.ms)
+        it.hid, it.inter, it.ms = spec.hidden, spec.inter, ((args.m,) if args.m else tuple(spec.ms))
         it.w4a16 = spec.mode == "w4a16"
         it.gu = weights[(fam, "gate_up", "plain" if it.w4a16 else "interleaved")]
         it.gu_plain = weights.get((fam, "gate_up", "plain")) if wid == 1 else None
@@ -506,12 +507,14 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed_steps")       # (for profiler launch lists of exactly these steps)
     with torch.cuda.stream(stream):
         t_start.record()
         for i in range(args.steps):
             step(i)
         t_end.record()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier()
     step_ms = t_start.elapsed_time(t_end) / args.steps
 
@@ -624,6 +627,13 @@ def run_ours(args, world, rank, local):
                 t = r[f"{which}_us"]
                 if dom is None or t > dom[0]:
                     dom = (t, it, m, which)
+    # DRAM bytes (read + write) per launch of the step's GEMMs from an ncu
+    # capture of this bench's own timed step (default workloads, one pass per
+    # launch): reported as the roofline's traffic when that launch is the
+    # dominant one; to be removed whenever the kernel changes before it is
+    # captured again
+    measured_traffic = {("prefill_h7168", 8192, "gate_up"): 352.4e6,
+                        ("prefill_h7168", 8192, "down"): 658.2e6}
     roofline = None
     if dom is not None:
         t_us, it, m, which = dom
@@ -647,6 +657,9 @@ def run_ours(args, world, rank, local):
         roofline["kernel"] = (f"{'nvfp4_gemm_swiglu_quant' if fused else ('bf16_fp4_gemm' if it.w4a16 else 'nvfp4_gemm')} "
                               f"{which} ({it.key}, M={m})")
         roofline["us_per_launch"] = t_us
+        roofline["traffic"] = measured_traffic.get((it.key, m, which))
+        if roofline["traffic"] is not None:
+            roofline["traffic_unit"] = "DRAM bytes read + written per launch (ncu, the bench's timed step)"
         roofline["timing"] = (f"{REPS} launches back to back in one CUDA graph (weight copies rotating), CUDA "
                               "events on the launching stream around 3 replays")
 
