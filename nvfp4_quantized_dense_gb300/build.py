@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libnvfp4mlp.so")
 
-UNITS = ["api.cu", "quant.cu", "gemv.cu", "gemm_tc.cu", "gemm_swapab.cu", "gemm_w4a16.cu", "noalloc.cu", "mlp_decode.cu"]
+UNITS = ["api.cu", "quant.cu", "gemv.cu", "gemm_tc.cu", "gemm_swapab.cu", "gemm_w4a16.cu", "gemm_w4a16_tmem.cu", "noalloc.cu", "mlp_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast-math: the quantize recipe relies on IEEE division and multiplication.
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -299,19 +299,23 @@ nvfp4_status w4a16_impl(const uint16_t *a, const uint16_t *pre_scale, const uint
   if (!w4a16_tc_supported(m, n, k)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (workspace && !aligned16(workspace)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (pre_scale) {
-    // The tensor-core kernel's converter warps are its critical path, and
-    // every weight tile reads the same activations: scale them once, into the
-    // front of the workspace, in a pass of their own.
+    // Every weight tile reads the same activations: they are scaled once,
+    // in a pass of their own -- by the TMEM kernel's f16 pre-pass, or else
+    // into the front of the workspace by bf16_awq_prescale (the shared-memory
+    // kernel's converter warps are its critical path).
     const size_t xs_bytes = round256((size_t)(m * k * 2));
     if (!workspace || ws_bytes < xs_bytes) return NVFP4_ERR_INVALID_ARG;
     uint16_t *xs = static_cast<uint16_t *>(workspace);
-    if (cudaError_t e = launch_awq_prescale(a, pre_scale, m, k, xs, st)) return from_cuda(e);
-    a = xs;
     workspace = static_cast<uint8_t *>(workspace) + xs_bytes;
     ws_bytes -= xs_bytes;
+    if (!w4a16_uses_tmem(m, n, k, ws_bytes ? workspace : nullptr, ws_bytes)) {
+      if (cudaError_t e = launch_awq_prescale(a, pre_scale, m, k, xs, st)) return from_cuda(e);
+      a = xs;
+      pre_scale = nullptr;
+    }
   }
   if (ws_bytes == 0) workspace = nullptr;
-  return from_cuda(launch_w4a16_tc(a, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes,
+  return from_cuda(launch_w4a16_tc(a, pre_scale, b_fp4, b_sf, alpha, d, m, n, k, workspace, ws_bytes,
                                    g_wait_limit.load(), st));
 }
 }  // namespace

@@ -523,7 +523,7 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
       }))
     return e;
   CUtensorMap tm_w, tm_x;
-  if (!make_byte_map(&tm_w, w, n, k / 2, 128, 128, true) || !make_byte_map(&tm_x, x, m, k / 2, 128, NT, true))
+  if (!make_byte_map(&tm_w, w, n, k / 2, 128, 128, 128) || !make_byte_map(&tm_x, x, m, k / 2, 128, NT, 128))
     return cudaErrorInvalidValue;
   SwapArgs a{};
   a.sfw = w_sf;

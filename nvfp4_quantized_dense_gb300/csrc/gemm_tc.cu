@@ -594,7 +594,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }  // namespace
 
 bool make_byte_map(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t row_bytes, uint32_t box_bytes,
-                   uint32_t box_rows, bool swizzle128) {
+                   uint32_t box_rows, int swizzle_bytes) {
   auto encode = get_encode();
   if (!encode) return false;
   cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
@@ -603,7 +603,9 @@ bool make_byte_map(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t row_b
   cuuint32_t estr[2] = {1u, 1u};
   return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE,
-                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                      : CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -662,7 +664,7 @@ cudaError_t launch_mode(const uint8_t *a, const uint8_t *a_sf, const uint8_t *b,
   CUtensorMap tm_a, tm_b;
   // codes [rows, k/2] bytes; box 128 bytes of K x 128 rows (activation rows
   // or half a weight tile), 128-byte swizzle
-  if (!make_byte_map(&tm_a, a, m, k / 2, 128, BM, true) || !make_byte_map(&tm_b, b, n, k / 2, 128, 128, true))
+  if (!make_byte_map(&tm_a, a, m, k / 2, 128, BM, 128) || !make_byte_map(&tm_b, b, n, k / 2, 128, 128, 128))
     return cudaErrorInvalidValue;
   TcArgs args{a_sf, b_sf, alpha, out_gs, d, out_fp4, out_sf, (int32_t)m, (int32_t)n, (int32_t)k,
               (int32_t)((m + BM - 1) / BM), (int32_t)((n + BN - 1) / BN), 0, wait_limit, device_status_ptr(), rs};

@@ -552,8 +552,6 @@ __global__ void __launch_bounds__(kThreads, 1)   // 16 warps: at most 128 regist
 
 int pick_nt(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : m <= 128 ? 128 : 256; }
 
-size_t round256(size_t b) { return (b + 255) / 256 * 256; }
-
 // Work split of one call: split-K over (tile, k-block) pairs for up to 64
 // tokens (one token tile), and above when whole tiles fill less than 80 % of
 // the rounds of one CTA per SM; whole tiles otherwise.
@@ -601,7 +599,7 @@ cudaError_t launch_nt(const Plan &pl, const uint16_t *x, const uint8_t *w, const
   CUtensorMap tm_x, tm_w;
   // activations bf16 [m, k]: box 128 bytes (64 elements) x NT rows, 128-byte swizzle
   // weight codes [n, k/2]: box BK/2 bytes x 128 rows, no swizzle
-  if (!make_byte_map(&tm_x, x, m, k * 2, 128, NT, true) || !make_byte_map(&tm_w, w, n, k / 2, C::BK / 2, 128, false))
+  if (!make_byte_map(&tm_x, x, m, k * 2, 128, NT, 128) || !make_byte_map(&tm_w, w, n, k / 2, C::BK / 2, 128, 0))
     return cudaErrorInvalidValue;
   W4A16Args a{};
   a.wsf = wsf;
@@ -643,13 +641,21 @@ bool w4a16_tc_supported(int64_t m, int64_t n, int64_t k) {
 
 size_t w4a16_workspace_bytes(int64_t m, int64_t n, int64_t k) {
   if (!w4a16_tc_supported(m, n, k)) return 0;
+  if (w4a16_tmem_supported(m, n, k)) return w4a16_tmem_workspace_bytes(m, n, k);
   return make_plan(m, n, k).ws_bytes;
 }
 
-cudaError_t launch_w4a16_tc(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, const float *alpha,
-                            uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws, size_t ws_bytes,
-                            uint32_t wait_limit, cudaStream_t st) {
+bool w4a16_uses_tmem(int64_t m, int64_t n, int64_t k, const void *ws, size_t ws_bytes) {
+  return w4a16_tmem_supported(m, n, k) && ws != nullptr && ws_bytes >= w4a16_tmem_workspace_bytes(m, n, k);
+}
+
+cudaError_t launch_w4a16_tc(const uint16_t *x, const uint16_t *pre_scale, const uint8_t *w, const uint8_t *wsf,
+                            const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws,
+                            size_t ws_bytes, uint32_t wait_limit, cudaStream_t st) {
   if (!w4a16_tc_supported(m, n, k)) return cudaErrorNotSupported;
+  if (w4a16_uses_tmem(m, n, k, ws, ws_bytes))
+    return launch_w4a16_tmem(x, pre_scale, w, wsf, alpha, d, m, n, k, ws, ws_bytes, wait_limit, st);
+  if (pre_scale) return cudaErrorInvalidValue;   // the caller scales the activations for this kernel
   const Plan pl = make_plan(m, n, k);
   switch (pl.nt) {
     case 16: return launch_nt<16>(pl, x, w, wsf, alpha, d, m, n, k, ws, ws_bytes, wait_limit, st);

@@ -1,0 +1,705 @@
+// W4A16 GEMM at decode sizes (up to 64 tokens): bf16 activations x NVFP4
+// weights ([P3] fp4_gemm with quant_mode "w4a16"), the dequantized weight
+// tiles held in tensor memory.
+//
+// Why TMEM.  A 128-row x 128-wide block of weights is 9 KB of codes and
+// scales in HBM but 32 KB once dequantized to 16 bits.  Written to shared
+// memory and read back by the MMA it costs 64 KB of shared-memory traffic per
+// 9 KB streamed, more than an SM's shared memory carries at its share of the
+// HBM bandwidth.  Here each converter thread dequantizes one weight row into
+// registers and stores it with tcgen05.st into TMEM, and the MMA takes its A
+// operand (the weights, M = 128) from there; only the activations (B, N = the
+// token tile) come from shared memory.
+//
+// Operand type f16.  E2M1 -> f16 is one conversion per two codes and the
+// UE4M3 scale one f16x2 multiply, both exact: the product has at most 6
+// significant bits and lies in f16's normal range (2^-11 .. 2688).  A
+// pre-pass turns each token row of the bf16 activations into f16 times a
+// power of two 2^e that brings the row's largest finite magnitude into
+// [2^15, 2^16): every element within 2^30 of that magnitude converts
+// exactly (smaller ones are f16 subnormals, rounded by at most 2^-25 in the
+// scaled units).  The MMA's products and fp32 sums are then those of the bf16
+// operands times 2^e, and the epilogue applies alpha and then 2^-e, so the
+// output is the bf16 computation's (a power-of-two scale commutes with every
+// rounding, barring underflow).
+//
+// Pipeline.  A k-block is 256 wide: the weight codes arrive as 128-byte rows
+// (whole 128-byte lines per weight row and request; 64-byte rows measured
+// about 72 % of the copy bandwidth in steady state), 128-byte swizzled so
+// that a thread reads its own row without bank conflicts.  Weights (codes and
+// the 128x4 scale tiles) and the f16 activation tiles travel in rings of
+// their own: a weight stage is released as soon as the converters hold its
+// codes in registers, so nearly the whole weight ring is in flight from HBM,
+// and the weights stream (and are dequantized into TMEM) while the
+// activation pre-pass is still running.  A k-block is dequantized in two
+// 128-wide halves into 64-column TMEM slots after the accumulators.
+//
+// Work split (as the swap-AB kernel's mixed split): every CTA owns `whole`
+// whole weight tiles, done last so that no CTA ends its run with a
+// reduction; the other tiles are cut into one contiguous run of (tile,
+// k-block) pairs per CTA, a tile shared by CTAs finished by the last to
+// arrive, which sums the fp32 partials in K order.
+//
+// Roles (768 threads, one CTA per SM): warp 0 weight producer, warp 3
+// activation producer, warps 1 (also TMEM owner) and 2 the MMA issuers of
+// halves 0 and 1 (at decode sizes one thread issuing every MMA would bound
+// the kernel), each accumulating into its own TMEM columns; warps 4..19
+// converters, one per (half, 64-wide quarter, TMEM lane quarter): warp w
+// writes TMEM lanes 32(w%4) .. 32(w%4)+31 (the lanes a warp may access), one
+// weight row per thread, and every converter warp visits every k-block, so
+// no ring barrier's phase is ambiguous (conversion is latency-bound: four
+// converter warps per SM sub-partition hide what two cannot); warps 20..23
+// epilogue, adding the two issuers' accumulators.  Every wait is bounded as
+// in the other tensor-core kernels.
+#include <cfloat>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "splitk.cuh"
+#include "tc_ptx.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kThreads = 768;
+constexpr int kWarpProdW = 0, kWarpMma0 = 1, kWarpMma1 = 2, kWarpProdX = 3;
+constexpr int kFirstConv = 4;
+constexpr int kFirstEpi = kFirstConv + 16;   // warps 20..23
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint32_t kDrainPolls = 1u << 22;
+constexpr int kBK = 256;                    // K per k-block
+constexpr int kSub = kBK / 64;              // 64-wide sub-blocks per k-block (one scale tile each)
+
+template <int NT>
+struct TCfg {
+  static constexpr uint32_t SUB_X = NT * 128;                   // NT rows x 64 f16, 128-byte swizzle
+  static constexpr uint32_t X_BYTES = kSub * SUB_X;             // one activation stage
+  static constexpr uint32_t WC_BYTES = 128 * kBK / 2;           // 128 rows x 128 bytes of codes
+  static constexpr uint32_t WS_BYTES = kSub * 512;              // 128x4 scale tiles
+  static constexpr uint32_t W_BYTES = WC_BYTES + WS_BYTES;      // one weight stage (a multiple of 1024)
+  static constexpr int XSTAGES = NT <= 32 ? 4 : 3;
+  static constexpr uint32_t BAR_BYTES = 1024;
+  static constexpr int WSTAGES_FIT = (int)((224u * 1024 - XSTAGES * X_BYTES - BAR_BYTES - 1024) / W_BYTES);
+  static constexpr int WSTAGES = WSTAGES_FIT > 16 ? 16 : WSTAGES_FIT;
+  static constexpr uint32_t ACC_COLS = 2 * 2 * NT;              // two tile buffers x two issuers
+  static constexpr uint32_t A_COLS = kBK / 4;                   // f16 pairs of one half k-block row
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int DSTAGES = (int)((TMEM_COLS - ACC_COLS) / A_COLS) / 2 * 2;
+  static constexpr uint32_t SMEM_BYTES = XSTAGES * X_BYTES + WSTAGES * W_BYTES + BAR_BYTES + 1024;
+  static_assert(W_BYTES % 1024 == 0 && X_BYTES % 1024 == 0, "stage alignment for the swizzles");
+  static_assert(DSTAGES >= 2 && DSTAGES % 2 == 0, "dequantized halves: slot parity = half");
+  static_assert(WSTAGES >= 4, "weight ring depth");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert((2 * WSTAGES + 2 * XSTAGES + 2 * DSTAGES + 6) * 8 + 16 <= BAR_BYTES, "barrier area");
+};
+
+struct TArgs {
+  const uint8_t *wsf;      // swizzled scales over N rows
+  const float *alpha;
+  const float *rs;         // [m] 2^-e of each token row
+  uint16_t *d;             // bf16 [M, N]
+  float *partials;         // [grid][maxfrag][NT][128] fp32 (tiles shared by CTAs)
+  int *counters;           // [split tiles] arrival counters
+  int32_t m, n, k;
+  int32_t wtiles, nkb;
+  int32_t grid, maxfrag, whole, split_tiles;
+  uint32_t wait_limit;
+  int *status;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// Eight E2M1 codes (one word, element i in nibble i) times an f16x2 scale ->
+// four f16x2 (elements 2i, 2i+1 in word i, the lower index in the low half).
+__device__ __forceinline__ void dequant8_f16(uint32_t codes, uint32_t scale_h2, uint32_t *out) {
+  uint32_t h[4];
+  asm("{\n"
+      ".reg .b8 b0, b1, b2, b3;\n"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n"
+      "}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(codes));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[i]) : "r"(h[i]), "r"(scale_h2));
+}
+
+// Two UE4M3 scale bytes (low byte first) -> each one as f16 in both halves.
+__device__ __forceinline__ void scales_to_h2(uint32_t two, uint32_t &s0, uint32_t &s1) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two));
+  s0 = __byte_perm(r, 0, 0x1010);
+  s1 = __byte_perm(r, 0, 0x3232);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a16_tmem_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                      const TArgs p) {
+  using C = TCfg<NT>;
+  constexpr int WST = C::WSTAGES, XST = C::XSTAGES, DST = C::DSTAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  auto st_x = [&](int r) { return base + r * C::X_BYTES; };
+  auto st_wc = [&](int r) { return base + XST * C::X_BYTES + r * C::W_BYTES; };
+  auto st_ws = [&](int r) { return st_wc(r) + C::WC_BYTES; };
+  uint64_t *wfull = reinterpret_cast<uint64_t *>(base + XST * C::X_BYTES + WST * C::W_BYTES);
+  uint64_t *wempty = wfull + WST;
+  uint64_t *xfull = wempty + WST;
+  uint64_t *xempty = xfull + XST;
+  uint64_t *dfull = xempty + XST;
+  uint64_t *dempty = dfull + DST;
+  uint64_t *tfull = dempty + DST;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
+  volatile int *last_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int r = 0; r < WST; ++r) {
+      ptx::mbar_init(&wfull[r], 1);
+      ptx::mbar_init(&wempty[r], 16);      // every converter warp, once it holds its codes
+    }
+    for (int r = 0; r < XST; ++r) {
+      ptx::mbar_init(&xfull[r], 1);
+      ptx::mbar_init(&xempty[r], 2);       // one commit per issuer
+    }
+    for (int d = 0; d < DST; ++d) {
+      ptx::mbar_init(&dfull[d], 8);        // the eight warps converting a half
+      ptx::mbar_init(&dempty[d], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&tfull[b], 2);        // one commit per issuer
+      ptx::mbar_init(&tempty[b], 128);
+      ptx::mbar_init(&drain[b], 1);
+    }
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tm_x);
+    ptx::prefetch_tensormap(&tm_w);
+  }
+  // The weight producer (warp 0, whose thread 0 initialized the barriers)
+  // starts streaming at once; the others wait until the barriers and the
+  // TMEM allocation are in place.
+  uint32_t tmem = 0;
+  if (warp == kWarpProdW) {
+    __syncwarp();
+    asm volatile("bar.arrive 1, %0;" ::"r"(kThreads) : "memory");
+  } else {
+    if (warp == kWarpMma0) {
+      ptx::tmem_alloc(tslot, C::TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory");
+    ptx::tc_fence_after();
+    tmem = *tslot;
+  }
+  auto a_col = [&](int d) { return C::ACC_COLS + (uint32_t)d * C::A_COLS; };
+
+  const int cp4 = p.k >> 6;              // 512-byte scale tiles per 128-row block
+  auto nsub_of = [&](int kb) { return min(kSub, cp4 - kb * kSub); };
+  // 64-wide sub-blocks of half h of k-block kb (0, 1 or 2)
+  auto nsub_half = [&](int kb, int h) { return min(2, max(0, nsub_of(kb) - 2 * h)); };
+  const MixedPartition mixed{p.nkb, p.grid, p.whole, p.split_tiles};
+  const uint32_t limit = p.wait_limit;
+  uint32_t issued_w = 0, issued_w_par = 0, issued_x = 0, issued_x_par = 0;
+  bool mma_issued = false;
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+  };
+
+  if (warp == kWarpProdW) {
+    // ---------------------------------------------------- weight producer
+    if (ptx::elect_one()) {
+      const uint64_t pol_w = ptx::l2_policy_evict_first();
+      int r = 0;
+      uint32_t ph = 0;
+      MixedIter mi(mixed, blockIdx.x);
+      int tile, kb0, kb1;
+      bool ok = true;
+      while (ok && !*abort_flag && mi.next(tile, kb0, kb1)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_bounded(&wempty[r], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          const uint32_t sfb = (uint32_t)nsub_of(kb) * 512u;   // scales only of the sub-blocks K has
+          ptx::mbar_arrive_expect_tx(&wfull[r], C::WC_BYTES + sfb);
+          ptx::tma_load_2d(st_wc(r), &tm_w, &wfull[r], kb * (kBK / 2), tile * 128, pol_w);
+          ptx::bulk_load(st_ws(r), p.wsf + ((size_t)tile * cp4 + kb * kSub) * 512, sfb, &wfull[r], pol_w);
+          issued_w |= 1u << r;
+          issued_w_par = (issued_w_par & ~(1u << r)) | (ph << r);
+          if (++r == WST) { r = 0; ph ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == kWarpProdX) {
+    // ------------------------------------------------ activation producer
+    pdl_wait();                          // the pre-pass wrote the f16 activations
+    if (ptx::elect_one()) {
+      const uint64_t pol_x = ptx::l2_policy_evict_last();
+      int r = 0;
+      uint32_t ph = 0;
+      MixedIter mi(mixed, blockIdx.x);
+      int tile, kb0, kb1;
+      bool ok = true;
+      while (ok && !*abort_flag && mi.next(tile, kb0, kb1)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_bounded(&xempty[r], ph ^ 1u, limit, kTimeoutNs, abort_flag)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&xfull[r], C::X_BYTES);
+#pragma unroll
+          for (int sb = 0; sb < kSub; ++sb)   // a sub-block past K reads zeros
+            ptx::tma_load_2d(st_x(r) + sb * C::SUB_X, &tm_x, &xfull[r], (kb * kSub + sb) * 128, 0, pol_x);
+          issued_x |= 1u << r;
+          issued_x_par = (issued_x_par & ~(1u << r)) | (ph << r);
+          if (++r == XST) { r = 0; ph ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+    // ----------------------------------------------------------------- MMA
+    // issuer h issues half h of every k-block
+    const int h = warp == kWarpMma0 ? 0 : 1;
+    if (ptx::elect_one()) {
+      // kind::f16: F32 accumulator (bits 4-5 = 1), A = B = F16 (0), K-major,
+      // N >> 3 in bits 17-22, M = 128 >> 4 in bits 24-28
+      constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | (8u << 24);
+      int xr = 0, it = 0, i = 0;
+      uint32_t xph = 0;
+      MixedIter mi(mixed, blockIdx.x);
+      int tile, kb0, kb1;
+      bool ok = true;
+      for (; ok && !*abort_flag && mi.next(tile, kb0, kb1); ++it) {
+        const int ab = it & 1;
+        if (!ptx::mbar_wait_bounded(&tempty[ab], (uint32_t)((it >> 1) & 1) ^ 1u, limit, kTimeoutNs, abort_flag)) {
+          give_up();
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)((ab * 2 + h) * NT);
+        bool first = true;
+        for (int kb = kb0; kb < kb1; ++kb, ++i) {
+          const int j = 2 * i + h, d = j % DST;
+          const uint32_t dph = (uint32_t)((j / DST) & 1);
+          bool got = ptx::mbar_wait_bounded(&dfull[d], dph, limit, kTimeoutNs, abort_flag);
+          if (got) got = ptx::mbar_wait_bounded(&xfull[xr], xph, limit, kTimeoutNs, abort_flag);
+          if (!got) {
+            give_up();
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t xs = ptx::smem_u32(st_x(xr)) + (uint32_t)(2 * h) * C::SUB_X;
+          const uint32_t wa = tmem + a_col(d);
+          const int ns = nsub_half(kb, h);
+          for (int sb = 0; sb < ns; ++sb)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              ptx::mma_f16_tmem_a(acc, wa + 8 * (4 * sb + jj),
+                                  ptx::smem_desc(xs + sb * C::SUB_X + 32 * jj, 16, 1024, 2), idesc, !first);
+              first = false;
+            }
+          mma_issued = true;
+          ptx::tc_commit(&dempty[d]);
+          ptx::tc_commit(&xempty[xr]);
+          if (++xr == XST) { xr = 0; xph ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::tc_commit(&tfull[ab]);          // also when this issuer had nothing to add
+      }
+    }
+  } else if (warp < kFirstEpi) {
+    // ---------------------------------------------------------- converters
+    // warp (h, qt, q): half h, its 64-wide quarter qt (sub-block 2h + qt of
+    // the k-block, TMEM columns 32 qt .. 32 qt + 31 of the half's slot), TMEM
+    // lanes 32 q ..  A half's slot has the half's parity (DST is even).
+    const int cg = (warp - kFirstConv) >> 2;
+    const int h = cg >> 1, qt = cg & 1, q = warp & 3;
+    const int sb = 2 * h + qt;
+    const int row = 32 * q + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16) + 32u * qt;
+    const int swz = row & 7;                  // 128-byte swizzle: chunk c of the row sits at c ^ swz
+    const uint32_t sf_off = (uint32_t)(sb * 512 + (row & 31) * 16 + (row >> 5) * 4);
+    const uint32_t c_off = (uint32_t)(row * (kBK / 2));
+    MixedIter mi(mixed, blockIdx.x);
+    int tile, kb0, kb1;
+    int i = 0, wr = 0;
+    uint32_t wph = 0;
+    bool ok = true;
+    while (ok && mi.next(tile, kb0, kb1)) {
+      for (int kb = kb0; kb < kb1; ++kb, ++i) {
+        const int j = 2 * i + h, d = j % DST;
+        const uint32_t dph = (uint32_t)((j / DST) & 1);
+        bool got = ptx::mbar_wait_bounded(&dempty[d], dph ^ 1u, limit, kTimeoutNs, abort_flag);
+        if (got) got = ptx::mbar_wait_bounded(&wfull[wr], wph, limit, kTimeoutNs, abort_flag);
+        if (__any_sync(0xffffffffu, !got)) {   // the warp leaves together
+          give_up();
+          ok = false;
+          break;
+        }
+        const bool have = sb < nsub_of(kb);    // this quarter holds some of K
+        const uint8_t *crow = st_wc(wr) + c_off;
+        const uint4 c0 = *reinterpret_cast<const uint4 *>(crow + (((2 * sb) ^ swz) << 4));
+        const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + (((2 * sb + 1) ^ swz) << 4));
+        const uint32_t sw = *reinterpret_cast<const uint32_t *>(st_ws(wr) + sf_off);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&wempty[wr]);   // the stage's codes are read (release)
+        if (++wr == WST) { wr = 0; wph ^= 1u; }
+        if (have) {
+          // elements 0..31 of the quarter: scales 0 and 1; 32..63: scales 2 and 3
+          uint32_t s0, s1, s2, s3;
+          scales_to_h2(sw, s0, s1);
+          scales_to_h2(sw >> 16, s2, s3);
+          uint32_t o[16];
+          dequant8_f16(c0.x, s0, o);
+          dequant8_f16(c0.y, s0, o + 4);
+          dequant8_f16(c0.z, s1, o + 8);
+          dequant8_f16(c0.w, s1, o + 12);
+          ptx::tmem_st16(t_lane + a_col(d), o);
+          dequant8_f16(c1.x, s2, o);
+          dequant8_f16(c1.y, s2, o + 4);
+          dequant8_f16(c1.z, s3, o + 8);
+          dequant8_f16(c1.w, s3, o + 12);
+          ptx::tmem_st16(t_lane + a_col(d) + 16, o);
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&dfull[d]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int et = threadIdx.x - 32 * kFirstEpi;
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    const float alpha = __ldg(p.alpha);
+    constexpr int TG = 16;                   // tokens per pass
+    constexpr int MAXC = 2;                  // contributors' partials loaded together
+    int it = 0;
+    auto load_acc = [&](int ab, int c, bool p1, float (&o)[16]) {
+      uint32_t v[16];
+      const uint32_t a0 = t_row + (uint32_t)(ab * 2 * NT + 16 * c);
+      ptx::tmem_ld16(a0, v);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int x = 0; x < 16; ++x) o[x] = __uint_as_float(v[x]);
+      if (p1) {
+        ptx::tmem_ld16(a0 + NT, v);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 16; ++x) o[x] += __uint_as_float(v[x]);
+      }
+    };
+    // bf16(alpha * v * 2^-e) of token t (< m)
+    auto out_bits = [&](float v, int t) {
+      const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v * __ldg(p.rs + t));
+      return *reinterpret_cast<const uint16_t *>(&o);
+    };
+    MixedIter mi(mixed, blockIdx.x);
+    int tile, kb0, kb1;
+    const int mt = min(p.m, NT);
+    for (; mi.next(tile, kb0, kb1); ++it) {
+      const int ab = it & 1;
+      const bool got = ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag);
+      if (!got) give_up();
+      if (ptx::bar_any(2, 128, !got || *abort_flag)) break;   // the four warps leave together
+      ptx::tc_fence_after();
+      const int n = tile * 128 + row;
+      const bool p1 = nsub_of(kb0) > 2;      // half 1 of the fragment holds some of K
+      const bool split_tile = mixed.is_split(tile);
+      const int64_t c_first = split_tile ? mixed.cta_of((int64_t)tile * p.nkb) : blockIdx.x;
+      const int64_t c_last = split_tile ? mixed.cta_of((int64_t)tile * p.nkb + p.nkb - 1) : blockIdx.x;
+      if (c_last == c_first) {
+#pragma unroll 1
+        for (int c = 0; c < NT / 16; ++c) {
+          float v[16];
+          load_acc(ab, c, p1, v);
+          if (n < p.n) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+              if (16 * c + x < mt) p.d[(size_t)(16 * c + x) * p.n + n] = out_bits(v[x], 16 * c + x);
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&tempty[ab]);
+        continue;
+      }
+      // partial slot of contributor cc: its fragment index is 0 except for
+      // c_first (every later contributor's run starts inside this tile)
+      const int f_first = tile - (int)(mixed.start(c_first) / p.nkb);
+      auto slot = [&](int64_t cc) {
+        return p.partials + ((size_t)cc * p.maxfrag + (cc == c_first ? f_first : 0)) * NT * 128;
+      };
+      float *mine = slot(blockIdx.x);
+#pragma unroll 1
+      for (int c = 0; c < NT / 16; ++c) {
+        float v[16];
+        load_acc(ab, c, p1, v);
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          if (16 * c + x < mt) mine[(16 * c + x) * 128 + row] = v[x];
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[ab]);
+      epi_bar();                    // every partial write of the CTA precedes the release below
+      if (et == 0)
+        *last_flag = atom_add_acq_rel_gpu(&p.counters[tile], 1) == (uint32_t)(c_last - c_first);
+      epi_bar();
+      if (!*last_flag) continue;
+      if (et == 0) p.counters[tile] = 0;
+#pragma unroll 1
+      for (int g0 = 0; g0 < mt; g0 += TG) {
+        float acc[TG];
+#pragma unroll
+        for (int x = 0; x < TG; ++x) acc[x] = 0.0f;
+        for (int64_t c0 = c_first; c0 <= c_last; c0 += MAXC) {   // K order; MAXC loads in flight
+          float pv[MAXC][TG];
+#pragma unroll
+          for (int u = 0; u < MAXC; ++u) {
+            const bool have = c0 + u <= c_last;
+            const float *pc = slot(have ? c0 + u : c0) + (size_t)g0 * 128 + row;
+#pragma unroll
+            for (int x = 0; x < TG; ++x) pv[u][x] = (have && g0 + x < mt) ? __ldcg(pc + x * 128) : 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < MAXC; ++u)
+            if (c0 + u <= c_last) {
+#pragma unroll
+              for (int x = 0; x < TG; ++x) acc[x] += pv[u][x];
+            }
+        }
+        if (n < p.n) {
+#pragma unroll
+          for (int x = 0; x < TG; ++x)
+            if (g0 + x < mt) p.d[(size_t)(g0 + x) * p.n + n] = out_bits(acc[x], g0 + x);
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    volatile int no_abort = 0;
+    if (warp == kWarpProdW && issued_w) {
+      for (int r = 0; r < WST; ++r)
+        if (issued_w & (1u << r)) ptx::mbar_wait_bounded(&wfull[r], (issued_w_par >> r) & 1u, kDrainPolls, 0, &no_abort);
+    }
+    if (warp == kWarpProdX && issued_x) {
+      for (int r = 0; r < XST; ++r)
+        if (issued_x & (1u << r)) ptx::mbar_wait_bounded(&xfull[r], (issued_x_par >> r) & 1u, kDrainPolls, 0, &no_abort);
+    }
+    if ((warp == kWarpMma0 || warp == kWarpMma1) && mma_issued) {
+      uint64_t *dr = &drain[warp == kWarpMma0 ? 0 : 1];
+      ptx::tc_commit(dr);
+      ptx::mbar_wait_bounded(dr, 0, kDrainPolls, 0, &no_abort);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kWarpMma0) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// Token rows of x (times the AWQ pre-scale s when given, rounded to bf16 as
+// the separate multiply does) -> f16 x16 = x * 2^e with e per row bringing
+// the row's largest finite magnitude into [2^15, 2^16), and rs[row] = 2^-e.
+// One CTA per row; a row of up to kPrepThreads * kPrepVecs * 8 elements is
+// read once into registers (all loads in flight together), longer rows read
+// their remainder twice.
+constexpr int kPrepThreads = 1024, kPrepVecs = 4;
+
+__global__ void __launch_bounds__(kPrepThreads) w4a16_act_f16_kernel(const uint16_t *__restrict__ x,
+                                                                     const uint16_t *__restrict__ s, int64_t k,
+                                                                     uint16_t *__restrict__ x16,
+                                                                     float *__restrict__ rs) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[kPrepThreads / 32];
+  const int64_t row = blockIdx.x;
+  const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * k);
+  const uint4 *sr = reinterpret_cast<const uint4 *>(s);
+  const int n8 = (int)(k >> 3);
+  auto load = [&](int i) {
+    uint4 v = xr[i];
+    if (s) {
+      const uint4 sv = __ldg(sr + i);
+      v = make_uint4(bf16x2_mul(v.x, sv.x), bf16x2_mul(v.y, sv.y), bf16x2_mul(v.z, sv.z), bf16x2_mul(v.w, sv.w));
+    }
+    return v;
+  };
+  auto fmax_finite = [](float a, float v) { return fabsf(v) <= FLT_MAX ? fmaxf(a, fabsf(v)) : a; };
+  auto vmax = [&](float a, const uint4 &v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) a = fmax_finite(fmax_finite(a, bf16_lo(w[u])), bf16_hi(w[u]));
+    return a;
+  };
+  uint4 keep[kPrepVecs];
+#pragma unroll
+  for (int u = 0; u < kPrepVecs; ++u) {
+    const int i = threadIdx.x + u * kPrepThreads;
+    keep[u] = i < n8 ? load(i) : make_uint4(0, 0, 0, 0);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int u = 0; u < kPrepVecs; ++u) amax = vmax(amax, keep[u]);
+  for (int i = threadIdx.x + kPrepVecs * kPrepThreads; i < n8; i += kPrepThreads) amax = vmax(amax, load(i));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kPrepThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+  int e = 0;
+  if (amax > 0.0f) {
+    int ex;
+    (void)frexpf(amax, &ex);             // amax in [2^(ex-1), 2^ex)
+    e = min(max(16 - ex, -126), 126);
+  }
+  const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+  if (threadIdx.x == 0) rs[row] = __uint_as_float((uint32_t)(127 - e) << 23);
+  uint4 *outr = reinterpret_cast<uint4 *>(x16 + row * k);
+  auto convert = [&](const uint4 &v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __half2 hv = __floats2half2_rn(bf16_lo(w[u]) * up, bf16_hi(w[u]) * up);
+      o[u] = *reinterpret_cast<const uint32_t *>(&hv);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+#pragma unroll
+  for (int u = 0; u < kPrepVecs; ++u) {
+    const int i = threadIdx.x + u * kPrepThreads;
+    if (i < n8) outr[i] = convert(keep[u]);
+  }
+  for (int i = threadIdx.x + kPrepVecs * kPrepThreads; i < n8; i += kPrepThreads) outr[i] = convert(load(i));
+}
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+int pick_nt(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : 64; }
+
+// Work split and workspace layout of one call: [arrival counters |
+// fp32 partials of shared tiles | f16 activations | row scales].
+struct TPlan {
+  int nt, wtiles, nkb, grid, maxfrag, whole, split_tiles;
+  size_t x16_off, rs_off, ws_bytes;
+};
+
+TPlan make_tplan(int64_t m, int64_t n, int64_t k) {
+  TPlan pl{};
+  pl.nt = pick_nt(m);
+  pl.wtiles = (int)((n + 127) / 128);
+  pl.nkb = (int)((k + kBK - 1) / kBK);   // the last k-block may be 64, 128 or 192 wide
+  const int sms = num_sms();
+  const int64_t w = (int64_t)pl.wtiles * pl.nkb;
+  pl.grid = (int)(w < sms ? w : sms);
+  // every CTA gets `whole` whole tiles; the remaining tiles are cut into one
+  // contiguous run of (tile, k-block) pairs per CTA, and every CTA must own
+  // at least one k-block of them when there are any
+  pl.whole = pl.wtiles / pl.grid;
+  pl.split_tiles = pl.wtiles - pl.whole * pl.grid;
+  if (pl.whole > 0 && pl.split_tiles > 0 && (int64_t)pl.split_tiles * pl.nkb < pl.grid) {
+    --pl.whole;
+    pl.split_tiles += pl.grid;
+  }
+  const int64_t su = (int64_t)pl.split_tiles * pl.nkb;
+  const int64_t per = (su + pl.grid - 1) / pl.grid;
+  pl.maxfrag = (int)((per + pl.nkb - 1) / pl.nkb + 1);
+  const bool shared = su > 0 && ((su % pl.grid != 0) || ((su / pl.grid) % pl.nkb != 0));
+  const size_t part_bytes = shared ? (size_t)pl.grid * pl.maxfrag * pl.nt * 128 * 4 : 0;
+  pl.x16_off = kCounterArea + round256(part_bytes);
+  pl.rs_off = pl.x16_off + round256((size_t)(m * k * 2));
+  pl.ws_bytes = pl.rs_off + round256((size_t)m * 4);
+  return pl;
+}
+
+template <int NT>
+cudaError_t launch_nt(const TPlan &pl, const uint16_t *x, const uint16_t *pre, const uint8_t *w, const uint8_t *wsf,
+                      const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k, uint8_t *ws,
+                      uint32_t wait_limit, cudaStream_t st) {
+  using C = TCfg<NT>;
+  static PerDeviceOnce smem_attr;   // the shared-memory limit is a setting of each device's context
+  if (cudaError_t e = smem_attr.run([] {
+        return cudaFuncSetAttribute(w4a16_tmem_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)C::SMEM_BYTES);
+      }))
+    return e;
+  uint16_t *x16 = reinterpret_cast<uint16_t *>(ws + pl.x16_off);
+  float *rs = reinterpret_cast<float *>(ws + pl.rs_off);
+  CUtensorMap tm_x, tm_w;
+  // f16 activations [m, k]: box 128 bytes (64 elements) x NT rows, 128-byte swizzle;
+  // weight codes [n, k/2]: box 128 bytes x 128 rows, 128-byte swizzle
+  if (!make_byte_map(&tm_x, x16, m, k * 2, 128, NT, 128) || !make_byte_map(&tm_w, w, n, k / 2, kBK / 2, 128, 128))
+    return cudaErrorInvalidValue;
+  TArgs a{};
+  a.wsf = wsf;
+  a.alpha = alpha;
+  a.rs = rs;
+  a.d = d;
+  a.m = (int32_t)m;
+  a.n = (int32_t)n;
+  a.k = (int32_t)k;
+  a.wtiles = pl.wtiles;
+  a.nkb = pl.nkb;
+  a.grid = pl.grid;
+  a.maxfrag = pl.maxfrag;
+  a.whole = pl.whole;
+  a.split_tiles = pl.split_tiles;
+  a.counters = reinterpret_cast<int *>(ws);
+  a.partials = reinterpret_cast<float *>(ws + kCounterArea);
+  a.wait_limit = wait_limit;
+  a.status = device_status_ptr();
+  if (!a.status) return cudaErrorInvalidValue;
+  if (cudaError_t e =
+          launch_pdl(w4a16_act_f16_kernel, dim3((unsigned)m), dim3(kPrepThreads), 0, st, x, pre, k, x16, rs))
+    return e;
+  return launch_pdl(w4a16_tmem_kernel<NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_x, tm_w, a);
+}
+
+}  // namespace
+
+bool w4a16_tmem_supported(int64_t m, int64_t n, int64_t k) {
+  return m > 0 && m <= 64 && w4a16_tc_supported(m, n, k);
+}
+
+size_t w4a16_tmem_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+  if (!w4a16_tmem_supported(m, n, k)) return 0;
+  return make_tplan(m, n, k).ws_bytes;
+}
+
+cudaError_t launch_w4a16_tmem(const uint16_t *x, const uint16_t *pre_scale, const uint8_t *w, const uint8_t *wsf,
+                              const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws,
+                              size_t ws_bytes, uint32_t wait_limit, cudaStream_t st) {
+  if (!w4a16_tmem_supported(m, n, k)) return cudaErrorNotSupported;
+  const TPlan pl = make_tplan(m, n, k);
+  if (!ws || ws_bytes < pl.ws_bytes) return cudaErrorInvalidValue;
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  switch (pl.nt) {
+    case 16: return launch_nt<16>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+    case 32: return launch_nt<32>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+    default: return launch_nt<64>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+  }
+}
+
+}  // namespace nvfp4

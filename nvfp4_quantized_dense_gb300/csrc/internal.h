@@ -106,9 +106,10 @@ int *device_status_ptr();
 // Host helpers shared by the tensor-core units.
 int num_sms();
 // 2-D TMA map over a row-major byte matrix [rows, row_bytes] (row stride
-// row_bytes), box box_bytes x box_rows, 128-byte swizzle when swizzle128.
+// row_bytes), box box_bytes x box_rows, swizzle_bytes-wide swizzle (128, 64,
+// or 0 for none; the box's row must not be wider than the swizzle).
 bool make_byte_map(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t row_bytes,
-                   uint32_t box_bytes, uint32_t box_rows, bool swizzle128);
+                   uint32_t box_bytes, uint32_t box_rows, int swizzle_bytes);
 
 // Decode-sized tensor-core path (weights as the MMA M operand).
 size_t swapab_workspace_bytes(TcMode mode, int64_t m, int64_t n, int64_t k);
@@ -119,16 +120,29 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
                           int64_t k, void *workspace, size_t ws_bytes, uint32_t wait_limit,
                           cudaStream_t st, const float *a_row_scale = nullptr);
 
-// W4A16 on the tensor cores (weights dequantized to bf16 in shared memory).
-// With a workspace of w4a16_workspace_bytes (zero-filled once; counters left
-// at zero), the work is split across CTAs along K -- up to 64 tokens always,
-// above when whole weight tiles would leave SMs idle; otherwise every CTA
-// owns whole tiles.
+// W4A16 on the tensor cores.  Up to 64 tokens, given a workspace of
+// w4a16_workspace_bytes (16-byte aligned, zero-filled once; counters left at
+// zero), the TMEM kernel runs: weights dequantized to f16 into tensor memory,
+// activations turned into f16 with a power-of-two scale per row by a
+// pre-pass into the workspace (times the AWQ pre-scale when pre_scale is
+// given), work split along K over all SMs.  Otherwise the shared-memory
+// kernel runs (weights dequantized to bf16 in shared memory; split along K
+// up to 64 tokens always and above when whole weight tiles would leave SMs
+// idle, given its workspace; whole tiles per CTA without one); it takes no
+// pre_scale (the caller scales the activations first).
 bool w4a16_tc_supported(int64_t m, int64_t n, int64_t k);
 size_t w4a16_workspace_bytes(int64_t m, int64_t n, int64_t k);
-cudaError_t launch_w4a16_tc(const uint16_t *x, const uint8_t *w, const uint8_t *wsf, const float *alpha,
-                            uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws, size_t ws_bytes,
-                            uint32_t wait_limit, cudaStream_t st);
+// true when launch_w4a16_tc with this workspace runs the TMEM kernel
+bool w4a16_uses_tmem(int64_t m, int64_t n, int64_t k, const void *ws, size_t ws_bytes);
+cudaError_t launch_w4a16_tc(const uint16_t *x, const uint16_t *pre_scale, const uint8_t *w, const uint8_t *wsf,
+                            const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws,
+                            size_t ws_bytes, uint32_t wait_limit, cudaStream_t st);
+// The TMEM kernel alone (gemm_w4a16_tmem.cu).
+bool w4a16_tmem_supported(int64_t m, int64_t n, int64_t k);
+size_t w4a16_tmem_workspace_bytes(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_w4a16_tmem(const uint16_t *x, const uint16_t *pre_scale, const uint8_t *w, const uint8_t *wsf,
+                              const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k, void *ws,
+                              size_t ws_bytes, uint32_t wait_limit, cudaStream_t st);
 
 // Whole decode MLP in one persistent kernel (mlp_decode.cu).
 struct MlpDecodeParams {

@@ -633,10 +633,10 @@ cudaError_t launch_nt(const Plan &pl, const MlpDecodeParams &q, cudaStream_t st)
   const int64_t m = q.m, hid = q.hidden, inter = q.inter;
   CUtensorMap tm_wgu, tm_xq, tm_wdn, tm_h;
   // codes [rows, K/2] bytes; box 128 bytes of K x (128 weight rows | NT token rows), 128-byte swizzle
-  if (!make_byte_map(&tm_wgu, q.w_gu, 2 * inter, hid / 2, 128, 128, true) ||
-      !make_byte_map(&tm_xq, q.x_fp4, m, hid / 2, 128, NT, true) ||
-      !make_byte_map(&tm_wdn, q.w_dn, hid, inter / 2, 128, 128, true) ||
-      !make_byte_map(&tm_h, q.h_fp4, m, inter / 2, 128, NT, true))
+  if (!make_byte_map(&tm_wgu, q.w_gu, 2 * inter, hid / 2, 128, 128, 128) ||
+      !make_byte_map(&tm_xq, q.x_fp4, m, hid / 2, 128, NT, 128) ||
+      !make_byte_map(&tm_wdn, q.w_dn, hid, inter / 2, 128, 128, 128) ||
+      !make_byte_map(&tm_h, q.h_fp4, m, inter / 2, 128, NT, 128))
     return cudaErrorInvalidValue;
   MlpArgs a{};
   uint8_t *ws = static_cast<uint8_t *>(q.workspace);

@@ -331,6 +331,22 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D(tmem) (+)= A(tmem) x B(smem)^T, 16-bit operands (type in idesc), fp32
+// accumulation.  A (M = 128 rows x K = 16) sits in TMEM lanes 0..127, row i
+// in lane i, two consecutive K elements per 32-bit column (the lower K index
+// in the low half): 8 columns from a_tmem.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               bool accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
 // Copy a 32-row x 16-byte block from shared memory to TMEM, replicated into
 // the four 32-lane sub-partitions (4 TMEM columns starting at taddr).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {

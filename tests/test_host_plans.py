@@ -9,12 +9,13 @@ k-blocks):
 every CTA takes floor(tiles/grid) whole tiles, the other tiles are cut into
 one contiguous run of (tile, k-block) pairs per CTA, and when those shared
 tiles have fewer k-blocks than there are CTAs one round of whole tiles joins
-them.  W4A16 tensor-core GEMM (k-blocks 128 wide up to 32 tokens, the last
-one possibly 64 wide; 64 wide above): one contiguous run per CTA up to 64
-tokens, and above when whole tiles would leave SMs idle.  The scratch is the
-counter area plus
-[grid][fragment slots][tokens padded][128] fp32 partials, only when a tile is
-shared.  The whole-MLP decode kernel plans both of its GEMM phases the
+them.  W4A16 tensor-core GEMM: up to 64 tokens the TMEM kernel, split as the
+swap-AB kernel without clusters, whose scratch is the counter area, the
+fp32 partials [grid][fragment slots][tokens padded][128] when a tile is
+shared, the f16 activations [m][k] and the fp32 row scales [m], each
+rounded up to 256 bytes; above, the shared-memory kernel (64-wide k-blocks, split only when
+whole tiles would leave SMs idle; counter area plus partials, only when a
+tile is shared).  The whole-MLP decode kernel plans both of its GEMM phases the
 swap-AB way on one grid (the smaller of the SM count and either phase's
 k-block count).  The rule that every CTA between a shared tile's first and
 last owner contributes to it is checked on the restated partition, and so is
@@ -85,11 +86,18 @@ def swapab_plan(m, n, k, sms, clusters=True):
 
 
 def w4a16_ws(m, n, k, sms):
-    nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128 if m <= 128 else 256
-    bk = 128 if nt <= 32 else 64            # k-block width: 128 up to 32 tokens
+    if m <= 64:
+        # TMEM kernel: the swap-AB kernel's mixed split (256-wide k-blocks, no
+        # clusters); the workspace also holds the f16 activations and the row
+        # scales
+        pl = swapab_plan(m, n, k, sms, clusters=False)
+        part = pl["ws"] - COUNTER_AREA if pl["ws"] else 0
+        return COUNTER_AREA + r256(part) + r256(m * k * 2) + r256(m * 4)
+    nt = 128 if m <= 128 else 256
+    bk = 64
     tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), math.ceil(k / bk)
     rounds = math.ceil(tiles / sms)
-    if nt > 64 and tiles * 100 >= rounds * sms * 80:    # whole tiles fill the rounds
+    if tiles * 100 >= rounds * sms * 80:    # whole tiles fill the rounds
         return 0
     w = tiles * nkb
     grid = min(w, sms)
@@ -98,6 +106,10 @@ def w4a16_ws(m, n, k, sms):
     if tiles > COUNTER_AREA // 4:
         return 0
     return COUNTER_AREA + grid * maxfrag * nt * 128 * 4 if shared else 0
+
+
+def r256(b):
+    return (b + 255) // 256 * 256
 
 
 SWAP_CASES = [
@@ -286,10 +298,14 @@ def test_swapab_reduction_bookkeeping_random_shapes():
                                    (1024, 5120, 17408)])
 @pytest.mark.parametrize("sms", [148, 152, 7])
 def test_w4a16_reduction_bookkeeping(m, n, k, sms):
-    """The W4A16 split-K (one contiguous run per CTA over all tiles) keeps
-    the same invariants as the swap-AB mixed split with no whole tiles."""
-    nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128 if m <= 128 else 256
-    bk = 128 if nt <= 32 else 64
+    """Up to 64 tokens the W4A16 TMEM kernel uses the swap-AB mixed split;
+    above, the split-K (one contiguous run per CTA over all tiles) keeps the
+    same invariants as the mixed split with no whole tiles."""
+    if m <= 64:
+        test_swapab_reduction_bookkeeping(m, n, k, sms)
+        return
+    nt = 128 if m <= 128 else 256
+    bk = 64
     tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), math.ceil(k / bk)
     grid = min(tiles * nkb, sms)
     units = tiles * nkb
