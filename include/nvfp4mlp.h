@@ -244,12 +244,22 @@ nvfp4_status nvfp4_gemm_swiglu_quant_per_token(const uint8_t *a_fp4, const uint8
  *   a bf16 [m, k];  b_fp4/b_sf as nvfp4_gemm;  alpha fp32 [1] = 1/gs_b only.
  *   workspace  optional DEVICE scratch (nullptr / 0 allowed): with
  *              bf16_fp4_gemm_workspace_bytes(m, n, k, algo) bytes, 16-byte
- *              aligned and zero-filled once before first use, the tensor-core
- *              path splits the work along K over all SMs -- up to 64 tokens
+ *              aligned and its first 64 KiB (the arrival counters)
+ *              zero-filled once before first use, the tensor-core path
+ *              splits the work along K over all SMs -- up to 64 tokens
  *              always, above when whole 128-row weight tiles would leave SMs
  *              idle (the counters are left at zero after every complete call;
  *              calls sharing it must be stream-ordered); with less, every SM
- *              owns whole weight tiles.  The result does not depend on it.
+ *              owns whole weight tiles.  Up to 64 tokens the workspace also
+ *              selects the TMEM kernel: the weights are dequantized to f16
+ *              in tensor memory and the activations are written into the
+ *              workspace by a pre-pass as f16 times a power of two 2^e per
+ *              token row (e puts the row's largest finite magnitude in
+ *              [2^15, 2^16); the epilogue multiplies by 2^-e).  That is exact
+ *              for every activation within 2^30 of its row's largest
+ *              magnitude (smaller ones are rounded by at most 2^-25 * 2^-e),
+ *              so the result depends on the workspace only through the
+ *              order of the fp32 accumulation.
  * Requires k % 64 == 0, n % 32 == 0. */
 nvfp4_status bf16_fp4_gemm(const uint16_t *a, const uint8_t *b_fp4, const uint8_t *b_sf,
                            const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k,
