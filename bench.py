@@ -284,6 +284,11 @@ def run_ours(args, world, rank, local):
     hbm_peak = pk["hbm_gbs"] if pk else 6800.0
     bf16_peak = pk["bf16_tflops"] if pk else 1900.0
     fp4_peak = bf16_peak * 6.0        # dense FP4 : dense BF16 = 13.5 : 2.25 (nominal)
+    # the sustained figure (cuBLAS bf16 back to back for seconds, under the
+    # power cap) is the denominator for kernels timed inside long runs of
+    # back-to-back launches, as every per-M record and the step are
+    bf16_sus = pk.get("bf16_tflops_sustained", bf16_peak) if pk else 1700.0
+    fp4_sus = bf16_sus * 6.0
     peak_src = "measured" if pk else "fallback"
     algo = {"auto": nv.ALGO_AUTO, "gemv": nv.ALGO_GEMV, "tc": nv.ALGO_TC, "tc1sm": nv.ALGO_TC_1SM,
             "swapab": nv.ALGO_TC_SWAPAB}[args.algo]
@@ -551,7 +556,9 @@ def run_ours(args, world, rank, local):
         return t
 
     w_bytes = {}      # per weight tensor: codes + scales
-    for it in items:
+    # the power-hungry prefill last, so that its clock drop under the power
+    # cap does not carry over into the other workloads' records
+    for it in [i for i in items if i.wid != 3] + [i for i in items if i.wid == 3]:
         hid, inter = it.hid, it.inter
         gu_w = 2 * inter * hid * 9 // 16
         dn_w = inter * hid * 9 // 16
@@ -576,9 +583,12 @@ def run_ours(args, world, rank, local):
                 r["down_hbm_frac"] = dn_b / (t_dn / 1000) / 1e9 / hbm_peak
                 r["path_hbm_frac"] = (gu_w + dn_w) / (t_fwd / 1000) / 1e9 / hbm_peak
             else:                # compute-bound: tensor peak of the contraction's dtype
-                pkk = bf16_peak if it.w4a16 else fp4_peak
-                r["gate_up_tensor_frac"] = gu_f / (t_gu / 1000) / 1e12 / pkk
-                r["down_tensor_frac"] = dn_f / (t_dn / 1000) / 1e12 / pkk
+                pks = bf16_sus if it.w4a16 else fp4_sus
+                pkb = bf16_peak if it.w4a16 else fp4_peak
+                r["gate_up_tensor_frac"] = gu_f / (t_gu / 1000) / 1e12 / pks
+                r["down_tensor_frac"] = dn_f / (t_dn / 1000) / 1e12 / pks
+                r["gate_up_tensor_frac_of_burst"] = gu_f / (t_gu / 1000) / 1e12 / pkb
+                r["down_tensor_frac_of_burst"] = dn_f / (t_dn / 1000) / 1e12 / pkb
                 r["gate_up_tflops"] = gu_f / (t_gu / 1000) / 1e12
             rec["per_m"][str(m)] = r
         if it.wid == 1 and it.gu_plain is not None:
@@ -647,13 +657,16 @@ def run_ours(args, world, rank, local):
         r = per[it.key]["per_m"][str(m)]
         if m > 64:
             flops = (4.0 if which == "gate_up" else 2.0) * m * it.hid * it.inter
-            pkk = bf16_peak if it.w4a16 else fp4_peak
+            pkk = bf16_sus if it.w4a16 else fp4_sus
+            pkb = bf16_peak if it.w4a16 else fp4_peak
             achieved = flops / (t_us / 1e6) / 1e12
             roofline = {"bound": "tensor", "achieved": achieved, "peak": pkk, "unit": "TFLOP/s",
                         "frac": achieved / pkk, "traffic": None,
                         "algorithmic_flops_per_launch": flops,
-                        "peak_note": ("measured bf16 burst" if it.w4a16 else
-                                      "measured bf16 burst x 6 (nominal fp4 : bf16)") + f" ({peak_src})"}
+                        "peak_note": ("measured bf16 sustained" if it.w4a16 else
+                                      "measured bf16 sustained x 6 (nominal fp4 : bf16)") + f" ({peak_src}); "
+                                     "the kernel is timed inside runs of back-to-back launches",
+                        "peak_burst": pkb, "frac_of_burst": achieved / pkb}
         else:
             nb = r[f"{which}_hbm_frac"] * hbm_peak * 1e9 * (t_us / 1e6)
             achieved = nb / (t_us / 1e6) / 1e9

@@ -68,22 +68,33 @@ constexpr int kFirstConv = 4;
 constexpr int kFirstEpi = kFirstConv + 16;   // warps 20..23
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kDrainPolls = 1u << 22;
-constexpr int kBK = 256;                    // K per k-block
-constexpr int kSub = kBK / 64;              // 64-wide sub-blocks per k-block (one scale tile each)
 
+// Two configurations.  Up to 64 tokens (weight streaming): 256-wide k-blocks
+// of 128-byte code rows, the halves of a k-block issued by two MMA issuers.
+// 128-token tiles (more tokens; the MMA is the bound): 128-wide k-blocks of
+// 64-byte code rows (64-byte swizzle), one issuer, 4 activation stages of
+// 32 KB.  Either way a k-block is dequantized in two halves, each into a TMEM
+// slot of BK/4 columns, by 16 converter warps, one per (half, quarter, TMEM
+// lane quarter).
 template <int NT>
 struct TCfg {
+  static constexpr bool DECODE = NT <= 64;
+  static constexpr int BK = DECODE ? 256 : 128;                 // K per k-block
+  static constexpr int SUB = BK / 64;                           // 64-wide sub-blocks (one scale tile each)
+  static constexpr int CPQ = BK / 128;                          // 32-element code chunks per quarter
+  static constexpr int NI = DECODE ? 2 : 1;                     // MMA issuers
+  static constexpr uint32_t CODE_ROW = BK / 2;                  // code bytes of a weight row per k-block
   static constexpr uint32_t SUB_X = NT * 128;                   // NT rows x 64 f16, 128-byte swizzle
-  static constexpr uint32_t X_BYTES = kSub * SUB_X;             // one activation stage
-  static constexpr uint32_t WC_BYTES = 128 * kBK / 2;           // 128 rows x 128 bytes of codes
-  static constexpr uint32_t WS_BYTES = kSub * 512;              // 128x4 scale tiles
+  static constexpr uint32_t X_BYTES = SUB * SUB_X;              // one activation stage
+  static constexpr uint32_t WC_BYTES = 128 * CODE_ROW;
+  static constexpr uint32_t WS_BYTES = SUB * 512;               // 128x4 scale tiles
   static constexpr uint32_t W_BYTES = WC_BYTES + WS_BYTES;      // one weight stage (a multiple of 1024)
-  static constexpr int XSTAGES = NT <= 32 ? 4 : 3;
+  static constexpr int XSTAGES = NT == 64 ? 3 : 4;
   static constexpr uint32_t BAR_BYTES = 1024;
   static constexpr int WSTAGES_FIT = (int)((224u * 1024 - XSTAGES * X_BYTES - BAR_BYTES - 1024) / W_BYTES);
   static constexpr int WSTAGES = WSTAGES_FIT > 16 ? 16 : WSTAGES_FIT;
-  static constexpr uint32_t ACC_COLS = 2 * 2 * NT;              // two tile buffers x two issuers
-  static constexpr uint32_t A_COLS = kBK / 4;                   // f16 pairs of one half k-block row
+  static constexpr uint32_t ACC_COLS = 2 * NI * NT;             // two tile buffers x the issuers
+  static constexpr uint32_t A_COLS = BK / 4;                    // f16 pairs of one half k-block row
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int DSTAGES = (int)((TMEM_COLS - ACC_COLS) / A_COLS) / 2 * 2;
   static constexpr uint32_t SMEM_BYTES = XSTAGES * X_BYTES + WSTAGES * W_BYTES + BAR_BYTES + 1024;
@@ -92,6 +103,7 @@ struct TCfg {
   static_assert(WSTAGES >= 4, "weight ring depth");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert((2 * WSTAGES + 2 * XSTAGES + 2 * DSTAGES + 6) * 8 + 16 <= BAR_BYTES, "barrier area");
+  static_assert(ACC_COLS + 2 * A_COLS <= TMEM_COLS, "TMEM columns");
 };
 
 struct TArgs {
@@ -102,7 +114,7 @@ struct TArgs {
   float *partials;         // [grid][maxfrag][NT][128] fp32 (tiles shared by CTAs)
   int *counters;           // [split tiles] arrival counters
   int32_t m, n, k;
-  int32_t wtiles, nkb;
+  int32_t wtiles, ttiles, nkb;   // tile t = weight tile t / ttiles, token tile t % ttiles
   int32_t grid, maxfrag, whole, split_tiles;
   uint32_t wait_limit;
   int *status;
@@ -142,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const TArgs p) {
   using C = TCfg<NT>;
   constexpr int WST = C::WSTAGES, XST = C::XSTAGES, DST = C::DSTAGES;
+  constexpr int BK = C::BK, SUB = C::SUB, NI = C::NI, CPQ = C::CPQ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto st_x = [&](int r) { return base + r * C::X_BYTES; };
@@ -169,14 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int r = 0; r < XST; ++r) {
       ptx::mbar_init(&xfull[r], 1);
-      ptx::mbar_init(&xempty[r], 2);       // one commit per issuer
+      ptx::mbar_init(&xempty[r], NI);      // one commit per issuer
     }
     for (int d = 0; d < DST; ++d) {
       ptx::mbar_init(&dfull[d], 8);        // the eight warps converting a half
       ptx::mbar_init(&dempty[d], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&tfull[b], 2);        // one commit per issuer
+      ptx::mbar_init(&tfull[b], NI);       // one commit per issuer
       ptx::mbar_init(&tempty[b], 128);
       ptx::mbar_init(&drain[b], 1);
     }
@@ -205,9 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto a_col = [&](int d) { return C::ACC_COLS + (uint32_t)d * C::A_COLS; };
 
   const int cp4 = p.k >> 6;              // 512-byte scale tiles per 128-row block
-  auto nsub_of = [&](int kb) { return min(kSub, cp4 - kb * kSub); };
-  // 64-wide sub-blocks of half h of k-block kb (0, 1 or 2)
-  auto nsub_half = [&](int kb, int h) { return min(2, max(0, nsub_of(kb) - 2 * h)); };
+  auto nsub_of = [&](int kb) { return min(SUB, cp4 - kb * SUB); };
+  // 64-wide sub-blocks of half h of k-block kb (0 .. SUB/2)
+  auto nsub_half = [&](int kb, int h) { return min(SUB / 2, max(0, nsub_of(kb) - (SUB / 2) * h)); };
   const MixedPartition mixed{p.nkb, p.grid, p.whole, p.split_tiles};
   const uint32_t limit = p.wait_limit;
   uint32_t issued_w = 0, issued_w_par = 0, issued_x = 0, issued_x_par = 0;
@@ -235,8 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t sfb = (uint32_t)nsub_of(kb) * 512u;   // scales only of the sub-blocks K has
           ptx::mbar_arrive_expect_tx(&wfull[r], C::WC_BYTES + sfb);
-          ptx::tma_load_2d(st_wc(r), &tm_w, &wfull[r], kb * (kBK / 2), tile * 128, pol_w);
-          ptx::bulk_load(st_ws(r), p.wsf + ((size_t)tile * cp4 + kb * kSub) * 512, sfb, &wfull[r], pol_w);
+          const int wt = tile / p.ttiles;
+          ptx::tma_load_2d(st_wc(r), &tm_w, &wfull[r], kb * (BK / 2), wt * 128, pol_w);
+          ptx::bulk_load(st_ws(r), p.wsf + ((size_t)wt * cp4 + kb * SUB) * 512, sfb, &wfull[r], pol_w);
           issued_w |= 1u << r;
           issued_w_par = (issued_w_par & ~(1u << r)) | (ph << r);
           if (++r == WST) { r = 0; ph ^= 1u; }
@@ -262,8 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::mbar_arrive_expect_tx(&xfull[r], C::X_BYTES);
 #pragma unroll
-          for (int sb = 0; sb < kSub; ++sb)   // a sub-block past K reads zeros
-            ptx::tma_load_2d(st_x(r) + sb * C::SUB_X, &tm_x, &xfull[r], (kb * kSub + sb) * 128, 0, pol_x);
+          for (int sb = 0; sb < SUB; ++sb)    // a sub-block past K reads zeros
+            ptx::tma_load_2d(st_x(r) + sb * C::SUB_X, &tm_x, &xfull[r], (kb * SUB + sb) * 128,
+                             (tile % p.ttiles) * NT, pol_x);
           issued_x |= 1u << r;
           issued_x_par = (issued_x_par & ~(1u << r)) | (ph << r);
           if (++r == XST) { r = 0; ph ^= 1u; }
@@ -272,9 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma0 || warp == kWarpMma1) {
     // ----------------------------------------------------------------- MMA
-    // issuer h issues half h of every k-block
-    const int h = warp == kWarpMma0 ? 0 : 1;
-    if (ptx::elect_one()) {
+    // issuer hi issues the halves h of every k-block with h % NI == hi
+    const int hi = warp == kWarpMma0 ? 0 : 1;
+    if (hi < NI && ptx::elect_one()) {
       // kind::f16: F32 accumulator (bits 4-5 = 1), A = B = F16 (0), K-major,
       // N >> 3 in bits 17-22, M = 128 >> 4 in bits 24-28
       constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | (8u << 24);
@@ -290,31 +305,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t acc = tmem + (uint32_t)((ab * 2 + h) * NT);
+        const uint32_t acc = tmem + (uint32_t)((ab * NI + hi) * NT);
         bool first = true;
-        for (int kb = kb0; kb < kb1; ++kb, ++i) {
-          const int j = 2 * i + h, d = j % DST;
-          const uint32_t dph = (uint32_t)((j / DST) & 1);
-          bool got = ptx::mbar_wait_bounded(&dfull[d], dph, limit, kTimeoutNs, abort_flag);
-          if (got) got = ptx::mbar_wait_bounded(&xfull[xr], xph, limit, kTimeoutNs, abort_flag);
-          if (!got) {
+        for (int kb = kb0; kb < kb1 && ok; ++kb, ++i) {
+          if (!ptx::mbar_wait_bounded(&xfull[xr], xph, limit, kTimeoutNs, abort_flag)) {
             give_up();
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          const uint32_t xs = ptx::smem_u32(st_x(xr)) + (uint32_t)(2 * h) * C::SUB_X;
-          const uint32_t wa = tmem + a_col(d);
-          const int ns = nsub_half(kb, h);
-          for (int sb = 0; sb < ns; ++sb)
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              ptx::mma_f16_tmem_a(acc, wa + 8 * (4 * sb + jj),
-                                  ptx::smem_desc(xs + sb * C::SUB_X + 32 * jj, 16, 1024, 2), idesc, !first);
-              first = false;
+          for (int h = hi; h < 2; h += NI) {
+            const int j = 2 * i + h, d = j % DST;
+            const uint32_t dph = (uint32_t)((j / DST) & 1);
+            if (!ptx::mbar_wait_bounded(&dfull[d], dph, limit, kTimeoutNs, abort_flag)) {
+              give_up();
+              ok = false;
+              break;
             }
-          mma_issued = true;
-          ptx::tc_commit(&dempty[d]);
+            ptx::tc_fence_after();
+            const uint32_t xs = ptx::smem_u32(st_x(xr)) + (uint32_t)(h * (SUB / 2)) * C::SUB_X;
+            const uint32_t wa = tmem + a_col(d);
+            const int ns = nsub_half(kb, h);
+            for (int sb = 0; sb < ns; ++sb)
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                ptx::mma_f16_tmem_a(acc, wa + 8 * (4 * sb + jj),
+                                    ptx::smem_desc(xs + sb * C::SUB_X + 32 * jj, 16, 1024, 2), idesc, !first);
+                first = false;
+              }
+            mma_issued = true;
+            ptx::tc_commit(&dempty[d]);
+          }
+          if (!ok) break;
           ptx::tc_commit(&xempty[xr]);
           if (++xr == XST) { xr = 0; xph ^= 1u; }
         }
@@ -324,17 +346,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kFirstEpi) {
     // ---------------------------------------------------------- converters
-    // warp (h, qt, q): half h, its 64-wide quarter qt (sub-block 2h + qt of
-    // the k-block, TMEM columns 32 qt .. 32 qt + 31 of the half's slot), TMEM
-    // lanes 32 q ..  A half's slot has the half's parity (DST is even).
+    // warp (h, qt, q): half h, its quarter qt (CPQ 32-element chunks starting
+    // at chunk (2h + qt) * CPQ of the k-block; TMEM columns (A_COLS / 2) * qt
+    // .. of the half's slot), TMEM lanes 32 q ..  A half's slot has the
+    // half's parity (DST is even).
     const int cg = (warp - kFirstConv) >> 2;
     const int h = cg >> 1, qt = cg & 1, q = warp & 3;
-    const int sb = 2 * h + qt;
+    const int chunk0 = (2 * h + qt) * CPQ;    // first code chunk of the quarter
+    const int sb = chunk0 >> 1;               // its 64-wide sub-block
     const int row = 32 * q + lane;
-    const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16) + 32u * qt;
-    const int swz = row & 7;                  // 128-byte swizzle: chunk c of the row sits at c ^ swz
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16) + (C::A_COLS / 2) * qt;
+    // chunk c of the row sits at c ^ swz: 128-byte swizzle (128-byte rows) or 64-byte (64-byte rows)
+    const int swz = C::CODE_ROW == 128 ? (row & 7) : ((row >> 1) & 3);
     const uint32_t sf_off = (uint32_t)(sb * 512 + (row & 31) * 16 + (row >> 5) * 4);
-    const uint32_t c_off = (uint32_t)(row * (kBK / 2));
+    const uint32_t c_off = (uint32_t)(row * C::CODE_ROW);
     MixedIter mi(mixed, blockIdx.x);
     int tile, kb0, kb1;
     int i = 0, wr = 0;
@@ -353,28 +378,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool have = sb < nsub_of(kb);    // this quarter holds some of K
         const uint8_t *crow = st_wc(wr) + c_off;
-        const uint4 c0 = *reinterpret_cast<const uint4 *>(crow + (((2 * sb) ^ swz) << 4));
-        const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + (((2 * sb + 1) ^ swz) << 4));
+        uint4 cv[CPQ];
+#pragma unroll
+        for (int c = 0; c < CPQ; ++c)
+          cv[c] = *reinterpret_cast<const uint4 *>(crow + (((chunk0 + c) ^ swz) << 4));
         const uint32_t sw = *reinterpret_cast<const uint32_t *>(st_ws(wr) + sf_off);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&wempty[wr]);   // the stage's codes are read (release)
         if (++wr == WST) { wr = 0; wph ^= 1u; }
         if (have) {
-          // elements 0..31 of the quarter: scales 0 and 1; 32..63: scales 2 and 3
-          uint32_t s0, s1, s2, s3;
-          scales_to_h2(sw, s0, s1);
-          scales_to_h2(sw >> 16, s2, s3);
-          uint32_t o[16];
-          dequant8_f16(c0.x, s0, o);
-          dequant8_f16(c0.y, s0, o + 4);
-          dequant8_f16(c0.z, s1, o + 8);
-          dequant8_f16(c0.w, s1, o + 12);
-          ptx::tmem_st16(t_lane + a_col(d), o);
-          dequant8_f16(c1.x, s2, o);
-          dequant8_f16(c1.y, s2, o + 4);
-          dequant8_f16(c1.z, s3, o + 8);
-          dequant8_f16(c1.w, s3, o + 12);
-          ptx::tmem_st16(t_lane + a_col(d) + 16, o);
+#pragma unroll
+          for (int c = 0; c < CPQ; ++c) {
+            // chunk chunk0 + c: 32 elements, scales 2 (chunk & 1) and 2 (chunk & 1) + 1 of the sub-block
+            uint32_t s0, s1;
+            scales_to_h2(sw >> (16 * ((chunk0 + c) & 1)), s0, s1);
+            uint32_t o[16];
+            dequant8_f16(cv[c].x, s0, o);
+            dequant8_f16(cv[c].y, s0, o + 4);
+            dequant8_f16(cv[c].z, s1, o + 8);
+            dequant8_f16(cv[c].w, s1, o + 12);
+            ptx::tmem_st16(t_lane + a_col(d) + 16 * c, o);
+          }
           ptx::tmem_wait_st();
         }
         ptx::tc_fence_before();
@@ -395,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     auto load_acc = [&](int ab, int c, bool p1, float (&o)[16]) {
       uint32_t v[16];
-      const uint32_t a0 = t_row + (uint32_t)(ab * 2 * NT + 16 * c);
+      const uint32_t a0 = t_row + (uint32_t)(ab * NI * NT + 16 * c);
       ptx::tmem_ld16(a0, v);
       ptx::tmem_wait_ld();
 #pragma unroll
@@ -407,22 +431,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 16; ++x) o[x] += __uint_as_float(v[x]);
       }
     };
-    // bf16(alpha * v * 2^-e) of token t (< m)
+    // bf16(alpha * v * 2^-e) of token row t (< m)
     auto out_bits = [&](float v, int t) {
       const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v * __ldg(p.rs + t));
       return *reinterpret_cast<const uint16_t *>(&o);
     };
     MixedIter mi(mixed, blockIdx.x);
     int tile, kb0, kb1;
-    const int mt = min(p.m, NT);
     for (; mi.next(tile, kb0, kb1); ++it) {
       const int ab = it & 1;
       const bool got = ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag);
       if (!got) give_up();
       if (ptx::bar_any(2, 128, !got || *abort_flag)) break;   // the four warps leave together
       ptx::tc_fence_after();
-      const int n = tile * 128 + row;
-      const bool p1 = nsub_of(kb0) > 2;      // half 1 of the fragment holds some of K
+      const int n = (tile / p.ttiles) * 128 + row;
+      const int t0 = (tile % p.ttiles) * NT;  // first token row of the tile
+      const int mt = min(p.m - t0, NT);
+      const bool p1 = NI > 1 && nsub_of(kb0) > SUB / 2;   // issuer 1 added half 1 of some k-block
       const bool split_tile = mixed.is_split(tile);
       const int64_t c_first = split_tile ? mixed.cta_of((int64_t)tile * p.nkb) : blockIdx.x;
       const int64_t c_last = split_tile ? mixed.cta_of((int64_t)tile * p.nkb + p.nkb - 1) : blockIdx.x;
@@ -434,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n < p.n) {
 #pragma unroll
             for (int x = 0; x < 16; ++x)
-              if (16 * c + x < mt) p.d[(size_t)(16 * c + x) * p.n + n] = out_bits(v[x], 16 * c + x);
+              if (16 * c + x < mt) p.d[(size_t)(t0 + 16 * c + x) * p.n + n] = out_bits(v[x], t0 + 16 * c + x);
           }
         }
         ptx::tc_fence_before();
@@ -488,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n < p.n) {
 #pragma unroll
           for (int x = 0; x < TG; ++x)
-            if (g0 + x < mt) p.d[(size_t)(g0 + x) * p.n + n] = out_bits(acc[x], g0 + x);
+            if (g0 + x < mt) p.d[(size_t)(t0 + g0 + x) * p.n + n] = out_bits(acc[x], t0 + g0 + x);
         }
       }
     }
@@ -597,28 +622,31 @@ __global__ void __launch_bounds__(kPrepThreads) w4a16_act_f16_kernel(const uint1
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-int pick_nt(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : 64; }
+int pick_nt(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128; }
 
 // Work split and workspace layout of one call: [arrival counters |
 // fp32 partials of shared tiles | f16 activations | row scales].
 struct TPlan {
-  int nt, wtiles, nkb, grid, maxfrag, whole, split_tiles;
+  int nt, wtiles, ttiles, nkb, grid, maxfrag, whole, split_tiles;
   size_t x16_off, rs_off, ws_bytes;
 };
 
 TPlan make_tplan(int64_t m, int64_t n, int64_t k) {
   TPlan pl{};
   pl.nt = pick_nt(m);
+  const int bk = pl.nt <= 64 ? TCfg<16>::BK : TCfg<128>::BK;
   pl.wtiles = (int)((n + 127) / 128);
-  pl.nkb = (int)((k + kBK - 1) / kBK);   // the last k-block may be 64, 128 or 192 wide
+  pl.ttiles = (int)((m + pl.nt - 1) / pl.nt);
+  pl.nkb = (int)((k + bk - 1) / bk);     // the last k-block may be narrower (64-wide steps)
+  const int tiles = pl.wtiles * pl.ttiles;
   const int sms = num_sms();
-  const int64_t w = (int64_t)pl.wtiles * pl.nkb;
+  const int64_t w = (int64_t)tiles * pl.nkb;
   pl.grid = (int)(w < sms ? w : sms);
   // every CTA gets `whole` whole tiles; the remaining tiles are cut into one
   // contiguous run of (tile, k-block) pairs per CTA, and every CTA must own
   // at least one k-block of them when there are any
-  pl.whole = pl.wtiles / pl.grid;
-  pl.split_tiles = pl.wtiles - pl.whole * pl.grid;
+  pl.whole = tiles / pl.grid;
+  pl.split_tiles = tiles - pl.whole * pl.grid;
   if (pl.whole > 0 && pl.split_tiles > 0 && (int64_t)pl.split_tiles * pl.nkb < pl.grid) {
     --pl.whole;
     pl.split_tiles += pl.grid;
@@ -650,7 +678,9 @@ cudaError_t launch_nt(const TPlan &pl, const uint16_t *x, const uint16_t *pre, c
   CUtensorMap tm_x, tm_w;
   // f16 activations [m, k]: box 128 bytes (64 elements) x NT rows, 128-byte swizzle;
   // weight codes [n, k/2]: box 128 bytes x 128 rows, 128-byte swizzle
-  if (!make_byte_map(&tm_x, x16, m, k * 2, 128, NT, 128) || !make_byte_map(&tm_w, w, n, k / 2, kBK / 2, 128, 128))
+  // weight codes [n, k/2]: box BK/2 bytes x 128 rows, swizzled as wide as the box
+  if (!make_byte_map(&tm_x, x16, m, k * 2, 128, NT, 128) ||
+      !make_byte_map(&tm_w, w, n, k / 2, C::CODE_ROW, 128, (int)C::CODE_ROW))
     return cudaErrorInvalidValue;
   TArgs a{};
   a.wsf = wsf;
@@ -661,6 +691,7 @@ cudaError_t launch_nt(const TPlan &pl, const uint16_t *x, const uint16_t *pre, c
   a.n = (int32_t)n;
   a.k = (int32_t)k;
   a.wtiles = pl.wtiles;
+  a.ttiles = pl.ttiles;
   a.nkb = pl.nkb;
   a.grid = pl.grid;
   a.maxfrag = pl.maxfrag;
@@ -680,7 +711,7 @@ cudaError_t launch_nt(const TPlan &pl, const uint16_t *x, const uint16_t *pre, c
 }  // namespace
 
 bool w4a16_tmem_supported(int64_t m, int64_t n, int64_t k) {
-  return m > 0 && m <= 64 && w4a16_tc_supported(m, n, k);
+  return m > 0 && w4a16_tc_supported(m, n, k) && (size_t)m * (size_t)k < ((size_t)1 << 31);
 }
 
 size_t w4a16_tmem_workspace_bytes(int64_t m, int64_t n, int64_t k) {
@@ -698,7 +729,8 @@ cudaError_t launch_w4a16_tmem(const uint16_t *x, const uint16_t *pre_scale, cons
   switch (pl.nt) {
     case 16: return launch_nt<16>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
     case 32: return launch_nt<32>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
-    default: return launch_nt<64>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+    case 64: return launch_nt<64>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+    default: return launch_nt<128>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
   }
 }
 

@@ -1,6 +1,7 @@
-"""GPU checks of what is particular to the W4A16 TMEM kernel (up to 64
-tokens, workspace given): the f16 activation pre-pass with its power-of-two
-scale 2^e per token row, undone by the epilogue.
+"""GPU checks of what is particular to the W4A16 TMEM kernel (workspace
+given; 16/32/64-token tiles of 256-wide k-blocks, 128-token tiles of 128-wide
+k-blocks): the f16 activation pre-pass with its power-of-two scale 2^e per
+token row, undone by the epilogue.
 
 * Identity weight (E2M1 code 1.0 times scale 1.0 on the diagonal): the GEMM
   returns the activations themselves, so the output must equal x bit for bit
@@ -78,7 +79,7 @@ def rows_in_range(m, k, seed):
     return oracle.bf16_round(x) + 0.0        # no negative zeros
 
 
-@pytest.mark.parametrize("m,n", [(1, 256), (7, 256), (16, 320), (33, 1024), (64, 512)])
+@pytest.mark.parametrize("m,n", [(1, 256), (7, 256), (16, 320), (33, 1024), (64, 512), (130, 256), (300, 384)])
 def test_identity_weight_returns_activations_bit_exact(lib, m, n):
     x = rows_in_range(m, n, seed=m)
     w, sfo = identity_weight(lib, n)
@@ -107,7 +108,8 @@ def test_wide_row_rounds_small_elements_within_bound(lib):
         assert np.array_equal(got[t][big], x[t][big]), "elements within 2^30 of the row max are exact"
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 384, 1024), (16, 1024, 2048), (40, 256, 640), (64, 512, 512)])
+@pytest.mark.parametrize("m,n,k", [(1, 384, 1024), (16, 1024, 2048), (40, 256, 640), (64, 512, 512),
+                                   (200, 512, 704), (129, 256, 1024)])
 def test_rows_at_extreme_magnitudes_each_within_tolerance(lib, m, n, k):
     ws = small_weights(n, k, 10)
     xbits, x = synth.activations(4, m, k)

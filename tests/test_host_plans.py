@@ -9,13 +9,12 @@ k-blocks):
 every CTA takes floor(tiles/grid) whole tiles, the other tiles are cut into
 one contiguous run of (tile, k-block) pairs per CTA, and when those shared
 tiles have fewer k-blocks than there are CTAs one round of whole tiles joins
-them.  W4A16 tensor-core GEMM: up to 64 tokens the TMEM kernel, split as the
-swap-AB kernel without clusters, whose scratch is the counter area, the
-fp32 partials [grid][fragment slots][tokens padded][128] when a tile is
-shared, the f16 activations [m][k] and the fp32 row scales [m], each
-rounded up to 256 bytes; above, the shared-memory kernel (64-wide k-blocks, split only when
-whole tiles would leave SMs idle; counter area plus partials, only when a
-tile is shared).  The whole-MLP decode kernel plans both of its GEMM phases the
+them.  W4A16 tensor-core GEMM (the TMEM kernel, given its workspace): tiles of
+128 weight rows x 16/32/64/128 tokens, split as the swap-AB kernel without
+clusters (whole tiles last); its scratch is the counter area, the fp32
+partials [grid][fragment slots][tokens padded][128] when a tile is shared,
+the f16 activations [m][k] and the fp32 row scales [m], each rounded up to
+256 bytes.  The whole-MLP decode kernel plans both of its GEMM phases the
 swap-AB way on one grid (the smaller of the SM count and either phase's
 k-block count).  The rule that every CTA between a shared tile's first and
 last owner contributes to it is checked on the restated partition, and so is
@@ -85,31 +84,32 @@ def swapab_plan(m, n, k, sms, clusters=True):
     return dict(nt=nt, tiles=tiles, kbt=kbt, grid=grid, whole=whole, split=split, ws=ws, cl=1)
 
 
+def mixed_plan(tiles, kbt, sms, nt):
+    """The mixed split (whole tiles last): grid, whole tiles per CTA, split
+    tiles, fragment slots and the partials' bytes (0 when no tile is
+    shared)."""
+    grid = min(tiles * kbt, sms)
+    whole = tiles // grid
+    split = tiles - whole * grid
+    if whole > 0 and split > 0 and split * kbt < grid:
+        whole, split = whole - 1, split + grid
+    units = split * kbt
+    maxfrag = math.ceil(math.ceil(units / grid) / kbt) + 1
+    shared = units > 0 and (units % grid != 0 or (units // grid) % kbt != 0)
+    return dict(grid=grid, whole=whole, split=split, maxfrag=maxfrag,
+                part=grid * maxfrag * nt * 128 * 4 if shared else 0)
+
+
 def w4a16_ws(m, n, k, sms):
-    if m <= 64:
-        # TMEM kernel: the swap-AB kernel's mixed split (256-wide k-blocks, no
-        # clusters); the workspace also holds the f16 activations and the row
-        # scales
-        pl = swapab_plan(m, n, k, sms, clusters=False)
-        part = pl["ws"] - COUNTER_AREA if pl["ws"] else 0
-        return COUNTER_AREA + r256(part) + r256(m * k * 2) + r256(m * 4)
-    nt = 128 if m <= 128 else 256
-    bk = 64
-    tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), math.ceil(k / bk)
-    rounds = math.ceil(tiles / sms)
-    if tiles * 100 >= rounds * sms * 80:    # whole tiles fill the rounds
-        return 0
-    w = tiles * nkb
-    grid = min(w, sms)
-    maxfrag = math.ceil(math.ceil(w / grid) / nkb) + 1
-    shared = w % grid != 0 or (w // grid) % nkb != 0
-    if tiles > COUNTER_AREA // 4:
-        return 0
-    return COUNTER_AREA + grid * maxfrag * nt * 128 * 4 if shared else 0
-
-
-def r256(b):
-    return (b + 255) // 256 * 256
+    """The W4A16 TMEM kernel's scratch: token tiles of 16/32/64 (256-wide
+    k-blocks) or 128 (128-wide k-blocks), tiles = weight tiles x token
+    tiles, the mixed split; counters, partials, the f16 activations [m][k]
+    and the fp32 row scales [m], each rounded up to 256 bytes."""
+    nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
+    bk = 256 if nt <= 64 else 128
+    tiles = math.ceil(n / 128) * math.ceil(m / nt)
+    pl = mixed_plan(tiles, math.ceil(k / bk), sms, nt)
+    return COUNTER_AREA + r256(pl["part"]) + r256(m * k * 2) + r256(m * 4)
 
 
 SWAP_CASES = [
@@ -298,34 +298,31 @@ def test_swapab_reduction_bookkeeping_random_shapes():
                                    (1024, 5120, 17408)])
 @pytest.mark.parametrize("sms", [148, 152, 7])
 def test_w4a16_reduction_bookkeeping(m, n, k, sms):
-    """Up to 64 tokens the W4A16 TMEM kernel uses the swap-AB mixed split;
-    above, the split-K (one contiguous run per CTA over all tiles) keeps the
-    same invariants as the mixed split with no whole tiles."""
-    if m <= 64:
-        test_swapab_reduction_bookkeeping(m, n, k, sms)
-        return
-    nt = 128 if m <= 128 else 256
-    bk = 64
-    tiles, nkb = math.ceil(n / 128) * math.ceil(m / nt), math.ceil(k / bk)
-    grid = min(tiles * nkb, sms)
-    units = tiles * nkb
-    maxfrag = math.ceil(math.ceil(units / grid) / nkb) + 1
+    """The W4A16 TMEM kernel's mixed split (weight tiles x token tiles,
+    whole tiles last) keeps the swap-AB split's invariants: every (tile,
+    k-block) covered once, a shared tile's contributors contiguous, each
+    contributor's partial slot its fragment's index below maxfrag."""
+    nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
+    kbt = math.ceil(k / (256 if nt <= 64 else 128))
+    tiles = math.ceil(n / 128) * math.ceil(m / nt)
+    pl = mixed_plan(tiles, kbt, sms, nt)
+    grid, whole, split = pl["grid"], pl["whole"], pl["split"]
+    units = split * kbt
     seen, holders = set(), {}
     for j in range(grid):
-        frags = _mixed_fragments(nkb, grid, 0, tiles, j)
-        assert frags, "every CTA owns at least one k-block"
-        for f, (tile, kb0, kb1) in enumerate(frags):
+        for f, (tile, kb0, kb1) in enumerate(_mixed_fragments(kbt, grid, whole, split, j)):
             for kb in range(kb0, kb1):
                 assert (tile, kb) not in seen
                 seen.add((tile, kb))
-            holders.setdefault(tile, []).append((j, f))
-    assert len(seen) == units
+            if tile < split:
+                holders.setdefault(tile, []).append((j, f))
+    assert len(seen) == tiles * kbt
     for tile, hs in holders.items():
-        c_first, c_last = ((tile * nkb + 1) * grid - 1) // units, ((tile * nkb + nkb) * grid - 1) // units
+        c_first, c_last = ((tile * kbt + 1) * grid - 1) // units, ((tile * kbt + kbt) * grid - 1) // units
         assert [c for c, _ in hs] == list(range(c_first, c_last + 1))
-        f_first = tile - (c_first * units // grid) // nkb
+        f_first = tile - (c_first * units // grid) // kbt
         for c, f in hs:
-            assert (f_first if c == c_first else 0) == f < maxfrag
+            assert (f_first if c == c_first else 0) == f < pl["maxfrag"]
 
 
 def _kwalk(kbt, early, u0, u1):
