@@ -68,28 +68,34 @@ constexpr int kFirstConv = 4;
 constexpr int kFirstEpi = kFirstConv + 16;   // warps 20..23
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kDrainPolls = 1u << 22;
+constexpr uint64_t kSettleNs = 20000;      // abort path of a pair: the partner's copies land meanwhile
 
-// Two configurations.  Up to 64 tokens (weight streaming): 256-wide k-blocks
-// of 128-byte code rows, the halves of a k-block issued by two MMA issuers.
-// 128-token tiles (more tokens; the MMA is the bound): 128-wide k-blocks of
-// 64-byte code rows (64-byte swizzle), one issuer, 4 activation stages of
-// 32 KB.  Either way a k-block is dequantized in two halves, each into a TMEM
-// slot of BK/4 columns, by 16 converter warps, one per (half, quarter, TMEM
-// lane quarter).
-template <int NT>
+// Two configurations, both with 256-wide k-blocks of 128-byte code rows,
+// each dequantized in two halves into TMEM slots of 64 columns by 16
+// converter warps, one per (half, 64-wide quarter, TMEM lane quarter).  Up to
+// 64 tokens (weight streaming) two MMA issuers take the halves, with a
+// full/empty barrier pair per half.  128-token tiles run on CTA pairs (256
+// weight rows, the tokens split 64/64 between the two CTAs' shared memory)
+// with one issuer and one barrier pair per k-block: a barrier wait or a
+// commit of the issuing thread costs about as much as an MMA at N = 128, and
+// the tensor pipe idles while it runs, so the fewer per MMA the better.
+template <int NT, bool PAIR = false>
 struct TCfg {
+  static_assert(!PAIR || NT == 128, "CTA pairs take 128-token tiles");
+  static constexpr int CL = PAIR ? 2 : 1;                       // CTAs per tile
   static constexpr bool DECODE = NT <= 64;
-  static constexpr int BK = DECODE ? 256 : 128;                 // K per k-block
+  static constexpr int BK = 256;                                // K per k-block
   static constexpr int SUB = BK / 64;                           // 64-wide sub-blocks (one scale tile each)
   static constexpr int CPQ = BK / 128;                          // 32-element code chunks per quarter
   static constexpr int NI = DECODE ? 2 : 1;                     // MMA issuers
   static constexpr uint32_t CODE_ROW = BK / 2;                  // code bytes of a weight row per k-block
-  static constexpr uint32_t SUB_X = NT * 128;                   // NT rows x 64 f16, 128-byte swizzle
+  static constexpr int XROWS = NT / CL;                         // token rows staged by one CTA
+  static constexpr uint32_t SUB_X = XROWS * 128;                // XROWS rows x 64 f16, 128-byte swizzle
   static constexpr uint32_t X_BYTES = SUB * SUB_X;              // one activation stage
   static constexpr uint32_t WC_BYTES = 128 * CODE_ROW;
   static constexpr uint32_t WS_BYTES = SUB * 512;               // 128x4 scale tiles
   static constexpr uint32_t W_BYTES = WC_BYTES + WS_BYTES;      // one weight stage (a multiple of 1024)
-  static constexpr int XSTAGES = NT == 64 ? 3 : 4;
+  static constexpr int XSTAGES = NT <= 32 ? 4 : NT == 64 ? 3 : PAIR ? 4 : 2;
   static constexpr uint32_t BAR_BYTES = 1024;
   static constexpr int WSTAGES_FIT = (int)((224u * 1024 - XSTAGES * X_BYTES - BAR_BYTES - 1024) / W_BYTES);
   static constexpr int WSTAGES = WSTAGES_FIT > 16 ? 16 : WSTAGES_FIT;
@@ -148,13 +154,13 @@ __device__ __forceinline__ void scales_to_h2(uint32_t two, uint32_t &s0, uint32_
   s1 = __byte_perm(r, 0, 0x3232);
 }
 
-template <int NT>
+template <int NT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_tmem_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                       const TArgs p) {
-  using C = TCfg<NT>;
+  using C = TCfg<NT, PAIR>;
   constexpr int WST = C::WSTAGES, XST = C::XSTAGES, DST = C::DSTAGES;
-  constexpr int BK = C::BK, SUB = C::SUB, NI = C::NI, CPQ = C::CPQ;
+  constexpr int BK = C::BK, SUB = C::SUB, NI = C::NI, CPQ = C::CPQ, CL = C::CL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto st_x = [&](int r) { return base + r * C::X_BYTES; };
@@ -174,6 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // In a pair, rank 0 (the leader) issues the pair's MMAs and owns the
+  // barriers that both CTAs' activation copies and dequantized slots
+  // complete on; the leader's commits release both CTAs' stages.
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  auto in_cta = [&](const void *v, uint32_t r) { return ptx::map_to_cta(ptx::smem_u32(v), r); };
+  const int cluster = blockIdx.x / CL;
   pdl_trigger();
   if (threadIdx.x == 0) {
     for (int r = 0; r < WST; ++r) {
@@ -185,12 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&xempty[r], NI);      // one commit per issuer
     }
     for (int d = 0; d < DST; ++d) {
-      ptx::mbar_init(&dfull[d], 8);        // the eight warps converting a half
+      // per half (two issuers): its eight converter warps; per k-block (one
+      // issuer): all sixteen (of both CTAs of a pair)
+      ptx::mbar_init(&dfull[d], (NI == 2 ? 8 : 16) * CL);
       ptx::mbar_init(&dempty[d], 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], NI);       // one commit per issuer
-      ptx::mbar_init(&tempty[b], 128);
+      ptx::mbar_init(&tempty[b], 4 * CL);  // one arrival per epilogue warp (of the pair)
       ptx::mbar_init(&drain[b], 1);
     }
     *abort_flag = 0;
@@ -202,7 +217,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // starts streaming at once; the others wait until the barriers and the
   // TMEM allocation are in place.
   uint32_t tmem = 0;
-  if (warp == kWarpProdW) {
+  if constexpr (PAIR) {
+    // both CTAs' barriers and the pair's TMEM exist before any remote arrival
+    if (warp == kWarpMma0) {
+      ptx::tmem_alloc_pair(tslot, C::TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    tmem = *tslot;
+  } else if (warp == kWarpProdW) {
     __syncwarp();
     asm volatile("bar.arrive 1, %0;" ::"r"(kThreads) : "memory");
   } else {
@@ -228,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto give_up = [&]() {
     *abort_flag = 1;
     atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+    if constexpr (PAIR) ptx::st_cluster_u32(in_cta(const_cast<const int *>(abort_flag), rank ^ 1u), 1u);
   };
 
   if (warp == kWarpProdW) {
@@ -236,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = ptx::l2_policy_evict_first();
       int r = 0;
       uint32_t ph = 0;
-      MixedIter mi(mixed, blockIdx.x);
+      MixedIter mi(mixed, cluster);
       int tile, kb0, kb1;
       bool ok = true;
       while (ok && !*abort_flag && mi.next(tile, kb0, kb1)) {
@@ -247,10 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t sfb = (uint32_t)nsub_of(kb) * 512u;   // scales only of the sub-blocks K has
-          ptx::mbar_arrive_expect_tx(&wfull[r], C::WC_BYTES + sfb);
-          const int wt = tile / p.ttiles;
-          ptx::tma_load_2d(st_wc(r), &tm_w, &wfull[r], kb * (BK / 2), wt * 128, pol_w);
-          ptx::bulk_load(st_ws(r), p.wsf + ((size_t)wt * cp4 + kb * SUB) * 512, sfb, &wfull[r], pol_w);
+          const int rb = (tile / p.ttiles) * CL + (int)rank;      // this CTA's 128-row weight block
+          if (rb * 128 < p.n) {
+            ptx::mbar_arrive_expect_tx(&wfull[r], C::WC_BYTES + sfb);
+            ptx::tma_load_2d(st_wc(r), &tm_w, &wfull[r], kb * (BK / 2), rb * 128, pol_w);
+            ptx::bulk_load(st_ws(r), p.wsf + ((size_t)rb * cp4 + kb * SUB) * 512, sfb, &wfull[r], pol_w);
+          } else {
+            ptx::mbar_arrive(&wfull[r]);   // rows past N (the pair's second half): nothing to load
+          }
           issued_w |= 1u << r;
           issued_w_par = (issued_w_par & ~(1u << r)) | (ph << r);
           if (++r == WST) { r = 0; ph ^= 1u; }
@@ -264,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = ptx::l2_policy_evict_last();
       int r = 0;
       uint32_t ph = 0;
-      MixedIter mi(mixed, blockIdx.x);
+      MixedIter mi(mixed, cluster);
       int tile, kb0, kb1;
       bool ok = true;
       while (ok && !*abort_flag && mi.next(tile, kb0, kb1)) {
@@ -274,13 +304,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&xfull[r], C::X_BYTES);
+          // this CTA's XROWS token rows; in a pair both halves land on the leader's barrier
+          if (leader) ptx::mbar_arrive_expect_tx(&xfull[r], CL * C::X_BYTES);
+          const int x_row = (tile % p.ttiles) * NT + (int)rank * C::XROWS;
 #pragma unroll
-          for (int sb = 0; sb < SUB; ++sb)    // a sub-block past K reads zeros
-            ptx::tma_load_2d(st_x(r) + sb * C::SUB_X, &tm_x, &xfull[r], (kb * SUB + sb) * 128,
-                             (tile % p.ttiles) * NT, pol_x);
-          issued_x |= 1u << r;
-          issued_x_par = (issued_x_par & ~(1u << r)) | (ph << r);
+          for (int sb = 0; sb < SUB; ++sb) {  // a sub-block past K reads zeros
+            if (PAIR && !leader)
+              ptx::tma_load_2d_to_pair_bar(st_x(r) + sb * C::SUB_X, &tm_x, in_cta(&xfull[r], 0),
+                                           (kb * SUB + sb) * 128, x_row, pol_x);
+            else
+              ptx::tma_load_2d(st_x(r) + sb * C::SUB_X, &tm_x, &xfull[r], (kb * SUB + sb) * 128, x_row, pol_x);
+          }
+          if (leader) {   // (a pair partner's copies complete on the leader's barrier)
+            issued_x |= 1u << r;
+            issued_x_par = (issued_x_par & ~(1u << r)) | (ph << r);
+          }
           if (++r == XST) { r = 0; ph ^= 1u; }
         }
       }
@@ -289,13 +327,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA
     // issuer hi issues the halves h of every k-block with h % NI == hi
     const int hi = warp == kWarpMma0 ? 0 : 1;
-    if (hi < NI && ptx::elect_one()) {
+    // commit: the MMAs so far have completed -> arrive on this barrier (of both CTAs of a pair)
+    auto commit = [&](uint64_t *bar) {
+      if constexpr (PAIR) {
+        ptx::tc_commit_pair(ptx::smem_u32(bar));
+        ptx::tc_commit_pair(in_cta(bar, 1));
+      } else {
+        ptx::tc_commit(bar);
+      }
+    };
+    if (leader && hi < NI && ptx::elect_one()) {
       // kind::f16: F32 accumulator (bits 4-5 = 1), A = B = F16 (0), K-major,
-      // N >> 3 in bits 17-22, M = 128 >> 4 in bits 24-28
-      constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | (8u << 24);
+      // N >> 3 in bits 17-22, M (128 per CTA) >> 4 in bits 24-28
+      constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(8 * CL) << 24);
       int xr = 0, it = 0, i = 0;
       uint32_t xph = 0;
-      MixedIter mi(mixed, blockIdx.x);
+      MixedIter mi(mixed, cluster);
       int tile, kb0, kb1;
       bool ok = true;
       for (; ok && !*abort_flag && mi.next(tile, kb0, kb1); ++it) {
@@ -313,35 +360,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-#pragma unroll
-          for (int h = hi; h < 2; h += NI) {
-            const int j = 2 * i + h, d = j % DST;
-            const uint32_t dph = (uint32_t)((j / DST) & 1);
-            if (!ptx::mbar_wait_bounded(&dfull[d], dph, limit, kTimeoutNs, abort_flag)) {
+          // one issuer: both halves' slots are ready together (one barrier per k-block)
+          const int ek = (2 * i) % DST;
+          const uint32_t eph = (uint32_t)(((2 * i) / DST) & 1);
+          if (NI == 1) {
+            if (!ptx::mbar_wait_bounded(&dfull[ek >> 1], eph, limit, kTimeoutNs, abort_flag)) {
               give_up();
               ok = false;
               break;
             }
             ptx::tc_fence_after();
+          }
+#pragma unroll
+          for (int h = hi; h < 2; h += NI) {
+            const int j = 2 * i + h, d = j % DST;
+            const uint32_t dph = (uint32_t)((j / DST) & 1);
+            if (NI == 2) {
+              if (!ptx::mbar_wait_bounded(&dfull[d], dph, limit, kTimeoutNs, abort_flag)) {
+                give_up();
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+            }
             const uint32_t xs = ptx::smem_u32(st_x(xr)) + (uint32_t)(h * (SUB / 2)) * C::SUB_X;
             const uint32_t wa = tmem + a_col(d);
             const int ns = nsub_half(kb, h);
             for (int sb = 0; sb < ns; ++sb)
 #pragma unroll
               for (int jj = 0; jj < 4; ++jj) {
-                ptx::mma_f16_tmem_a(acc, wa + 8 * (4 * sb + jj),
-                                    ptx::smem_desc(xs + sb * C::SUB_X + 32 * jj, 16, 1024, 2), idesc, !first);
+                const uint64_t bd = ptx::smem_desc(xs + sb * C::SUB_X + 32 * jj, 16, 1024, 2);
+                if constexpr (PAIR)
+                  ptx::mma_f16_tmem_a_pair(acc, wa + 8 * (4 * sb + jj), bd, idesc, !first);
+                else
+                  ptx::mma_f16_tmem_a(acc, wa + 8 * (4 * sb + jj), bd, idesc, !first);
                 first = false;
               }
             mma_issued = true;
-            ptx::tc_commit(&dempty[d]);
+            if (NI == 2) commit(&dempty[d]);
           }
           if (!ok) break;
-          ptx::tc_commit(&xempty[xr]);
+          if (NI == 1) commit(&dempty[ek >> 1]);
+          commit(&xempty[xr]);
           if (++xr == XST) { xr = 0; xph ^= 1u; }
         }
         if (!ok) break;
-        ptx::tc_commit(&tfull[ab]);          // also when this issuer had nothing to add
+        commit(&tfull[ab]);                  // also when this issuer had nothing to add
       }
     }
   } else if (warp < kFirstEpi) {
@@ -360,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int swz = C::CODE_ROW == 128 ? (row & 7) : ((row >> 1) & 3);
     const uint32_t sf_off = (uint32_t)(sb * 512 + (row & 31) * 16 + (row >> 5) * 4);
     const uint32_t c_off = (uint32_t)(row * C::CODE_ROW);
-    MixedIter mi(mixed, blockIdx.x);
+    MixedIter mi(mixed, cluster);
     int tile, kb0, kb1;
     int i = 0, wr = 0;
     uint32_t wph = 0;
@@ -369,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = kb0; kb < kb1; ++kb, ++i) {
         const int j = 2 * i + h, d = j % DST;
         const uint32_t dph = (uint32_t)((j / DST) & 1);
-        bool got = ptx::mbar_wait_bounded(&dempty[d], dph ^ 1u, limit, kTimeoutNs, abort_flag);
+        const int bi = NI == 2 ? d : d >> 1;   // its slot's barriers: per half, or per k-block
+        bool got = ptx::mbar_wait_bounded(&dempty[bi], dph ^ 1u, limit, kTimeoutNs, abort_flag);
         if (got) got = ptx::mbar_wait_bounded(&wfull[wr], wph, limit, kTimeoutNs, abort_flag);
         if (__any_sync(0xffffffffu, !got)) {   // the warp leaves together
           give_up();
@@ -403,7 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&dfull[d]);
+        if (lane == 0) {
+          if (PAIR && !leader) ptx::mbar_arrive_remote(in_cta(&dfull[bi], 0));
+          else ptx::mbar_arrive(&dfull[bi]);
+        }
       }
     }
   } else {
@@ -431,12 +499,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 16; ++x) o[x] += __uint_as_float(v[x]);
       }
     };
+    // accumulator buffer ab read: free it for the next tile (the leader's barrier in a pair)
+    auto release_acc = [&](int ab) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR && !leader) ptx::mbar_arrive_remote(in_cta(&tempty[ab], 0));
+        else ptx::mbar_arrive(&tempty[ab]);
+      }
+    };
     // bf16(alpha * v * 2^-e) of token row t (< m)
     auto out_bits = [&](float v, int t) {
       const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v * __ldg(p.rs + t));
       return *reinterpret_cast<const uint16_t *>(&o);
     };
-    MixedIter mi(mixed, blockIdx.x);
+    MixedIter mi(mixed, cluster);
     int tile, kb0, kb1;
     for (; mi.next(tile, kb0, kb1); ++it) {
       const int ab = it & 1;
@@ -444,13 +521,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!got) give_up();
       if (ptx::bar_any(2, 128, !got || *abort_flag)) break;   // the four warps leave together
       ptx::tc_fence_after();
-      const int n = (tile / p.ttiles) * 128 + row;
+      const int n = ((tile / p.ttiles) * CL + (int)rank) * 128 + row;
       const int t0 = (tile % p.ttiles) * NT;  // first token row of the tile
       const int mt = min(p.m - t0, NT);
       const bool p1 = NI > 1 && nsub_of(kb0) > SUB / 2;   // issuer 1 added half 1 of some k-block
       const bool split_tile = mixed.is_split(tile);
-      const int64_t c_first = split_tile ? mixed.cta_of((int64_t)tile * p.nkb) : blockIdx.x;
-      const int64_t c_last = split_tile ? mixed.cta_of((int64_t)tile * p.nkb + p.nkb - 1) : blockIdx.x;
+      const int64_t c_first = split_tile ? mixed.cta_of((int64_t)tile * p.nkb) : cluster;
+      const int64_t c_last = split_tile ? mixed.cta_of((int64_t)tile * p.nkb + p.nkb - 1) : cluster;
       if (c_last == c_first) {
 #pragma unroll 1
         for (int c = 0; c < NT / 16; ++c) {
@@ -462,17 +539,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (16 * c + x < mt) p.d[(size_t)(t0 + 16 * c + x) * p.n + n] = out_bits(v[x], t0 + 16 * c + x);
           }
         }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&tempty[ab]);
+        release_acc(ab);
         continue;
       }
       // partial slot of contributor cc: its fragment index is 0 except for
       // c_first (every later contributor's run starts inside this tile)
       const int f_first = tile - (int)(mixed.start(c_first) / p.nkb);
       auto slot = [&](int64_t cc) {
-        return p.partials + ((size_t)cc * p.maxfrag + (cc == c_first ? f_first : 0)) * NT * 128;
+        return p.partials + (((size_t)cc * p.maxfrag + (cc == c_first ? f_first : 0)) * CL + rank) * NT * 128;
       };
-      float *mine = slot(blockIdx.x);
+      float *mine = slot(cluster);
 #pragma unroll 1
       for (int c = 0; c < NT / 16; ++c) {
         float v[16];
@@ -481,14 +557,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 16; ++x)
           if (16 * c + x < mt) mine[(16 * c + x) * 128 + row] = v[x];
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&tempty[ab]);
+      release_acc(ab);
       epi_bar();                    // every partial write of the CTA precedes the release below
       if (et == 0)
-        *last_flag = atom_add_acq_rel_gpu(&p.counters[tile], 1) == (uint32_t)(c_last - c_first);
+        *last_flag = atom_add_acq_rel_gpu(&p.counters[tile * CL + (int)rank], 1) == (uint32_t)(c_last - c_first);
       epi_bar();
       if (!*last_flag) continue;
-      if (et == 0) p.counters[tile] = 0;
+      if (et == 0) p.counters[tile * CL + (int)rank] = 0;
 #pragma unroll 1
       for (int g0 = 0; g0 < mt; g0 += TG) {
         float acc[TG];
@@ -532,14 +607,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if ((warp == kWarpMma0 || warp == kWarpMma1) && mma_issued) {
       uint64_t *dr = &drain[warp == kWarpMma0 ? 0 : 1];
-      ptx::tc_commit(dr);
+      if constexpr (PAIR) ptx::tc_commit_pair(ptx::smem_u32(dr));
+      else ptx::tc_commit(dr);
       ptx::mbar_wait_bounded(dr, 0, kDrainPolls, 0, &no_abort);
+    }
+    if (PAIR && threadIdx.x == 0) {
+      // some of a pair CTA's copies complete on the other CTA's barrier: a
+      // short settle time covers those
+      const uint64_t t0 = ptx::globaltimer();
+      while (ptx::globaltimer() - t0 < kSettleNs) __nanosleep(1000);
     }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();   // the partner's MMAs and copies no longer touch this CTA
+  else __syncthreads();
   ptx::tc_fence_after();
-  if (warp == kWarpMma0) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == kWarpMma0) {
+    if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
 }
 
 // Token rows of x (times the AWQ pre-scale s when given, rounded to bf16 as
@@ -627,24 +713,25 @@ int pick_nt(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128
 // Work split and workspace layout of one call: [arrival counters |
 // fp32 partials of shared tiles | f16 activations | row scales].
 struct TPlan {
-  int nt, wtiles, ttiles, nkb, grid, maxfrag, whole, split_tiles;
+  int nt, cl, wtiles, ttiles, nkb, grid, maxfrag, whole, split_tiles;   // grid: CTA clusters (pairs or single CTAs)
   size_t x16_off, rs_off, ws_bytes;
 };
 
 TPlan make_tplan(int64_t m, int64_t n, int64_t k) {
   TPlan pl{};
   pl.nt = pick_nt(m);
+  pl.cl = pl.nt == 128 ? 2 : 1;          // 128-token tiles: CTA pairs, 256 weight rows per tile
   const int bk = pl.nt <= 64 ? TCfg<16>::BK : TCfg<128>::BK;
-  pl.wtiles = (int)((n + 127) / 128);
+  pl.wtiles = (int)((n + 128 * pl.cl - 1) / (128 * pl.cl));
   pl.ttiles = (int)((m + pl.nt - 1) / pl.nt);
   pl.nkb = (int)((k + bk - 1) / bk);     // the last k-block may be narrower (64-wide steps)
   const int tiles = pl.wtiles * pl.ttiles;
-  const int sms = num_sms();
+  const int units = num_sms() / pl.cl;   // clusters that fit, one CTA per SM
   const int64_t w = (int64_t)tiles * pl.nkb;
-  pl.grid = (int)(w < sms ? w : sms);
-  // every CTA gets `whole` whole tiles; the remaining tiles are cut into one
-  // contiguous run of (tile, k-block) pairs per CTA, and every CTA must own
-  // at least one k-block of them when there are any
+  pl.grid = (int)(w < units ? w : units);
+  // every cluster gets `whole` whole tiles; the remaining tiles are cut into
+  // one contiguous run of (tile, k-block) pairs per cluster, and every cluster
+  // must own at least one k-block of them when there are any
   pl.whole = tiles / pl.grid;
   pl.split_tiles = tiles - pl.whole * pl.grid;
   if (pl.whole > 0 && pl.split_tiles > 0 && (int64_t)pl.split_tiles * pl.nkb < pl.grid) {
@@ -655,31 +742,30 @@ TPlan make_tplan(int64_t m, int64_t n, int64_t k) {
   const int64_t per = (su + pl.grid - 1) / pl.grid;
   pl.maxfrag = (int)((per + pl.nkb - 1) / pl.nkb + 1);
   const bool shared = su > 0 && ((su % pl.grid != 0) || ((su / pl.grid) % pl.nkb != 0));
-  const size_t part_bytes = shared ? (size_t)pl.grid * pl.maxfrag * pl.nt * 128 * 4 : 0;
+  const size_t part_bytes = shared ? (size_t)pl.grid * pl.maxfrag * pl.cl * pl.nt * 128 * 4 : 0;
   pl.x16_off = kCounterArea + round256(part_bytes);
   pl.rs_off = pl.x16_off + round256((size_t)(m * k * 2));
   pl.ws_bytes = pl.rs_off + round256((size_t)m * 4);
   return pl;
 }
 
-template <int NT>
+template <int NT, bool PAIR>
 cudaError_t launch_nt(const TPlan &pl, const uint16_t *x, const uint16_t *pre, const uint8_t *w, const uint8_t *wsf,
                       const float *alpha, uint16_t *d, int64_t m, int64_t n, int64_t k, uint8_t *ws,
                       uint32_t wait_limit, cudaStream_t st) {
-  using C = TCfg<NT>;
+  using C = TCfg<NT, PAIR>;
   static PerDeviceOnce smem_attr;   // the shared-memory limit is a setting of each device's context
   if (cudaError_t e = smem_attr.run([] {
-        return cudaFuncSetAttribute(w4a16_tmem_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(w4a16_tmem_kernel<NT, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)C::SMEM_BYTES);
       }))
     return e;
   uint16_t *x16 = reinterpret_cast<uint16_t *>(ws + pl.x16_off);
   float *rs = reinterpret_cast<float *>(ws + pl.rs_off);
   CUtensorMap tm_x, tm_w;
-  // f16 activations [m, k]: box 128 bytes (64 elements) x NT rows, 128-byte swizzle;
-  // weight codes [n, k/2]: box 128 bytes x 128 rows, 128-byte swizzle
+  // f16 activations [m, k]: box 128 bytes (64 elements) x XROWS rows, 128-byte swizzle;
   // weight codes [n, k/2]: box BK/2 bytes x 128 rows, swizzled as wide as the box
-  if (!make_byte_map(&tm_x, x16, m, k * 2, 128, NT, 128) ||
+  if (!make_byte_map(&tm_x, x16, m, k * 2, 128, C::XROWS, 128) ||
       !make_byte_map(&tm_w, w, n, k / 2, C::CODE_ROW, 128, (int)C::CODE_ROW))
     return cudaErrorInvalidValue;
   TArgs a{};
@@ -705,7 +791,23 @@ cudaError_t launch_nt(const TPlan &pl, const uint16_t *x, const uint16_t *pre, c
   if (cudaError_t e =
           launch_pdl(w4a16_act_f16_kernel, dim3((unsigned)m), dim3(kPrepThreads), 0, st, x, pre, k, x16, rs))
     return e;
-  return launch_pdl(w4a16_tmem_kernel<NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_x, tm_w, a);
+  if constexpr (!PAIR)
+    return launch_pdl(w4a16_tmem_kernel<NT, PAIR>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_x, tm_w, a);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C::CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(a.grid * C::CL);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, w4a16_tmem_kernel<NT, PAIR>, tm_x, tm_w, a);
 }
 
 }  // namespace
@@ -727,10 +829,10 @@ cudaError_t launch_w4a16_tmem(const uint16_t *x, const uint16_t *pre_scale, cons
   if (!ws || ws_bytes < pl.ws_bytes) return cudaErrorInvalidValue;
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   switch (pl.nt) {
-    case 16: return launch_nt<16>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
-    case 32: return launch_nt<32>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
-    case 64: return launch_nt<64>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
-    default: return launch_nt<128>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+    case 16: return launch_nt<16, false>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+    case 32: return launch_nt<32, false>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+    case 64: return launch_nt<64, false>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
+    default: return launch_nt<128, true>(pl, x, pre_scale, w, wsf, alpha, d, m, n, k, wsb, wait_limit, st);
   }
 }
 

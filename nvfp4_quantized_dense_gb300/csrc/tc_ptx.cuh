@@ -347,6 +347,22 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// The same for a CTA pair (cta_group::2, issued by the pair's even CTA): A
+// is M = 256 rows, each CTA's 128 in its own TMEM at a_tmem; B is N rows,
+// each CTA holding N/2 of them at the same shared-memory offset; each CTA's
+// TMEM receives the accumulator of its own 128 rows.
+__device__ __forceinline__ void mma_f16_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                    uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
 // Copy a 32-row x 16-byte block from shared memory to TMEM, replicated into
 // the four 32-lane sub-partitions (4 TMEM columns starting at taddr).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {

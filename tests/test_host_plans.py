@@ -10,9 +10,11 @@ every CTA takes floor(tiles/grid) whole tiles, the other tiles are cut into
 one contiguous run of (tile, k-block) pairs per CTA, and when those shared
 tiles have fewer k-blocks than there are CTAs one round of whole tiles joins
 them.  W4A16 tensor-core GEMM (the TMEM kernel, given its workspace): tiles of
-128 weight rows x 16/32/64/128 tokens, split as the swap-AB kernel without
-clusters (whole tiles last); its scratch is the counter area, the fp32
-partials [grid][fragment slots][tokens padded][128] when a tile is shared,
+128 weight rows x 16/32/64 tokens per CTA, or 256 weight rows x 128 tokens
+per CTA pair, split as the swap-AB kernel without clusters (whole tiles
+last, over the clusters); its scratch is the counter area, the fp32
+partials [clusters][fragment slots][pair CTA][tokens padded][128] when a
+tile is shared,
 the f16 activations [m][k] and the fp32 row scales [m], each rounded up to
 256 bytes.  The whole-MLP decode kernel plans both of its GEMM phases the
 swap-AB way on one grid (the smaller of the SM count and either phase's
@@ -100,16 +102,23 @@ def mixed_plan(tiles, kbt, sms, nt):
                 part=grid * maxfrag * nt * 128 * 4 if shared else 0)
 
 
-def w4a16_ws(m, n, k, sms):
-    """The W4A16 TMEM kernel's scratch: token tiles of 16/32/64 (256-wide
-    k-blocks) or 128 (128-wide k-blocks), tiles = weight tiles x token
-    tiles, the mixed split; counters, partials, the f16 activations [m][k]
-    and the fp32 row scales [m], each rounded up to 256 bytes."""
+def w4a16_tiles(m, n, k, sms):
+    """The W4A16 TMEM kernel's tiling: 256-wide k-blocks; token tiles of
+    16/32/64 (one CTA, 128 weight rows) or 128 (a CTA pair, 256 weight rows);
+    tiles = weight tiles x token tiles over the SMs' clusters."""
     nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
-    bk = 256 if nt <= 64 else 128
-    tiles = math.ceil(n / 128) * math.ceil(m / nt)
-    pl = mixed_plan(tiles, math.ceil(k / bk), sms, nt)
-    return COUNTER_AREA + r256(pl["part"]) + r256(m * k * 2) + r256(m * 4)
+    cl = 2 if nt == 128 else 1
+    tiles = math.ceil(n / (128 * cl)) * math.ceil(m / nt)
+    return nt, cl, tiles, math.ceil(k / 256), sms // cl
+
+
+def w4a16_ws(m, n, k, sms):
+    """The W4A16 TMEM kernel's scratch: counters, the partials of the mixed
+    split (one [tokens][128] slot per CTA of a cluster), the f16 activations
+    [m][k] and the fp32 row scales [m], each rounded up to 256 bytes."""
+    nt, cl, tiles, kbt, units = w4a16_tiles(m, n, k, sms)
+    pl = mixed_plan(tiles, kbt, units, nt)
+    return COUNTER_AREA + r256(pl["part"] * cl) + r256(m * k * 2) + r256(m * 4)
 
 
 SWAP_CASES = [
@@ -302,10 +311,8 @@ def test_w4a16_reduction_bookkeeping(m, n, k, sms):
     whole tiles last) keeps the swap-AB split's invariants: every (tile,
     k-block) covered once, a shared tile's contributors contiguous, each
     contributor's partial slot its fragment's index below maxfrag."""
-    nt = 16 if m <= 16 else 32 if m <= 32 else 64 if m <= 64 else 128
-    kbt = math.ceil(k / (256 if nt <= 64 else 128))
-    tiles = math.ceil(n / 128) * math.ceil(m / nt)
-    pl = mixed_plan(tiles, kbt, sms, nt)
+    nt, cl, tiles, kbt, units = w4a16_tiles(m, n, k, sms)
+    pl = mixed_plan(tiles, kbt, units, nt)
     grid, whole, split = pl["grid"], pl["whole"], pl["split"]
     units = split * kbt
     seen, holders = set(), {}
