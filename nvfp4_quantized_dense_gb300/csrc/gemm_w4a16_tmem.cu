@@ -259,7 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProdW) {
     // ---------------------------------------------------- weight producer
     if (ptx::elect_one()) {
-      const uint64_t pol_w = ptx::l2_policy_evict_first();
+      // a weight tile read once (one token tile) need not stay in L2; with
+      // several token tiles the cluster reads it again for each, back to back
+      const uint64_t pol_w = p.ttiles == 1 ? ptx::l2_policy_evict_first() : ptx::l2_policy_evict_normal();
       int r = 0;
       uint32_t ph = 0;
       MixedIter mi(mixed, cluster);
