@@ -250,12 +250,13 @@ nvfp4_status nvfp4_gemm_swiglu_quant_per_token(const uint8_t *a_fp4, const uint8
  *              always, above when whole 128-row weight tiles would leave SMs
  *              idle (the counters are left at zero after every complete call;
  *              calls sharing it must be stream-ordered); with less, every SM
- *              owns whole weight tiles.  Up to 64 tokens the workspace also
- *              selects the TMEM kernel: the weights are dequantized to f16
- *              in tensor memory and the activations are written into the
- *              workspace by a pre-pass as f16 times a power of two 2^e per
- *              token row (e puts the row's largest finite magnitude in
- *              [2^15, 2^16); the epilogue multiplies by 2^-e).  That is exact
+ *              owns whole weight tiles.  The workspace also selects the
+ *              TMEM kernel: the weights are dequantized to f16 in tensor
+ *              memory (128-token tiles on CTA pairs) and the activations
+ *              are written into the workspace by a pre-pass as f16 times a
+ *              power of two 2^e per token row (e puts the row's largest
+ *              finite magnitude in [2^15, 2^16); the epilogue multiplies by
+ *              2^-e).  That is exact
  *              for every activation within 2^30 of its row's largest
  *              magnitude (smaller ones are rounded by at most 2^-25 * 2^-e),
  *              so the result depends on the workspace only through the

@@ -1,9 +1,9 @@
 // W4A16 GEMM on the tensor cores: bf16 activations x NVFP4 weights
 // ([P3] fp4_gemm with quant_mode "w4a16": the activation is not quantized,
-// alpha holds only the weight dequant factor).  This is the kernel for more
-// than 64 tokens, and for any token count when the caller gives no
-// workspace; up to 64 tokens with a workspace the TMEM kernel
-// (gemm_w4a16_tmem.cu) runs instead.
+// alpha holds only the weight dequant factor).  This is the kernel for
+// calls without a workspace; with one the TMEM kernel (gemm_w4a16_tmem.cu)
+// runs instead.  (Its split-K planning below still serves that case's
+// whole-tile grid.)
 //
 // The tensor cores need both operands of a kind::f16 MMA in the same type,
 // so the weight is dequantized to bf16 in shared memory: converter warps read

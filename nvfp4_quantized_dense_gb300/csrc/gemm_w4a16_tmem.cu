@@ -1,6 +1,7 @@
-// W4A16 GEMM at decode sizes (up to 64 tokens): bf16 activations x NVFP4
-// weights ([P3] fp4_gemm with quant_mode "w4a16"), the dequantized weight
-// tiles held in tensor memory.
+// W4A16 GEMM on the tensor cores: bf16 activations x NVFP4 weights ([P3]
+// fp4_gemm with quant_mode "w4a16"), the dequantized weight tiles held in
+// tensor memory; 16/32/64-token tiles on one CTA (decode), 128-token tiles on
+// CTA pairs.
 //
 // Why TMEM.  A 128-row x 128-wide block of weights is 9 KB of codes and
 // scales in HBM but 32 KB once dequantized to 16 bits.  Written to shared
@@ -42,8 +43,9 @@
 //
 // Roles (768 threads, one CTA per SM): warp 0 weight producer, warp 3
 // activation producer, warps 1 (also TMEM owner) and 2 the MMA issuers of
-// halves 0 and 1 (at decode sizes one thread issuing every MMA would bound
-// the kernel), each accumulating into its own TMEM columns; warps 4..19
+// halves 0 and 1 at decode sizes (one thread issuing every MMA would bound
+// the kernel; 128-token tiles: warp 1 alone), each accumulating into its own
+// TMEM columns; warps 4..19
 // converters, one per (half, 64-wide quarter, TMEM lane quarter): warp w
 // writes TMEM lanes 32(w%4) .. 32(w%4)+31 (the lanes a warp may access), one
 // weight row per thread, and every converter warp visits every k-block, so

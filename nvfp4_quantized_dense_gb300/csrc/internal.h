@@ -120,16 +120,15 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
                           int64_t k, void *workspace, size_t ws_bytes, uint32_t wait_limit,
                           cudaStream_t st, const float *a_row_scale = nullptr);
 
-// W4A16 on the tensor cores.  Up to 64 tokens, given a workspace of
-// w4a16_workspace_bytes (16-byte aligned, zero-filled once; counters left at
-// zero), the TMEM kernel runs: weights dequantized to f16 into tensor memory,
-// activations turned into f16 with a power-of-two scale per row by a
-// pre-pass into the workspace (times the AWQ pre-scale when pre_scale is
-// given), work split along K over all SMs.  Otherwise the shared-memory
-// kernel runs (weights dequantized to bf16 in shared memory; split along K
-// up to 64 tokens always and above when whole weight tiles would leave SMs
-// idle, given its workspace; whole tiles per CTA without one); it takes no
-// pre_scale (the caller scales the activations first).
+// W4A16 on the tensor cores.  Given a workspace of w4a16_workspace_bytes
+// (16-byte aligned, its counter area zero-filled once; counters left at
+// zero), the TMEM kernel runs: weights dequantized to f16 into tensor memory
+// (128-token tiles on CTA pairs), activations turned into f16 with a
+// power-of-two scale per row by a pre-pass into the workspace (times the AWQ
+// pre-scale when pre_scale is given), the swap-AB mixed split.  Without a
+// workspace the shared-memory kernel runs (weights dequantized to bf16 in
+// shared memory, whole tiles per CTA); it takes no pre_scale (the caller
+// scales the activations first).
 bool w4a16_tc_supported(int64_t m, int64_t n, int64_t k);
 size_t w4a16_workspace_bytes(int64_t m, int64_t n, int64_t k);
 // true when launch_w4a16_tc with this workspace runs the TMEM kernel
