@@ -121,3 +121,25 @@ def test_rows_at_extreme_magnitudes_each_within_tolerance(lib, m, n, k):
     ref = oracle.gemm_w4a16(x, ws.packed, ws.sf, alpha)
     for t in range(m):
         assert_gemm_close(got[t:t + 1], ref[t:t + 1], what=f"token row {t} (scale 2^{int(np.log2(scale[t, 0]))})")
+
+
+@pytest.mark.parametrize("m,n,k", [(16, 1024, 2048), (200, 512, 1024)])
+def test_bounded_wait_gives_up_cleanly(lib, m, n, k):
+    """A wait limit of one poll makes the pipeline waits run out (one CTA per
+    tile at 16 tokens, CTA pairs at 200): the kernel records
+    NVFP4_ERR_DEVICE_TIMEOUT and returns, and the next call on a fresh
+    workspace is correct."""
+    ws = small_weights(n, k, 11)
+    xbits, x = synth.activations(4, m, k)
+    alpha = np.float32(1.0) / ws.gs
+    wd = ws.device_prepared(lib)
+    assert lib.nvfp4_get_device_status() == 0
+    lib.nvfp4_set_wait_limit(1)
+    try:
+        run_tmem(lib, xbits, wd[0], wd[1], alpha, m, n, k)
+    finally:
+        lib.nvfp4_set_wait_limit(0)
+    assert lib.nvfp4_get_device_status() == lib.ERR_DEVICE_TIMEOUT
+    assert lib.nvfp4_get_device_status() == 0          # read clears it
+    got = run_tmem(lib, xbits, wd[0], wd[1], alpha, m, n, k)
+    assert_gemm_close(got, oracle.gemm_w4a16(x, ws.packed, ws.sf, alpha))
