@@ -725,7 +725,7 @@ TPlan make_tplan(int64_t m, int64_t n, int64_t k) {
   TPlan pl{};
   pl.nt = pick_nt(m);
   pl.cl = pl.nt == 128 ? 2 : 1;          // 128-token tiles: CTA pairs, 256 weight rows per tile
-  const int bk = pl.nt <= 64 ? TCfg<16>::BK : TCfg<128>::BK;
+  const int bk = pl.nt <= 64 ? TCfg<16>::BK : TCfg<128, true>::BK;
   pl.wtiles = (int)((n + 128 * pl.cl - 1) / (128 * pl.cl));
   pl.ttiles = (int)((m + pl.nt - 1) / pl.nt);
   pl.nkb = (int)((k + bk - 1) / bk);     // the last k-block may be narrower (64-wide steps)
