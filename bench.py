@@ -459,13 +459,13 @@ def run_ours(args, world, rank, local):
 
     def launches(it):
         """Kernels one forward of each M launches: quantize + 2 GEMMs (W4A4);
-        2 GEMMs + silu_mul_bf16 (W4A16), where a tensor-core W4A16 GEMM of
-        up to 64 tokens with its workspace is the activation pre-pass + the
+        2 GEMMs + silu_mul_bf16 (W4A16), where a tensor-core W4A16 GEMM given
+        its workspace (as here, at every M) is the activation pre-pass + the
         TMEM kernel."""
         if not it.w4a16:
             return 3 * len(it.ms)
-        per_gemm = lambda m: 1 if algo == nv.ALGO_GEMV or m > 64 else 2
-        return sum(2 * per_gemm(m) + 1 for m in it.ms)
+        per_gemm = 1 if algo == nv.ALGO_GEMV else 2
+        return sum(2 * per_gemm + 1 for m in it.ms)
 
     stream = torch.cuda.Stream(device=dev)
     SH[0] = stream.cuda_stream

@@ -142,6 +142,58 @@ def test_w4a4_is_deterministic(lib, algo):
         assert int(scratch[0][: 4 * ntiles].view(torch.int32).abs().sum()) == 0
 
 
+def test_swapab_after_w4a16_on_a_shared_workspace(lib):
+    """One buffer serves a W4A16 call and then swap-AB calls, as the header
+    allows.  The W4A16 call leaves its fp32 partials and f16 activations
+    where the swap-AB kernel keeps its partial tiles (16 tiles of 16 k-blocks
+    over 128 CTAs: every tile shared by 16 CTAs); the swap-AB result must not
+    depend on them, and a second call on the same buffer is identical."""
+    m, n, k = 16, 1024, 4096
+    ws = small_weights(n, k, 4)
+    wdev = ws.device_prepared(lib)
+    nbytes = max(lib.nvfp4_workspace_bytes(m, n, k, TC_SWAPAB), lib.bf16_fp4_gemm_workspace_bytes(m, n, k, TC))
+    buf = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    xbits, _ = synth.activations(4, m, k)
+    d16 = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    lib.bf16_fp4_gemm_ex(bf16_dev(xbits), wdev[0], wdev[1], scalar(1.0), d16, m, n, k, buf, nbytes, algo=TC)
+    torch.cuda.synchronize()
+    counter_area = 64 * 1024
+    swap_need = lib.nvfp4_workspace_bytes(m, n, k, TC_SWAPAB)
+    assert int(torch.count_nonzero(buf[counter_area:swap_need])) > 0, "no leftovers where the partials go"
+    _, _, gs_x, xq, xs = quantized_activation(0, m, k)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    first = run_w4a4(lib, xq, xs, wdev, alpha, m, n, k, TC_SWAPAB, (buf, nbytes))
+    assert_gemm_close(first, oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha))
+    again = run_w4a4(lib, xq, xs, wdev, alpha, m, n, k, TC_SWAPAB, (buf, nbytes))
+    assert np.array_equal(first, again)
+
+
+# (1, 5120, 4096): 40 tiles of 16 k-blocks over 152 CTAs, runs crossing tiles
+@pytest.mark.parametrize("m,n,k", [(16, 1024, 4096), (1, 5120, 4096)])
+def test_swapab_bounded_wait_gives_up_cleanly(lib, m, n, k):
+    """A wait limit of one poll makes the pipeline and partial-word waits
+    run out: the kernel records NVFP4_ERR_DEVICE_TIMEOUT and returns; after
+    the workspace is zero-filled again (as the header asks after a timeout)
+    the next call on it is right."""
+    ws = small_weights(n, k, 12)
+    wdev = ws.device_prepared(lib)
+    _, _, gs_x, xq, xs = quantized_activation(0, m, k)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    scratch = workspace(lib, m, n, k, TC_SWAPAB)
+    assert scratch[0] is not None
+    assert lib.nvfp4_get_device_status() == 0
+    lib.nvfp4_set_wait_limit(1)
+    try:
+        run_w4a4(lib, xq, xs, wdev, alpha, m, n, k, TC_SWAPAB, scratch)
+    finally:
+        lib.nvfp4_set_wait_limit(0)
+    assert lib.nvfp4_get_device_status() == lib.ERR_DEVICE_TIMEOUT
+    scratch[0].zero_()
+    got = run_w4a4(lib, xq, xs, wdev, alpha, m, n, k, TC_SWAPAB, scratch)
+    assert lib.nvfp4_get_device_status() == 0
+    assert_gemm_close(got, oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha))
+
+
 def test_swapab_without_workspace_still_correct(lib):
     """Too little scratch: the kernel runs one unit per weight tile instead."""
     m, n, k = 4, 512, 4096
