@@ -130,6 +130,22 @@ struct TArgs {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
+// A split tile's sum handed out in chunks (128-token tiles): chunk c covers
+// token rows 8 (c >> 2) .. +7 and weight rows 32 (c & 3) .. +31 of the
+// tile.  The epilogue posts the task; its own warps and every converter warp
+// that has finished dequantizing take chunks through `word` = generation
+// (bits 16-31) | chunk count (8-15) | chunks handed out (0-7), so one atomic
+// returns a chunk index together with the post it belongs to.
+struct SumTask {
+  int64_t c_first, c_last;
+  int32_t tile, t0, mt, f_first;
+  uint32_t word;
+  int32_t done;          // chunks finished
+  int32_t stop;          // the epilogue has no more tiles
+  int32_t idle;          // converter warps done dequantizing (taking chunks)
+  int32_t use;           // this sum is posted in chunks (else the epilogue sums alone)
+};
+
 // Eight E2M1 codes (one word, element i in nibble i) times an f16x2 scale ->
 // four f16x2 (elements 2i, 2i+1 in word i, the lower index in the low half).
 __device__ __forceinline__ void dequant8_f16(uint32_t codes, uint32_t scale_h2, uint32_t *out) {
@@ -180,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(drain + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   volatile int *last_flag = abort_flag + 1;
+  SumTask *task = reinterpret_cast<SumTask *>((reinterpret_cast<uintptr_t>(last_flag + 1) + 15) & ~uintptr_t(15));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // In a pair, rank 0 (the leader) issues the pair's MMAs and owns the
@@ -189,6 +206,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
   auto in_cta = [&](const void *v, uint32_t r) { return ptx::map_to_cta(ptx::smem_u32(v), r); };
   const int cluster = blockIdx.x / CL;
+  // One chunk of the posted split-tile sum (128-token tiles): thread `lane`
+  // of the calling warp adds weight row 32 (ch & 3) + lane of token rows
+  // 8 (ch >> 2) .. +7 over the tile's contributors in K order and stores
+  // them as bf16(alpha * v * 2^-e).
+  auto sum_chunk = [&](int ch) {
+    constexpr int TGC = 8, MAXC = 2;
+    const int row = 32 * (ch & 3) + (int)(threadIdx.x & 31), g0 = TGC * (ch >> 2);
+    const int64_t c_first = task->c_first, c_last = task->c_last;
+    const int tl = task->tile, t0 = task->t0, mt = task->mt, f_first = task->f_first;
+    const int n = ((tl / p.ttiles) * CL + (int)rank) * 128 + row;
+    auto slot = [&](int64_t cc) {
+      return p.partials + (((size_t)cc * p.maxfrag + (cc == c_first ? f_first : 0)) * CL + rank) * NT * 128;
+    };
+    float acc[TGC];
+#pragma unroll
+    for (int x = 0; x < TGC; ++x) acc[x] = 0.0f;
+    for (int64_t c0 = c_first; c0 <= c_last; c0 += MAXC) {
+      float pv[MAXC][TGC];
+#pragma unroll
+      for (int u = 0; u < MAXC; ++u) {
+        const bool have = c0 + u <= c_last;
+        const float *pc = slot(have ? c0 + u : c0) + (size_t)g0 * 128 + row;
+#pragma unroll
+        for (int x = 0; x < TGC; ++x) pv[u][x] = (have && g0 + x < mt) ? __ldcg(pc + x * 128) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < MAXC; ++u)
+        if (c0 + u <= c_last) {
+#pragma unroll
+          for (int x = 0; x < TGC; ++x) acc[x] += pv[u][x];
+        }
+    }
+    if (n < p.n) {
+      const float alpha = __ldg(p.alpha);
+#pragma unroll
+      for (int x = 0; x < TGC; ++x)
+        if (g0 + x < mt) {
+          const __nv_bfloat16 o = __float2bfloat16_rn(alpha * acc[x] * __ldg(p.rs + t0 + g0 + x));
+          p.d[(size_t)(t0 + g0 + x) * p.n + n] = *reinterpret_cast<const uint16_t *>(&o);
+        }
+    }
+  };
+  // Take chunks of the current post until none is left; returns the
+  // generation of the post the last grab belonged to.
+  auto take_chunks = [&]() {
+    for (;;) {
+      uint32_t old = 0;
+      if ((threadIdx.x & 31) == 0) old = atomicAdd(&task->word, 1u);
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if ((old & 0xFFu) >= ((old >> 8) & 0xFFu)) return old >> 16;
+      __threadfence_block();                 // the fields of that post
+      sum_chunk((int)(old & 0xFFu));
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) atomicAdd(&task->done, 1);
+    }
+  };
   pdl_trigger();
   if (threadIdx.x == 0) {
     for (int r = 0; r < WST; ++r) {
@@ -211,6 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&drain[b], 1);
     }
     *abort_flag = 0;
+    task->word = 0;
+    task->done = 0;
+    task->stop = 0;
+    task->idle = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tm_x);
     ptx::prefetch_tensormap(&tm_w);
@@ -478,6 +555,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if constexpr (NT == 128) {
+      // Done dequantizing: take chunks of the split-tile sums the epilogue
+      // posts from now on, until it has no more tiles (bounded wait).
+      if (lane == 0) atomicAdd(&task->idle, 1);
+      uint32_t seen = 0, polls = 0;
+      uint64_t w0 = 0;
+      while (ok) {
+        if ((*reinterpret_cast<volatile uint32_t *>(&task->word) >> 16) != seen) {
+          seen = take_chunks();
+          polls = 0;
+          w0 = 0;
+          continue;
+        }
+        if (*reinterpret_cast<volatile int *>(&task->stop) || *abort_flag) break;
+        ++polls;
+        bool late = limit && polls >= limit;
+        if (!limit && (polls & 63u) == 0) {
+          const uint64_t now = ptx::globaltimer();
+          if (w0 == 0) w0 = now;
+          else late = now - w0 > kTimeoutNs;
+        }
+        if (__any_sync(0xffffffffu, late)) {   // the warp leaves together
+          give_up();
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     pdl_wait();
@@ -519,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     MixedIter mi(mixed, cluster);
     int tile, kb0, kb1;
+    uint32_t gen = 0;                        // posts of split-tile sums (thread et == 0)
     for (; mi.next(tile, kb0, kb1); ++it) {
       const int ab = it & 1;
       const bool got = ptx::mbar_wait_bounded(&tfull[ab], (uint32_t)((it >> 1) & 1), limit, kTimeoutNs, abort_flag);
@@ -568,6 +674,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       epi_bar();
       if (!*last_flag) continue;
       if (et == 0) p.counters[tile * CL + (int)rank] = 0;
+      bool chunked = false;
+      if constexpr (NT == 128) {
+        // ~512 loads a thread if this group summed alone (16 round trips):
+        // post it in chunks, which converter warps done dequantizing take too,
+        // once at least half of them are, or when at most one tile is left
+        // to dequantize (they join as soon as it is done); otherwise sum
+        // alone (an 8-token chunk costs as many round trips as the 16 token
+        // rows of a pass below, and later tiles' accumulators wait)
+        const int later = (mi.x < mi.end ? 1 : 0) + (mi.t_end - mi.t);   // fragments after this one
+        if (et == 0) task->use = *reinterpret_cast<volatile int *>(&task->idle) >= 8 || later <= 1;
+        epi_bar();
+        chunked = task->use != 0;
+      }
+      if (chunked) {
+        if (et == 0) {
+          task->c_first = c_first;
+          task->c_last = c_last;
+          task->tile = tile;
+          task->t0 = t0;
+          task->mt = mt;
+          task->f_first = f_first;
+          atomicExch(&task->done, 0);
+          ++gen;
+          __threadfence_block();
+          atomicExch(&task->word, (gen << 16) | ((uint32_t)((mt + 7) >> 3) * 4u << 8));
+        }
+        epi_bar();
+        take_chunks();
+        bool ok = true;
+        if (et == 0) {
+          const int nch = (int)((mt + 7) >> 3) * 4;
+          uint64_t w0 = 0;
+          for (uint32_t polls = 1; *reinterpret_cast<volatile int *>(&task->done) < nch; ++polls) {
+            if (*abort_flag || (limit && polls >= limit)) { ok = false; break; }
+            if (!limit && (polls & 63u) == 0) {
+              const uint64_t now = ptx::globaltimer();
+              if (w0 == 0) w0 = now;
+              else if (now - w0 > kTimeoutNs) { ok = false; break; }
+            }
+            __nanosleep(64);
+          }
+          if (!ok) give_up();
+          __threadfence_block();              // the chunks' stores before the next post
+        }
+        if (ptx::bar_any(2, 128, !ok || *abort_flag)) break;
+      } else {
 #pragma unroll 1
       for (int g0 = 0; g0 < mt; g0 += TG) {
         float acc[TG];
@@ -595,6 +747,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (g0 + x < mt) p.d[(size_t)(t0 + g0 + x) * p.n + n] = out_bits(acc[x], t0 + g0 + x);
         }
       }
+      }
+    }
+    if (NT == 128 && et == 0) {
+      __threadfence_block();
+      *reinterpret_cast<volatile int *>(&task->stop) = 1;   // the converter warps may leave
     }
   }
 

@@ -143,3 +143,29 @@ def test_bounded_wait_gives_up_cleanly(lib, m, n, k):
     assert lib.nvfp4_get_device_status() == 0          # read clears it
     got = run_tmem(lib, xbits, wd[0], wd[1], alpha, m, n, k)
     assert_gemm_close(got, oracle.gemm_w4a16(x, ws.packed, ws.sf, alpha))
+
+
+# 128-token tiles on CTA pairs, every weight tile shared: 2 pair tiles of 32
+# k-blocks (32 contributors each), token tiles of one pair tile split over
+# 68 k-blocks (~38 contributors), two token tiles with a ragged second one
+@pytest.mark.parametrize("m,n,k", [(128, 512, 8192), (130, 256, 17408), (256, 768, 2048), (200, 512, 3072)])
+def test_split_128_token_tiles(lib, m, n, k):
+    """Tiles of 128 token rows shared by many CTA pairs: the last to arrive
+    sums every contributor's 128-token partial in K order.  The result
+    matches the oracle, a second call on the same workspace is bit for bit
+    the first, and every counter is back at zero afterwards."""
+    ws = small_weights(n, k, 16)
+    xbits, x = synth.activations(4, m, k)
+    alpha = np.float32(1.0) / ws.gs
+    w, sfo = ws.device_prepared(lib)
+    nbytes = lib.bf16_fp4_gemm_workspace_bytes(m, n, k, TC)
+    scratch = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        d = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lib.bf16_fp4_gemm_ex(bf16_dev(xbits), w, sfo, scalar(alpha), d, m, n, k, scratch, nbytes, algo=TC)
+        torch.cuda.synchronize()
+        outs.append(bf16_host(d))
+        assert int(torch.count_nonzero(scratch[:64 * 1024])) == 0, "counters not reset"
+    assert np.array_equal(outs[0], outs[1])
+    assert_gemm_close(outs[0], oracle.gemm_w4a16(x, ws.packed, ws.sf, alpha))
