@@ -32,30 +32,57 @@ __device__ __forceinline__ void load16_bf16(const uint16_t *p, float (&x)[16]) {
   }
 }
 
-// x [m, k] bf16 -> codes [m, k/2] + scales.  Grid (ceil(k/64), ceil(m/128)).
-__global__ void __launch_bounds__(kTileThreads) quantize_kernel(
+// x [m, k] bf16 -> codes [m, k/2] + scales.  Grid (ceil(k/128), ceil(m/128)):
+// a CTA takes two consecutive scale tiles along K, thread t the block at
+// offset t of each; both blocks' loads are issued before either is
+// quantized, so an SM (three CTAs of 512 threads) keeps twice the bytes in
+// flight that one block a thread would (HBM-bound: 96 % of the measured copy
+// bandwidth at [8192, 7168], against 83 % with one).
+__global__ void __launch_bounds__(kTileThreads, 3) quantize_kernel(
     const uint16_t *__restrict__ x, int64_t m, int64_t k, const float *__restrict__ gs_ptr,
     uint8_t *__restrict__ out_fp4, uint8_t *__restrict__ out_sf, bool swizzled) {
   pdl_trigger();
   pdl_wait();
-  int64_t row, col;
-  tile_coords(threadIdx.x, row, col);
+  constexpr int TPC = 2;
+  const int t = threadIdx.x;
+  const int64_t row = (int64_t)blockIdx.y * 128 + ((t >> 2) & 3) * 32 + (t >> 4);
   const int64_t cols = k >> 4;
   const int64_t cp4 = (cols + 3) >> 2;
-  const bool valid = row < m && col < cols;
-  uint32_t sf = 0;
-  if (valid) {
-    const float gs = __ldg(gs_ptr);
-    float v[16];
-    load16_bf16(x + row * k + col * 16, v);
-    uint32_t lo, hi;
-    sf = quantize_block16(v, gs, lo, hi);
-    *reinterpret_cast<uint2 *>(out_fp4 + row * (k >> 1) + col * 8) = make_uint2(lo, hi);
+  uint4 raw[TPC][2];
+#pragma unroll
+  for (int i = 0; i < TPC; ++i) {
+    const int64_t col = ((int64_t)blockIdx.x * TPC + i) * 4 + (t & 3);
+    if (row < m && col < cols) {
+      const uint4 *q = reinterpret_cast<const uint4 *>(x + row * k + col * 16);
+      raw[i][0] = __ldcs(q);
+      raw[i][1] = __ldcs(q + 1);
+    }
   }
-  if (swizzled) {
-    out_sf[(((int64_t)blockIdx.y * cp4 + blockIdx.x) << 9) + threadIdx.x] = (uint8_t)sf;
-  } else if (valid) {
-    out_sf[row * cols + col] = (uint8_t)sf;
+  const float gs = __ldg(gs_ptr);
+#pragma unroll
+  for (int i = 0; i < TPC; ++i) {
+    const int64_t tile = (int64_t)blockIdx.x * TPC + i;
+    const int64_t col = tile * 4 + (t & 3);
+    const bool valid = row < m && col < cols;
+    uint32_t sf = 0;
+    if (valid) {
+      const uint32_t w[8] = {raw[i][0].x, raw[i][0].y, raw[i][0].z, raw[i][0].w,
+                             raw[i][1].x, raw[i][1].y, raw[i][1].z, raw[i][1].w};
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[2 * j] = bf16_lo(w[j]);
+        v[2 * j + 1] = bf16_hi(w[j]);
+      }
+      uint32_t lo, hi;
+      sf = quantize_block16(v, gs, lo, hi);
+      *reinterpret_cast<uint2 *>(out_fp4 + row * (k >> 1) + col * 8) = make_uint2(lo, hi);
+    }
+    if (swizzled) {
+      if (tile < cp4) out_sf[(((int64_t)blockIdx.y * cp4 + tile) << 9) + t] = (uint8_t)sf;
+    } else if (valid) {
+      out_sf[row * cols + col] = (uint8_t)sf;
+    }
   }
 }
 
@@ -251,7 +278,7 @@ inline unsigned grid_for(int64_t work, int threads) {
 
 cudaError_t launch_quantize(const uint16_t *x, int64_t m, int64_t k, const float *gs,
                             uint8_t *out_fp4, uint8_t *out_sf, bool swizzled, cudaStream_t st) {
-  const dim3 grid((unsigned)((k / 16 + 3) / 4), (unsigned)((m + 127) / 128));
+  const dim3 grid((unsigned)(((k / 16 + 3) / 4 + 1) / 2), (unsigned)((m + 127) / 128));
   return launch_pdl(quantize_kernel, grid, dim3(kTileThreads), 0, st, x, m, k, gs, out_fp4, out_sf, swizzled);
 }
 
