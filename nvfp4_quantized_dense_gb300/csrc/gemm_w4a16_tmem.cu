@@ -792,10 +792,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Token rows of x (times the AWQ pre-scale s when given, rounded to bf16 as
 // the separate multiply does) -> f16 x16 = x * 2^e with e per row bringing
 // the row's largest finite magnitude into [2^15, 2^16), and rs[row] = 2^-e.
-// One CTA per row; a row of up to kPrepThreads * kPrepVecs * 8 elements is
-// read once into registers (all loads in flight together), longer rows read
-// their remainder twice.
-constexpr int kPrepThreads = 1024, kPrepVecs = 4;
+// One CTA per row; a row of up to kPrepThreads * kPrepVecs * 8 elements
+// (18432) is read once into registers (all loads in flight together), longer
+// rows read their remainder twice.  256 threads a CTA, so that several rows
+// are in flight on an SM (a 1024-thread CTA at this register count took the
+// whole register file: one row at a time, ~1/4 of HBM at 1024 rows).
+constexpr int kPrepThreads = 256, kPrepVecs = 9;
 
 __global__ void __launch_bounds__(kPrepThreads) w4a16_act_f16_kernel(const uint16_t *__restrict__ x,
                                                                      const uint16_t *__restrict__ s, int64_t k,
