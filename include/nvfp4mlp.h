@@ -212,6 +212,33 @@ nvfp4_status nvfp4_gemm_swiglu_quant_ex(const uint8_t *a_fp4, const uint8_t *a_s
                                         int64_t k, void *workspace, size_t ws_bytes,
                                         nvfp4_algo algo, nvfp4_stream_t stream);
 
+/* The activation quantize folded into the fused gate_up GEMM (the decode
+ * chain's nvfp4_quantize -> nvfp4_gemm_swiglu_quant; [P2] deepseek_v2.py
+ * excerpt: fp4_quantize and the fused kernel, both launched with enable_pdl).
+ *   x bf16 [m, k], x_global_scale fp32 [1]: quantized exactly as
+ *     nvfp4_quantize(x, m, k, x_global_scale, x_fp4, x_sf,
+ *     NVFP4_SF_SWIZZLED_128x4), and x_fp4 uint8 [m, k/2] / x_sf are written
+ *     with that result (caller-owned, as nvfp4_quantize's outputs);
+ *   then out_fp4 / out_sf = nvfp4_gemm_swiglu_quant(x_fp4, x_sf, w_int_fp4,
+ *     w_int_sf, alpha, out_global_scale, ...), bit for bit.
+ * For m <= 64 with nvfp4_quantize_gemm_swiglu_quant_workspace_bytes() of
+ * workspace (16-byte aligned, zero-filled once before its first use; the
+ * call leaves its counters at zero) this is one launch: the CTAs first
+ * through the grid-dependency wait quantize x in chunks that they count in
+ * the workspace, and every CTA issues its activation loads once all chunks
+ * are counted, so the separate quantize launch and the grid completion
+ * between the two leave the decode chain.  Otherwise (larger m, or less
+ * workspace) it makes the two launches.  After NVFP4_ERR_DEVICE_TIMEOUT the
+ * workspace must be zero-filled again.  Requires n % 128 == 0, k % 64 == 0,
+ * 16-byte aligned x, x_fp4, x_sf, weights and outputs. */
+size_t nvfp4_quantize_gemm_swiglu_quant_workspace_bytes(int64_t m, int64_t n, int64_t k);
+nvfp4_status nvfp4_quantize_gemm_swiglu_quant(const uint16_t *x, const float *x_global_scale,
+                                              uint8_t *x_fp4, uint8_t *x_sf, const uint8_t *w_int_fp4,
+                                              const uint8_t *w_int_sf, const float *alpha,
+                                              const float *out_global_scale, uint8_t *out_fp4,
+                                              uint8_t *out_sf, int64_t m, int64_t n, int64_t k,
+                                              void *workspace, size_t ws_bytes, nvfp4_stream_t stream);
+
 /* Per-token dynamic activation scales ([P3] MoE excerpt: nvfp4_quantize(...,
  * per_token_activation=True) returns a per-token scale).  Each row r gets its
  * own global scale gs_r = fp32(448*6 / amax(row r)) (1 for an all-zero row)

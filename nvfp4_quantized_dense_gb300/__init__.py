@@ -40,6 +40,7 @@ _SIGS = {
     "nvfp4_gemm_ex": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
     "nvfp4_gemm_swiglu_quant": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
     "nvfp4_gemm_swiglu_quant_ex": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
+    "nvfp4_quantize_gemm_swiglu_quant": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
     "bf16_fp4_gemm": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
     "bf16_fp4_gemm_ex": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
     "bf16_fp4_gemm_prescaled": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _I, _P],
@@ -55,7 +56,8 @@ _SIGS = {
 EXPORTS = sorted(list(_SIGS) + ["nvfp4_status_string", "nvfp4_version", "nvfp4_sf_bytes",
                                 "nvfp4_workspace_bytes", "bf16_fp4_gemm_prescaled_workspace_bytes",
                                 "bf16_fp4_gemm_workspace_bytes",
-                                "nvfp4_mlp_decode_workspace_bytes"])
+                                "nvfp4_mlp_decode_workspace_bytes",
+                                "nvfp4_quantize_gemm_swiglu_quant_workspace_bytes"])
 
 
 def load(path=LIB_PATH):
@@ -80,6 +82,8 @@ def load(path=LIB_PATH):
     lib.bf16_fp4_gemm_workspace_bytes.restype = _SZ
     lib.nvfp4_mlp_decode_workspace_bytes.argtypes = [_I64, _I64, _I64]
     lib.nvfp4_mlp_decode_workspace_bytes.restype = _SZ
+    lib.nvfp4_quantize_gemm_swiglu_quant_workspace_bytes.argtypes = [_I64, _I64, _I64]
+    lib.nvfp4_quantize_gemm_swiglu_quant_workspace_bytes.restype = _SZ
     _lib = lib
     return lib
 
@@ -209,6 +213,18 @@ def nvfp4_gemm_swiglu_quant(a_fp4, a_sf, w_int_fp4, w_int_sf, alpha, out_global_
     _call("nvfp4_gemm_swiglu_quant", _ptr(a_fp4), _ptr(a_sf), _ptr(w_int_fp4), _ptr(w_int_sf),
           _ptr(alpha), _ptr(out_global_scale), _ptr(out_fp4), _ptr(out_sf), m, n, k,
           _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def nvfp4_quantize_gemm_swiglu_quant_workspace_bytes(m, n, k):
+    return load().nvfp4_quantize_gemm_swiglu_quant_workspace_bytes(m, n, k)
+
+
+def nvfp4_quantize_gemm_swiglu_quant(x, x_global_scale, x_fp4, x_sf, w_int_fp4, w_int_sf, alpha,
+                                     out_global_scale, out_fp4, out_sf, m, n, k, workspace=None, ws_bytes=0,
+                                     stream=None):
+    _call("nvfp4_quantize_gemm_swiglu_quant", _ptr(x), _ptr(x_global_scale), _ptr(x_fp4), _ptr(x_sf),
+          _ptr(w_int_fp4), _ptr(w_int_sf), _ptr(alpha), _ptr(out_global_scale), _ptr(out_fp4), _ptr(out_sf),
+          m, n, k, _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def nvfp4_gemm_swiglu_quant_ex(a_fp4, a_sf, w_int_fp4, w_int_sf, alpha, out_global_scale, out_fp4,

@@ -271,6 +271,41 @@ nvfp4_status nvfp4_gemm_swiglu_quant(const uint8_t *a_fp4, const uint8_t *a_sf,
                                     NVFP4_ALGO_AUTO, stream);
 }
 
+size_t nvfp4_quantize_gemm_swiglu_quant_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+  if (m <= 0 || n <= 0 || k <= 0) return 0;
+  if (m <= 64 && swapab_supported(TC_W4A4_SWIGLU, m, n, k)) return swapab_fold_workspace_bytes(m, n, k);
+  return nvfp4_workspace_bytes(m, n, k, NVFP4_ALGO_AUTO);
+}
+
+nvfp4_status nvfp4_quantize_gemm_swiglu_quant(const uint16_t *x, const float *x_global_scale, uint8_t *x_fp4,
+                                              uint8_t *x_sf, const uint8_t *w_int_fp4, const uint8_t *w_int_sf,
+                                              const float *alpha, const float *out_global_scale,
+                                              uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
+                                              int64_t k, void *workspace, size_t ws_bytes,
+                                              nvfp4_stream_t stream) {
+  if (!x || !x_global_scale || !x_fp4 || !x_sf || !w_int_fp4 || !w_int_sf || !alpha || !out_global_scale ||
+      !out_fp4 || !out_sf)
+    return NVFP4_ERR_INVALID_ARG;
+  if (nvfp4_status s = check_gemm_shape(m, n, k)) return s;
+  if (n % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(x_fp4) || !aligned16(x_sf) || !aligned16(w_int_fp4) || !aligned16(w_int_sf) ||
+      !aligned16(out_fp4) || !aligned16(out_sf))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (nvfp4_status s = check_arch()) return s;
+  if (m == 0) return NVFP4_OK;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (m <= 64 && swapab_supported(TC_W4A4_SWIGLU, m, n, k) && workspace && aligned16(workspace) &&
+      ws_bytes >= swapab_fold_workspace_bytes(m, n, k))
+    return from_cuda(launch_swapab_quantize_fold(x, x_global_scale, x_fp4, x_sf, w_int_fp4, w_int_sf, alpha,
+                                                 out_global_scale, out_fp4, out_sf, m, n, k, workspace, ws_bytes,
+                                                 g_wait_limit.load(), st));
+  // otherwise the two launches it stands for
+  if (nvfp4_status s = nvfp4_quantize(x, m, k, x_global_scale, x_fp4, x_sf, NVFP4_SF_SWIZZLED_128x4, stream))
+    return s;
+  return nvfp4_gemm_swiglu_quant_ex(x_fp4, x_sf, w_int_fp4, w_int_sf, alpha, out_global_scale, out_fp4, out_sf,
+                                    m, n, k, workspace, ws_bytes, NVFP4_ALGO_AUTO, stream);
+}
+
 }  // extern "C"
 
 namespace {

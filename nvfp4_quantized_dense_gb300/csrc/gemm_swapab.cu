@@ -23,9 +23,21 @@
 // its first use; the kernel leaves its counters at zero after every complete
 // call.
 //
+// Activation quantize folded in (decode gate_up): given bf16 x, the kernel
+// writes x's NVFP4 codes and swizzled scales itself, exactly as
+// nvfp4_quantize, into the buffers its activation loads read.  The CTAs
+// first through the grid-dependency wait take chunks of x's 16-element
+// blocks from a counter in the workspace (one block per epilogue thread),
+// then chunks of the zero padding rows of the scale block; a producer issues
+// its activation halves once every chunk of x's blocks has been counted.
+// This takes the separate quantize launch, and the grid completion between
+// it and the GEMM, off the decode chain.  The last CTA done with the
+// counters resets them.
+//
 // Roles per CTA (192 threads, one CTA per SM): warp 0 TMA producer,
 // warp 1 TMEM owner + MMA issuer (double-buffered accumulators), warps 2..5
-// epilogue (TMEM lane = weight row).  Bounded waits as in gemm_tc.cu.
+// phase A (with the fold) and the epilogue (TMEM lane = weight row).
+// Bounded waits as in gemm_tc.cu.
 #include <algorithm>
 #include <atomic>
 
@@ -44,6 +56,8 @@ constexpr int kThreads = 192;
 constexpr int ACC_BUFS = 2;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kDrainPolls = 1u << 22;
+constexpr int XCHUNK = 128;          // phase A: blocks of x per chunk (one per epilogue thread)
+constexpr int PCHUNK = 1024;         // phase A: padding words of the scale block per chunk
 
 template <int NT>
 struct Cfg {
@@ -80,6 +94,13 @@ struct SwapArgs {
   uint32_t wait_limit;
   int *status;
   const float *rs;      // optional per-token activation dequant factor [M]
+  // activation quantize folded in (xsrc != nullptr)
+  const uint16_t *xsrc;  // bf16 x [M, K]
+  const float *gs_x;     // x global scale
+  uint8_t *xq;           // x codes [M, K/2] (what tm_x reads)
+  uint8_t *xs;           // x scales, swizzled over M rows (what sfx reads)
+  uint32_t *xsync;       // [0] chunk counter, [1] x chunks done, [2] CTAs done with both
+  int32_t xchunks, pchunks;   // chunks of x's blocks (counted), of scale padding (not)
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -115,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(parts + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
   volatile int *last_flag = abort_flag + 1;
+  volatile int *x_phase_done = abort_flag + 2;
+  volatile uint32_t *x_grab = reinterpret_cast<volatile uint32_t *>(abort_flag + 3);   // two slots
   auto st_w = [&](int s) { return base + s * C::STAGE_BYTES; };
   auto st_x = [&](int s) { return st_w(s) + W_BYTES; };
   auto st_sfw = [&](int s) { return st_x(s) + C::X_BYTES; };
@@ -135,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&parts[0], 128 * (p.cl > 1 ? p.cl - 1 : 1));   // every epilogue thread of the others
     ptx::mbar_init(&parts[1], 128);                               // every epilogue thread of the first CTA
     *abort_flag = 0;
+    *x_phase_done = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tensormap(&tm_w);
     ptx::prefetch_tensormap(&tm_x);
@@ -188,6 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto flush = [&]() {
         pdl_wait();
+        // with the fold: x's blocks are quantized by the first CTAs through
+        // the wait (after a give-up the halves still go out, reading
+        // whatever the buffers hold, so that every stage completes)
+        if (p.xsrc && !ptx::counter_wait_bounded(&p.xsync[1], (uint32_t)p.xchunks, limit, kTimeoutNs, abort_flag)) {
+          *abort_flag = 1;
+          atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+        }
         for (int i = 0; i < npend; ++i) issue_x(pend_s[i], pend_kb[i]);
         flushed = true;
       };
@@ -217,6 +248,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!flushed) flush();
+      if (p.xsrc) {
+        // This CTA reads and takes no phase-A counter any more once its own
+        // epilogue warps are past phase A; the last CTA to get here resets
+        // the counters for the next call.
+        uint64_t t0 = 0;
+        bool ok = true;
+        for (uint32_t polls = 1; !*x_phase_done && !*abort_flag; ++polls) {
+          if (limit ? polls >= limit : false) ok = false;
+          if (!limit && (polls & 63u) == 0) {
+            const uint64_t now = ptx::globaltimer();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kTimeoutNs) ok = false;
+          }
+          if (!ok) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (ok && !*abort_flag &&
+            atom_add_acq_rel_gpu(reinterpret_cast<int *>(&p.xsync[2]), 1) == (uint32_t)p.grid - 1) {
+          p.xsync[0] = 0;
+          p.xsync[1] = 0;
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          p.xsync[2] = 0;
+        }
+      }
     }
   } else if (warp == 1) {
     pdl_wait();
@@ -270,6 +329,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;                 // weight row within the tile
     const int et = threadIdx.x - 64;             // 0..127 across the epilogue warps
+    if (p.xsrc) {
+      // phase A: chunks of x's blocks (counted), then chunks of the padding
+      // rows m..127 of the scale block (zero), until none is left
+      const int cols = p.k >> 4, xcp4 = cols >> 2;
+      const float gsx = __ldg(p.gs_x);
+      const int64_t nblk = (int64_t)p.m * cols, npad = (int64_t)(128 - p.m) * xcp4;
+      for (int par = 0;; par ^= 1) {
+        if (et == 0) x_grab[par] = atomicAdd(&p.xsync[0], 1u);
+        epi_bar();
+        const uint32_t ci = x_grab[par];
+        if (ci >= (uint32_t)(p.xchunks + p.pchunks)) break;
+        if (ci < (uint32_t)p.xchunks) {
+          const int64_t b = (int64_t)ci * XCHUNK + et;
+          if (b < nblk) {
+            const int row = (int)(b / cols), j = (int)(b - (int64_t)row * cols);
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.xsrc + (size_t)row * p.k + 16 * j);
+            const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            float xv[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              xv[2 * i] = bf16_lo(w[i]);
+              xv[2 * i + 1] = bf16_hi(w[i]);
+            }
+            uint32_t lo, hi;
+            const uint32_t sf = quantize_block16(xv, gsx, lo, hi);
+            *reinterpret_cast<uint2 *>(p.xq + (size_t)row * (p.k >> 1) + 8 * j) = make_uint2(lo, hi);
+            p.xs[sf_swizzled_offset(row, j, xcp4)] = (uint8_t)sf;
+          }
+          ptx::fence_proxy_async_global();     // these stores -> the activation TMA reads
+          epi_bar();
+          if (et == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.xsync[1]) : "memory");
+        } else {
+          for (int i = et; i < PCHUNK; i += 128) {
+            const int64_t w = (int64_t)(ci - p.xchunks) * PCHUNK + i;
+            if (w < npad) {
+              const int row = p.m + (int)(w / xcp4), j4 = (int)(w % xcp4);
+              *reinterpret_cast<uint32_t *>(p.xs + sf_swizzled_offset(row, 4 * j4, xcp4)) = 0u;
+            }
+          }
+        }
+      }
+      if (et == 0) *x_phase_done = 1;
+    }
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
     const float alpha = __ldg(p.alpha);
     const int mt = min(p.m, NT);
@@ -510,11 +613,18 @@ Plan make_plan(int64_t m, int64_t n, int64_t k) {
   return pl;
 }
 
+// The activation quantize folded into the launch (bf16 x in, the quantized
+// activation buffers written by the kernel itself).
+struct Fold {
+  const uint16_t *x;
+  const float *gs_x;
+};
+
 template <int MODE, int NT>
 cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, const uint8_t *w,
                       const uint8_t *w_sf, const float *alpha, const float *out_gs, uint16_t *d,
                       uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k, void *ws,
-                      uint32_t wait_limit, cudaStream_t st, const float *rs) {
+                      uint32_t wait_limit, cudaStream_t st, const float *rs, const Fold *fold) {
   using C = Cfg<NT>;
   // the shared-memory limit is a setting of each device's context
   static PerDeviceOnce smem_attr;
@@ -553,6 +663,17 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   a.wait_limit = wait_limit;
   a.status = device_status_ptr();
   a.rs = rs;
+  if (fold) {
+    // the three phase-A words sit in the last 256 bytes of the counter area,
+    // past every tile counter
+    a.xsrc = fold->x;
+    a.gs_x = fold->gs_x;
+    a.xq = const_cast<uint8_t *>(x);
+    a.xs = const_cast<uint8_t *>(x_sf);
+    a.xsync = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + kCounterArea - 256);
+    a.xchunks = (int32_t)((m * (k / 16) + XCHUNK - 1) / XCHUNK);
+    a.pchunks = (int32_t)(((128 - m) * (k / 64) + PCHUNK - 1) / PCHUNK);
+  }
   if (!a.status) return cudaErrorInvalidValue;
   if (pl.cl <= 1)
     return launch_pdl(swapab_kernel<MODE, NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_w, tm_x, a);
@@ -577,17 +698,17 @@ template <int MODE>
 cudaError_t launch_mode(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, const uint8_t *w,
                         const uint8_t *w_sf, const float *alpha, const float *out_gs, uint16_t *d,
                         uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n, int64_t k, void *ws,
-                        uint32_t wait_limit, cudaStream_t st, const float *rs) {
+                        uint32_t wait_limit, cudaStream_t st, const float *rs, const Fold *fold = nullptr) {
   switch (pl.nt) {
     case 16:
       return launch_nt<MODE, 16>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
-                                 wait_limit, st, rs);
+                                 wait_limit, st, rs, fold);
     case 32:
       return launch_nt<MODE, 32>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
-                                 wait_limit, st, rs);
+                                 wait_limit, st, rs, fold);
     default:
       return launch_nt<MODE, 64>(pl, x, x_sf, w, w_sf, alpha, out_gs, d, out_fp4, out_sf, m, n, k, ws,
-                                 wait_limit, st, rs);
+                                 wait_limit, st, rs, fold);
   }
 }
 
@@ -603,6 +724,25 @@ bool swapab_supported(TcMode mode, int64_t m, int64_t n, int64_t k) {
 size_t swapab_workspace_bytes(TcMode mode, int64_t m, int64_t n, int64_t k) {
   if (!swapab_supported(mode, m, n, k)) return 0;
   return make_plan(m, n, k).ws_bytes;
+}
+
+size_t swapab_fold_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+  if (!swapab_supported(TC_W4A4_SWIGLU, m, n, k)) return 0;
+  return std::max(make_plan(m, n, k).ws_bytes, kCounterArea);
+}
+
+cudaError_t launch_swapab_quantize_fold(const uint16_t *x, const float *gs_x, uint8_t *x_fp4, uint8_t *x_sf,
+                                        const uint8_t *w_int, const uint8_t *w_int_sf, const float *alpha,
+                                        const float *out_gs, uint8_t *out_fp4, uint8_t *out_sf, int64_t m,
+                                        int64_t n, int64_t k, void *workspace, size_t ws_bytes,
+                                        uint32_t wait_limit, cudaStream_t st) {
+  if (!swapab_supported(TC_W4A4_SWIGLU, m, n, k) || workspace == nullptr ||
+      ws_bytes < swapab_fold_workspace_bytes(m, n, k))
+    return cudaErrorNotSupported;
+  const Plan pl = make_plan(m, n, k);
+  const Fold fold{x, gs_x};
+  return launch_mode<TC_W4A4_SWIGLU>(pl, x_fp4, x_sf, w_int, w_int_sf, alpha, out_gs, nullptr, out_fp4, out_sf,
+                                     m, n, k, workspace, wait_limit, st, nullptr, &fold);
 }
 
 cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const uint8_t *b,

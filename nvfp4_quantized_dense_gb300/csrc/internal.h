@@ -119,6 +119,16 @@ cudaError_t launch_swapab(TcMode mode, const void *a, const uint8_t *a_sf, const
                           uint16_t *d, uint8_t *out_fp4, uint8_t *out_sf, int64_t m, int64_t n,
                           int64_t k, void *workspace, size_t ws_bytes, uint32_t wait_limit,
                           cudaStream_t st, const float *a_row_scale = nullptr);
+// The fused gate_up with the activation quantize folded in (bf16 x in; x's
+// NVFP4 codes and swizzled scales written to x_fp4 / x_sf as nvfp4_quantize
+// would).  Needs swapab_fold_workspace_bytes of workspace (zero-filled once;
+// its counters are left at zero); cudaErrorNotSupported otherwise.
+size_t swapab_fold_workspace_bytes(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_swapab_quantize_fold(const uint16_t *x, const float *gs_x, uint8_t *x_fp4, uint8_t *x_sf,
+                                        const uint8_t *w_int, const uint8_t *w_int_sf, const float *alpha,
+                                        const float *out_gs, uint8_t *out_fp4, uint8_t *out_sf, int64_t m,
+                                        int64_t n, int64_t k, void *workspace, size_t ws_bytes,
+                                        uint32_t wait_limit, cudaStream_t st);
 
 // W4A16 on the tensor cores.  Given a workspace of w4a16_workspace_bytes
 // (16-byte aligned, its counter area zero-filled once; counters left at
