@@ -244,12 +244,18 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_w4a4_kernel(GemvArgs p) {
 }
 
 
-template <int MT>
-__global__ void __launch_bounds__(kWarps * 32) gemv_w4a16_kernel(GemvArgs p) {
+// W4A16: each warp takes R consecutive weight rows; its lanes split K into
+// 32-element chunks and put B chunks of every row in flight (B*R 16-byte
+// evict-first loads per lane before the first is used), so that an SM holds
+// ~100 KB of the weight stream in flight.  Each chunk is consumed 8 elements
+// at a time: the activations (bf16, read through L1: every warp reads the
+// same token rows) are converted to fp32 once and used for the R rows.
+template <int MT, int R, int B>
+__global__ void __launch_bounds__(kWarps * 32, 2) gemv_w4a16_kernel(GemvArgs p) {
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t row0 = ((int64_t)blockIdx.x * kWarps + warp) * R;
   const int64_t kb = p.k >> 1;
   const int64_t cp4 = ((p.k >> 4) + 3) >> 2;
   const int mt = (int)min((int64_t)MT, p.m - p.m0);
@@ -257,68 +263,94 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_w4a16_kernel(GemvArgs p) {
   const uint16_t *a = reinterpret_cast<const uint16_t *>(p.a);
   const uint64_t pol = evict_first_policy();
 
-  float acc[MT];
+  float acc[MT][R];
 #pragma unroll
-  for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[t][r] = 0.0f;
 
-  for (int64_t c = lane; c < nchunks; c += 32) {
-    const uint4 wv = ld_stream16(p.b + row * kb + c * 16, pol);
-    const uint32_t wsf = ld_sf_pair(p.b_sf, row, 2 * c, cp4);
-    uint32_t wh[16];
-    decode_chunk(wv, wh);
-    float wf[32];
+  for (int64_t c0 = lane; c0 < nchunks; c0 += 32 * B) {
+    uint4 wv[B][R];
+    uint32_t wsf[B][R];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const __half2 v = *reinterpret_cast<const __half2 *>(&wh[i]);
-      wf[2 * i] = __low2float(v);
-      wf[2 * i + 1] = __high2float(v);
-    }
-    const float s0 = e4m3_decode(wsf & 0xFF), s1 = e4m3_decode((wsf >> 8) & 0xFF);
-    uint32_t pw[16];                 // AWQ pre-scale of these 32 channels (bf16 pairs)
-    if (p.pqs) {
-      const uint4 *sp = reinterpret_cast<const uint4 *>(p.pqs + c * 32);
+    for (int b = 0; b < B; ++b) {
+      const int64_t c = c0 + 32 * b;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 v = __ldg(sp + q);
-        pw[4 * q] = v.x; pw[4 * q + 1] = v.y; pw[4 * q + 2] = v.z; pw[4 * q + 3] = v.w;
+      for (int r = 0; r < R; ++r) {
+        if (c < nchunks) {
+          wv[b][r] = ld_stream16(p.b + (row0 + r) * kb + c * 16, pol);
+          wsf[b][r] = ld_sf_pair(p.b_sf, row0 + r, 2 * c, cp4);
+        } else {
+          wv[b][r] = make_uint4(0u, 0u, 0u, 0u);
+          wsf[b][r] = 0u;
+        }
       }
     }
 #pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      if (t < mt) {
-        const uint4 *ap = reinterpret_cast<const uint4 *>(a + (p.m0 + t) * p.k + c * 32);
-        float b0 = 0.0f, b1 = 0.0f;
+    for (int b = 0; b < B; ++b) {
+      const int64_t c = c0 + 32 * b;
+      if (c >= nchunks) continue;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+      for (int t = 0; t < MT; ++t) {
+        if (t >= mt) continue;
+        const uint4 *ap = reinterpret_cast<const uint4 *>(a + (p.m0 + t) * p.k + c * 32);
+        const uint4 *sp = reinterpret_cast<const uint4 *>(p.pqs ? p.pqs + c * 32 : nullptr);
+        float bs[R][2];
+#pragma unroll
+        for (int r = 0; r < R; ++r) bs[r][0] = bs[r][1] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {            // elements 8q .. 8q+7 (scale block q >> 1)
           const uint4 v = __ldg(ap + q);
           const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+          uint32_t s4[4] = {0u, 0u, 0u, 0u};
+          if (sp) {
+            const uint4 sv = __ldg(sp + q);
+            s4[0] = sv.x; s4[1] = sv.y; s4[2] = sv.z; s4[3] = sv.w;
+          }
+          float x[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int idx = q * 8 + e * 2;
-            float &bs = (idx < 16) ? b0 : b1;
             float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
-            if (p.pqs) {             // bf16(x * s): the fp32 product is exact, one rounding
-              x0 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(x0, bf16_lo(pw[4 * q + e]))));
-              x1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(x1, bf16_hi(pw[4 * q + e]))));
+            if (sp) {                            // bf16(x * s): the fp32 product is exact, one rounding
+              x0 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(x0, bf16_lo(s4[e]))));
+              x1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(x1, bf16_hi(s4[e]))));
             }
-            bs = fmaf(x0, wf[idx], bs);
-            bs = fmaf(x1, wf[idx + 1], bs);
+            x[2 * e] = x0;
+            x[2 * e + 1] = x1;
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const uint32_t codes = q == 0 ? wv[b][r].x : q == 1 ? wv[b][r].y : q == 2 ? wv[b][r].z : wv[b][r].w;
+            uint32_t wh[4];
+            e2m1x8_to_half2x4(codes, wh);
+            float &sum = bs[r][q >> 1];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const __half2 h = *reinterpret_cast<const __half2 *>(&wh[i]);
+              sum = fmaf(x[2 * i], __low2float(h), sum);
+              sum = fmaf(x[2 * i + 1], __high2float(h), sum);
+            }
           }
         }
-        acc[t] = fmaf(b0, s0, acc[t]);
-        acc[t] = fmaf(b1, s1, acc[t]);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          acc[t][r] = fmaf(bs[r][0], e4m3_decode(wsf[b][r] & 0xFF), acc[t][r]);
+          acc[t][r] = fmaf(bs[r][1], e4m3_decode((wsf[b][r] >> 8) & 0xFF), acc[t][r]);
+        }
       }
     }
   }
   const float alpha = __ldg(p.alpha);
 #pragma unroll
-  for (int t = 0; t < MT; ++t) {
-    const float v = warp_sum(acc[t]);
-    if (lane == 0 && t < mt) {
-      const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v);
-      p.d[(p.m0 + t) * p.n + row] = *reinterpret_cast<const uint16_t *>(&o);
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float v = warp_sum(acc[t][r]);
+      if (lane == 0 && t < mt) {
+        const __nv_bfloat16 o = __float2bfloat16_rn(alpha * v);
+        p.d[(p.m0 + t) * p.n + row0 + r] = *reinterpret_cast<const uint16_t *>(&o);
+      }
     }
-  }
 }
 
 template <int MT>
@@ -330,7 +362,13 @@ cudaError_t launch_mt(GemvMode mode, const GemvArgs &a, cudaStream_t st) {
     case GEMV_W4A4_SWIGLU:
       return launch_pdl(gemv_w4a4_kernel<MT, 4, true>, dim3((unsigned)(a.n / 32)), block, 0, st, a);
     case GEMV_W4A16:
-      return launch_pdl(gemv_w4a16_kernel<MT>, dim3((unsigned)(a.n / kWarps)), block, 0, st, a);
+      if constexpr (MT > 4) return cudaErrorInvalidValue;   // W4A16 passes hold at most 4 tokens
+      // two rows a warp (the activation chunk converted once for both) when
+      // that still leaves 16 warps an SM; one row with twice the chunks in
+      // flight otherwise
+      if (a.n >= (int64_t)num_sms() * kWarps * 2 * 2 * 2)
+        return launch_pdl(gemv_w4a16_kernel<MT, 2, 4>, dim3((unsigned)(a.n / (kWarps * 2))), block, 0, st, a);
+      return launch_pdl(gemv_w4a16_kernel<MT, 1, 8>, dim3((unsigned)(a.n / kWarps)), block, 0, st, a);
   }
   return cudaErrorInvalidValue;
 }
@@ -343,10 +381,11 @@ cudaError_t launch_gemv(GemvMode mode, const void *a, const uint8_t *a_sf, const
                         cudaStream_t st, const float *a_row_scale, const uint16_t *pre_scale) {
   GemvArgs args{static_cast<const uint8_t *>(a), a_sf, b, b_sf, alpha, out_gs, d, out_fp4, out_sf,
                 m, n, k, 0, a_row_scale, pre_scale};
-  // passes of 16, 8, 4, 2 or 1 tokens until every token is covered
+  // passes of 16, 8, 4, 2 or 1 tokens (W4A16: at most 4) until every token is covered
   for (int64_t m0 = 0; m0 < m;) {
     const int64_t left = m - m0;
-    const int mt = left >= 16 ? 16 : left > 4 ? 8 : left > 2 ? 4 : (int)left;
+    int mt = left >= 16 ? 16 : left > 4 ? 8 : left > 2 ? 4 : (int)left;
+    if (mode == GEMV_W4A16 && mt > 4) mt = 4;
     args.m0 = m0;
     cudaError_t e;
     switch (mt) {
