@@ -414,13 +414,21 @@ def run_ours(args, world, rank, local):
             else:
                 ws_bytes = max(ws_bytes, nv.nvfp4_workspace_bytes(m, 2 * inter, hid, algo),
                                nv.nvfp4_workspace_bytes(m, hid, inter, algo))
+        # a second input/output set for the end-to-end run (host copies of one
+        # step overlap the other step's kernels); the intermediates are shared
+        it.x_alt, it.out_alt = torch.empty_like(it.x), torch.empty_like(it.out)
+        alt, r0 = {}, 0
+        for m in it.ms:
+            alt[m] = dict(it.bufs[m], x=it.x_alt[:m], out=it.out_alt[r0:r0 + m])
+            r0 += m
+        it.bufsets = (it.bufs, alt)
         items.append(it)
     # one zero-filled scratch (split-K partials + arrival counters) shared by
     # every GEMM of the step: they run in stream order
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
 
-    def gate_up(it, m, c):
-        b = it.bufs[m]
+    def gate_up(it, m, c, s=0):
+        b = it.bufsets[s][m]
         gq, gsf, _ = it.gu[c]
         if it.w4a16:
             nv.bf16_fp4_gemm_ex(b["x"], gq, gsf, it.a_gu, b["gu"], m, 2 * it.inter, it.hid, ws, ws_bytes, algo,
@@ -429,8 +437,8 @@ def run_ours(args, world, rank, local):
             nv.nvfp4_gemm_swiglu_quant_ex(b["xq"], b["xs"], gq, gsf, it.a_gu, it.gs_h, b["hq"], b["hs"], m,
                                           2 * it.inter, it.hid, ws, ws_bytes, algo, stream=SH[0])
 
-    def down(it, m, c):
-        b = it.bufs[m]
+    def down(it, m, c, s=0):
+        b = it.bufsets[s][m]
         dq, dsf, _ = it.dn[c]
         if it.w4a16:
             nv.bf16_fp4_gemm_ex(b["h16"], dq, dsf, it.a_dn, b["out"], m, it.hid, it.inter, ws, ws_bytes, algo,
@@ -439,14 +447,14 @@ def run_ours(args, world, rank, local):
             nv.nvfp4_gemm_ex(b["hq"], b["hs"], dq, dsf, it.a_dn, b["out"], m, it.hid, it.inter, ws, ws_bytes,
                              algo, stream=SH[0])
 
-    def forward(it, m, c):
-        b = it.bufs[m]
+    def forward(it, m, c, s=0):
+        b = it.bufsets[s][m]
         if not it.w4a16:
             nv.nvfp4_quantize(b["x"], m, it.hid, it.gs_x_d, b["xq"], b["xs"], stream=SH[0])
-        gate_up(it, m, c)
+        gate_up(it, m, c, s)
         if it.w4a16:
             nv.silu_mul_bf16(b["gu"], m, it.inter, b["h16"], stream=SH[0])
-        down(it, m, c)
+        down(it, m, c, s)
 
     def forward_unfused(it, m, c):
         """The unfused decode chain: gate_up GEMM to bf16 on the plain weight,
@@ -692,45 +700,50 @@ def run_ours(args, world, rank, local):
         roofline["timing"] = (f"{REPS} launches back to back in one CUDA graph (weight copies rotating), CUDA "
                               "events on the launching stream around 3 replays")
 
-    # ------------------------------- end to end through the C ABI (no graph)
+    # ------------------------------------------- end to end through the C ABI
     x_host = {it.key: it.x.cpu().pin_memory() for it in items}
     out_host = {it.key: torch.empty(it.out.shape, dtype=torch.bfloat16).pin_memory() for it in items}
     h2d = sum(it.x.numel() * 2 for it in items)
     d2h = sum(it.out.numel() * 2 for it in items)
     e2e_steps = max(3, min(args.steps, 20))
-    # The copies run on two streams of their own, one per direction: a
-    # workload's x goes in once the previous step's forwards of that workload
-    # have read it, and its output comes back as soon as its forwards are
-    # done (before the next step's forwards overwrite it).  The workload with
-    # the largest copies runs first, so its copies overlap the kernels of
-    # the others (this step's and the next step's input alike).
+    # Every step copies every workload's x in from pinned host memory and its
+    # output back out, on two streams of their own (one per direction).  The
+    # steps alternate between two device input/output sets, so that the copies
+    # of one step run under the kernels of its neighbours: step i's inputs go
+    # in once step i-2 (the same set) has read them, its kernels (the step's
+    # graph, as in the timed arm) wait for those inputs and for step i-2's
+    # outputs to have left, and its outputs go out as soon as it is done.
+    with torch.cuda.stream(stream):
+        e2e_graphs = [[graph_of(lambda c=c, s=s: [forward(it, m, c, s) for it in items for m in it.ms])
+                       for c in range(NCOPY)] for s in range(2)]
+    torch.cuda.synchronize()
     in_stream, out_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     order = sorted(items, key=lambda it: -(it.x.numel() + it.out.numel()))
-    ev_in = {it.key: torch.cuda.Event() for it in items}
-    ev_done = {it.key: torch.cuda.Event() for it in items}
-    ev_out = {it.key: torch.cuda.Event() for it in items}
-    for it in items:                            # (so that the first waits are satisfied)
-        ev_done[it.key].record(stream)
-        ev_out[it.key].record(out_stream)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for st in range(2):                         # (so that the first waits are satisfied)
+        ev_done[st].record(stream)
+        ev_out[st].record(out_stream)
     torch.cuda.synchronize()
 
     def e2e_step(i):
-        for it in order:
-            in_stream.wait_event(ev_done[it.key])
-            with torch.cuda.stream(in_stream):
-                it.x.copy_(x_host[it.key], non_blocking=True)
-            ev_in[it.key].record(in_stream)
-        for it in order:
-            stream.wait_event(ev_in[it.key])
-            stream.wait_event(ev_out[it.key])
-            with torch.cuda.stream(stream):
-                for m in it.ms:
-                    forward(it, m, i % NCOPY)
-            ev_done[it.key].record(stream)
-            out_stream.wait_event(ev_done[it.key])
-            with torch.cuda.stream(out_stream):
-                out_host[it.key].copy_(it.out, non_blocking=True)
-            ev_out[it.key].record(out_stream)
+        st = i % 2
+        in_stream.wait_event(ev_done[st])
+        with torch.cuda.stream(in_stream):
+            for it in order:
+                (it.x, it.x_alt)[st].copy_(x_host[it.key], non_blocking=True)
+        ev_in[st].record(in_stream)
+        stream.wait_event(ev_in[st])
+        stream.wait_event(ev_out[st])
+        with torch.cuda.stream(stream):
+            e2e_graphs[st][i % NCOPY].replay()
+        ev_done[st].record(stream)
+        out_stream.wait_event(ev_done[st])
+        with torch.cuda.stream(out_stream):
+            for it in order:
+                out_host[it.key].copy_((it.out, it.out_alt)[st], non_blocking=True)
+        ev_out[st].record(out_stream)
 
     for i in range(2):
         e2e_step(i)
@@ -741,6 +754,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - w0) / e2e_steps
     e2e_value = world * tokens_per_step / e2e_s
+    del e2e_graphs
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -770,9 +784,10 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "note": "direct API calls, no graph, pinned host buffers; x of every workload in, every "
-                            "output out, each step, the copies on two streams of their own (one per "
-                            "direction) overlapping the other workloads' kernels"},
+                    "note": "host wall clock per step; pinned host buffers; x of every workload in and every "
+                            "output out, each step, on two copy streams of their own; the steps alternate "
+                            "between two device input/output sets so that one step's copies overlap its "
+                            "neighbours' kernels; the step's API calls replayed from their CUDA graph"},
             "gpu_launches": launches_per_step * args.steps,
         }
         print(json.dumps(line), flush=True)
