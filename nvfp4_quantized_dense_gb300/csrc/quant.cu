@@ -8,11 +8,13 @@ namespace nvfp4 {
 
 namespace {
 
-// One CTA covers one 512-byte tile of the swizzled scale layout: 128 rows x
-// 4 scale columns (64 elements of K).  Thread t owns the block (row, column)
-// whose scale byte sits at offset t of that tile, so the scale stores are one
-// contiguous 512-byte write per CTA, and each group of 4 threads reads 128
-// contiguous bytes of one input row.
+// The tiled kernels map a 512-byte tile of the swizzled scale layout (128
+// rows x 4 scale columns, 64 elements of K) onto one CTA's threads: thread t
+// owns the block (row, column) whose scale byte sits at offset t of the tile,
+// so each tile's scale stores are one contiguous 512-byte write, and each
+// group of 4 threads reads 128 contiguous bytes of one input row.  The
+// quantize kernel takes two consecutive tiles along K a CTA, the fused
+// SiLU*mul quantize one.
 constexpr int kTileThreads = 512;
 
 __device__ __forceinline__ void tile_coords(int t, int64_t &row, int64_t &col) {
@@ -171,30 +173,30 @@ __global__ void __launch_bounds__(kTileThreads) silu_mul_quantize_kernel(
   out_sf[(((int64_t)blockIdx.y * cp4 + blockIdx.x) << 9) + threadIdx.x] = (uint8_t)sf;
 }
 
-// out [m, i] = bf16(silu(gate) * up); 8 outputs per thread, grid-stride.
+// out [m, i] = bf16(silu(gate) * up); 8 outputs per thread on a 2-D grid
+// (x: groups of 8 columns, y: rows), so that no thread divides an index: the
+// kernel's ALU work (the correctly rounded exponential and division) is what
+// it shares the HBM time with.
 __global__ void __launch_bounds__(256) silu_mul_bf16_kernel(const uint16_t *__restrict__ gate_up,
                                                             int64_t m, int64_t inter,
                                                             uint16_t *__restrict__ out) {
   pdl_trigger();
   pdl_wait();
-  const int64_t per_row = inter >> 3;
-  const int64_t total = m * per_row;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = idx / per_row, c8 = idx - row * per_row;
-    const uint4 g = __ldcs(reinterpret_cast<const uint4 *>(gate_up + row * 2 * inter + c8 * 8));
-    const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(gate_up + row * 2 * inter + inter + c8 * 8));
-    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
-    uint32_t o[4];
+  const int64_t c8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = blockIdx.y;
+  if (c8 >= (inter >> 3) || row >= m) return;
+  const uint4 g = __ldcs(reinterpret_cast<const uint4 *>(gate_up + row * 2 * inter + c8 * 8));
+  const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(gate_up + row * 2 * inter + inter + c8 * 8));
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float h0 = silu_mul(bf16_lo(gw[i]), bf16_lo(uw[i]));
-      const float h1 = silu_mul(bf16_hi(gw[i]), bf16_hi(uw[i]));
-      const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);  // .x = h0 -> low half
-      o[i] = *reinterpret_cast<const uint32_t *>(&b);
-    }
-    *reinterpret_cast<uint4 *>(out + row * inter + c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int i = 0; i < 4; ++i) {
+    const float h0 = silu_mul(bf16_lo(gw[i]), bf16_lo(uw[i]));
+    const float h1 = silu_mul(bf16_hi(gw[i]), bf16_hi(uw[i]));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);  // .x = h0 -> low half
+    o[i] = *reinterpret_cast<const uint32_t *>(&b);
   }
+  *reinterpret_cast<uint4 *>(out + row * inter + c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // NVFP4_AWQ activation pre-scale: out[r, c] = bf16(x[r, c] * s[c]); the fp32
@@ -307,8 +309,15 @@ cudaError_t launch_silu_mul_quantize_masked(const uint16_t *gate_up, const int32
 
 cudaError_t launch_silu_mul_bf16(const uint16_t *gate_up, int64_t m, int64_t i, uint16_t *out,
                                  cudaStream_t st) {
-  return launch_pdl(silu_mul_bf16_kernel, dim3(grid_for(m * (i / 8), 256)), dim3(256), 0, st, gate_up, m, i,
-                    out);
+  if (m > 65535) {      // (the grid's y extent) in slices of rows
+    for (int64_t r0 = 0; r0 < m; r0 += 65535) {
+      const int64_t rows = m - r0 < 65535 ? m - r0 : 65535;
+      if (cudaError_t e = launch_silu_mul_bf16(gate_up + r0 * 2 * i, rows, i, out + r0 * i, st)) return e;
+    }
+    return cudaSuccess;
+  }
+  const dim3 grid((unsigned)((i / 8 + 255) / 256), (unsigned)m);
+  return launch_pdl(silu_mul_bf16_kernel, grid, dim3(256), 0, st, gate_up, m, i, out);
 }
 
 cudaError_t launch_awq_prescale(const uint16_t *x, const uint16_t *s, int64_t m, int64_t k, uint16_t *out,

@@ -101,7 +101,9 @@ def test_silu_mul_quantize(lib, m, inter):
     print(f"silu_mul_quant m={m} i={inter}: {nflip} boundary flips, {nsf} scale differences")
 
 
-@pytest.mark.parametrize("m,inter", [(1, 17408), (16, 17408), (128, 17408), (3, 520)])
+# (5, 2056): a ragged last block of column groups; (65539, 24): rows past the
+# launch grid's y extent, taken in slices
+@pytest.mark.parametrize("m,inter", [(1, 17408), (16, 17408), (128, 17408), (3, 520), (5, 2056), (65539, 24)])
 def test_silu_mul_bf16_within_one_ulp(lib, m, inter):
     bits, gu = _gate_up_input(m, inter, 1)
     out = torch.empty((m, inter), dtype=torch.bfloat16, device="cuda")
