@@ -118,7 +118,9 @@ struct WorkIter {
   }
 };
 
-template <int MODE, int NT>
+// FOLD: the activation quantize folded in (a separate instance, so that the
+// plain kernel carries none of its code)
+template <int MODE, int NT, bool FOLD = false>
 __global__ void __launch_bounds__(kThreads, 1)
     swapab_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                   const SwapArgs p) {
@@ -215,9 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with the fold: x's blocks are quantized by the first CTAs through
         // the wait (after a give-up the halves still go out, reading
         // whatever the buffers hold, so that every stage completes)
-        if (p.xsrc && !ptx::counter_wait_bounded(&p.xsync[1], (uint32_t)p.xchunks, limit, kTimeoutNs, abort_flag)) {
-          *abort_flag = 1;
-          atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+        if constexpr (FOLD) {
+          if (!ptx::counter_wait_bounded(&p.xsync[1], (uint32_t)p.xchunks, limit, kTimeoutNs, abort_flag)) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0, (int)NVFP4_ERR_DEVICE_TIMEOUT);
+          }
         }
         for (int i = 0; i < npend; ++i) issue_x(pend_s[i], pend_kb[i]);
         flushed = true;
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!flushed) flush();
-      if (p.xsrc) {
+      if constexpr (FOLD) {
         // This CTA reads and takes no phase-A counter any more once its own
         // epilogue warps are past phase A; the last CTA to get here resets
         // the counters for the next call.
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;                 // weight row within the tile
     const int et = threadIdx.x - 64;             // 0..127 across the epilogue warps
-    if (p.xsrc) {
+    if constexpr (FOLD) {
       // phase A: chunks of x's blocks (counted), then chunks of the padding
       // rows m..127 of the scale block (zero), until none is left
       const int cols = p.k >> 4, xcp4 = cols >> 2;
@@ -629,9 +633,16 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   // the shared-memory limit is a setting of each device's context
   static PerDeviceOnce smem_attr;
   if (cudaError_t e = smem_attr.run([] {
+        if constexpr (MODE == TC_W4A4_SWIGLU)
+          if (cudaError_t e2 = cudaFuncSetAttribute(swapab_kernel<MODE, NT, true>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES))
+            return e2;
         return cudaFuncSetAttribute(swapab_kernel<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES);
       }))
     return e;
+  auto kernel = swapab_kernel<MODE, NT>;
+  if constexpr (MODE == TC_W4A4_SWIGLU)
+    if (fold) kernel = swapab_kernel<MODE, NT, true>;
   CUtensorMap tm_w, tm_x;
   if (!make_byte_map(&tm_w, w, n, k / 2, 128, 128, 128) || !make_byte_map(&tm_x, x, m, k / 2, 128, NT, 128))
     return cudaErrorInvalidValue;
@@ -676,7 +687,7 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   }
   if (!a.status) return cudaErrorInvalidValue;
   if (pl.cl <= 1)
-    return launch_pdl(swapab_kernel<MODE, NT>, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_w, tm_x, a);
+    return launch_pdl(kernel, dim3(a.grid), dim3(kThreads), C::SMEM_BYTES, st, tm_w, tm_x, a);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -691,7 +702,7 @@ cudaError_t launch_nt(const Plan &pl, const uint8_t *x, const uint8_t *x_sf, con
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, swapab_kernel<MODE, NT>, tm_w, tm_x, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_x, a);
 }
 
 template <int MODE>
