@@ -362,13 +362,16 @@ cudaError_t launch_mt(GemvMode mode, const GemvArgs &a, cudaStream_t st) {
     case GEMV_W4A4_SWIGLU:
       return launch_pdl(gemv_w4a4_kernel<MT, 4, true>, dim3((unsigned)(a.n / 32)), block, 0, st, a);
     case GEMV_W4A16:
-      if constexpr (MT > 4) return cudaErrorInvalidValue;   // W4A16 passes hold at most 4 tokens
-      // two rows a warp (the activation chunk converted once for both) when
-      // that still leaves 16 warps an SM; one row with twice the chunks in
-      // flight otherwise
-      if (a.n >= (int64_t)num_sms() * kWarps * 2 * 2 * 2)
-        return launch_pdl(gemv_w4a16_kernel<MT, 2, 4>, dim3((unsigned)(a.n / (kWarps * 2))), block, 0, st, a);
-      return launch_pdl(gemv_w4a16_kernel<MT, 1, 8>, dim3((unsigned)(a.n / kWarps)), block, 0, st, a);
+      if constexpr (MT > 4) {
+        return cudaErrorInvalidValue;   // W4A16 passes hold at most 4 tokens
+      } else {
+        // two rows a warp (the activation chunk converted once for both) when
+        // that still leaves 16 warps an SM; one row with twice the chunks in
+        // flight otherwise
+        if (a.n >= (int64_t)num_sms() * kWarps * 2 * 2 * 2)
+          return launch_pdl(gemv_w4a16_kernel<MT, 2, 4>, dim3((unsigned)(a.n / (kWarps * 2))), block, 0, st, a);
+        return launch_pdl(gemv_w4a16_kernel<MT, 1, 8>, dim3((unsigned)(a.n / kWarps)), block, 0, st, a);
+      }
   }
   return cudaErrorInvalidValue;
 }
