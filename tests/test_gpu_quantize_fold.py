@@ -170,3 +170,15 @@ def test_fold_argument_errors(lib):
     assert status(a11=1000) == lib.ERR_UNSUPPORTED_SHAPE           # n % 128
     assert status(a12=100) == lib.ERR_UNSUPPORTED_SHAPE            # k % 64
     assert lib.nvfp4_quantize_gemm_swiglu_quant_workspace_bytes(0, n, k) == 0
+
+
+def test_fold_m_zero_is_a_noop(lib):
+    m, n, k = 0, 1024, 256
+    ws = small_weights(n, k, 6)
+    wi = ws.device_interleaved(lib)
+    buf = torch.full((1 << 16,), 0x5A, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((1, k), dtype=torch.bfloat16, device="cuda")
+    one = scalar(1.0)
+    lib.nvfp4_quantize_gemm_swiglu_quant(x, one, buf, buf, wi[0], wi[1], one, one, buf, buf, m, n, k, None, 0)
+    torch.cuda.synchronize()
+    assert bool((buf == 0x5A).all()), "an M = 0 call wrote to its outputs"
