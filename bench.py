@@ -719,6 +719,23 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     in_stream, out_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     order = sorted(items, key=lambda it: -(it.x.numel() + it.out.numel()))
+
+    def copy_gbs(dst, src, stream_):
+        """This machine's host-link rate for one copy of the step's size (the
+        end-to-end number is bound by it where it is slow)."""
+        with torch.cuda.stream(stream_):
+            dst.copy_(src, non_blocking=True)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream_)
+            for _ in range(3):
+                dst.copy_(src, non_blocking=True)
+            e1.record(stream_)
+        stream_.synchronize()
+        return src.numel() * src.element_size() * 3 / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+    big = order[0]
+    link = {"h2d_gbs": copy_gbs(big.x, x_host[big.key], in_stream),
+            "d2h_gbs": copy_gbs(out_host[big.key], big.out, out_stream)}
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
@@ -783,7 +800,7 @@ def run_ours(args, world, rank, local):
             "roofline": roofline, "per_workload": per, "elementwise": elementwise,
             "cpu_baseline": cpu, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
+                    "d2h_bytes_per_step": d2h, "host_link": link,
                     "note": "host wall clock per step; pinned host buffers; x of every workload in and every "
                             "output out, each step, on two copy streams of their own; the steps alternate "
                             "between two device input/output sets so that one step's copies overlap its "
