@@ -666,8 +666,8 @@ def run_ours(args, world, rank, local):
     # launch): reported as the roofline's traffic when that launch is the
     # dominant one; to be removed whenever the kernel changes before it is
     # captured again
-    measured_traffic = {("prefill_h7168", 8192, "gate_up"): 301.4e6,
-                        ("prefill_h7168", 8192, "down"): 563.6e6}
+    measured_traffic = {("prefill_h7168", 8192, "gate_up"): 287.8e6,
+                        ("prefill_h7168", 8192, "down"): 523.2e6}
     roofline = None
     if dom is not None:
         t_us, it, m, which = dom

@@ -89,10 +89,16 @@ constexpr uint64_t kSettleNs = 50000ull;                // then 50 us for copies
 // while k-block g's operands are still in flight -- so the scale path is off
 // the refill loop (commit -> operand TMA -> MMA) that bounds the pipeline.
 // The writers learn of that commit from the empty barrier of the operand
-// stage that held k-block g - T_SLOTS, waited on by phase parity; this needs
-// T_SLOTS <= STAGES: the barrier's next phase belongs to k-block
-// g - T_SLOTS + STAGES, whose MMAs cannot run before writer g is done, so
-// the awaited phase is never overtaken.
+// stage that held k-block g - T_SLOTS, waited on by phase parity; the
+// barrier's next phase belongs to k-block g - T_SLOTS + STAGES, whose MMAs
+// cannot run before writer g is done, so the awaited phase is never
+// overtaken.  With T_SLOTS == STAGES the TMEM slot of k-block g is its
+// operand stage, and the writers arrive on that stage's full barrier next
+// to the operand bytes: the MMA issuer waits on one barrier per k-block
+// (each wait costs the single issuing thread a hundred-odd cycles even when
+// the phase has already completed).  Both the producer's and the writers'
+// arrivals for k-block g follow the commit of k-block g - STAGES, so no
+// arrival lands in a neighbouring phase.
 template <bool PAIR>
 struct Cfg {
   static constexpr uint32_t B_BYTES = PAIR ? B_HALF : 2 * B_HALF;
@@ -105,7 +111,7 @@ struct Cfg {
   static constexpr uint32_t SMEM_BYTES = STAGES * OPND_BYTES + SF_SLOTS * SF_BYTES + 1024 /*align*/ + 512 /*barriers*/;
   static constexpr int CLUSTER = PAIR ? 2 : 1;
   static_assert(SF_COL + T_SLOTS * SF_SLOT <= TMEM_COLS, "TMEM columns");
-  static_assert(T_SLOTS <= STAGES, "a writer's awaited commit phase must not be overtaken");
+  static_assert(T_SLOTS == STAGES, "a k-block's scale slot is its operand stage (one full barrier for both)");
   static_assert(OPND_BYTES % 1024 == 0, "operand slots keep the 1024-byte swizzle alignment");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -151,8 +157,7 @@ struct Smem {
   __device__ uint64_t *tfull() const { return sempty() + C::SF_SLOTS; }
   __device__ uint64_t *tempty() const { return tfull() + 1; }
   __device__ uint64_t *drain() const { return tempty() + 1; }
-  __device__ uint64_t *sf_full() const { return drain() + 1; }
-  __device__ uint32_t *tslot() const { return reinterpret_cast<uint32_t *>(sf_full() + C::T_SLOTS); }
+  __device__ uint32_t *tslot() const { return reinterpret_cast<uint32_t *>(drain() + 1); }
   __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(tslot() + 1); }
 };
 
@@ -187,11 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&sm.full()[s], 1);
+      // the operand producer's arrival (with the tile bytes) and one per
+      // scale-writer warp of the pair
+      ptx::mbar_init(&sm.full()[s], 1 + 4 * CL);
       ptx::mbar_init(&sm.empty()[s], 1);
     }
-    for (int t = 0; t < C::T_SLOTS; ++t)
-      ptx::mbar_init(&sm.sf_full()[t], 4 * CL);   // one arrival per scale-writer warp of the pair
     for (int s = 0; s < C::SF_SLOTS; ++s) {
       ptx::mbar_init(&sm.sfull()[s], 1);
       ptx::mbar_init(&sm.sempty()[s], 4);         // one arrival per scale-writer warp of this CTA
@@ -318,20 +323,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
-          const int s = g % STAGES, t = g % C::T_SLOTS;
-          const uint32_t ph = (uint32_t)(g / STAGES) & 1u, tph = (uint32_t)(g / C::T_SLOTS) & 1u;
-          // the stage's operand tiles (both CTAs' halves in a pair), then the
-          // k-block's TMEM scale slot (usually written while the operands
-          // were in flight)
-          if (!ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag) ||
-              !ptx::mbar_wait_bounded(&sm.sf_full()[t], tph, limit, kDefaultTimeoutNs, abort_flag)) {
+          const int s = g % STAGES;
+          const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
+          // the stage's operand tiles (both CTAs' halves in a pair) and its
+          // TMEM scale slot (usually written while the operands were in
+          // flight)
+          if (!ptx::mbar_wait_bounded(&sm.full()[s], ph, limit, kDefaultTimeoutNs, abort_flag)) {
             give_up();
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           const int nk = min(KSTEPS, ksteps_total - kb * KSTEPS);
-          const uint32_t sf = tmem + SF_COL + t * C::SF_SLOT;
+          const uint32_t sf = tmem + SF_COL + s * C::SF_SLOT;
           const uint32_t a_s = ptx::smem_u32(sm.a(s)), b_s = ptx::smem_u32(sm.b(s));
           for (int j = 0; j < nk; ++j) {
             const uint64_t ad = ptx::smem_desc(a_s + 32 * j, 16, 1024, 2);
@@ -452,8 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           ptx::mbar_arrive(&sm.sempty()[ss]);       // the smem scale slot may be refilled
-          if constexpr (PAIR) ptx::mbar_arrive_remote(in_cta(&sm.sf_full()[t], 0));
-          else ptx::mbar_arrive(&sm.sf_full()[t]);
+          // the k-block's scale slot is ready: one arrival on its stage's
+          // full barrier (the leader's in a pair)
+          if constexpr (PAIR) ptx::mbar_arrive_remote(in_cta(&sm.full()[t], 0));
+          else ptx::mbar_arrive(&sm.full()[t]);
         }
       }
       if (!ok) break;
@@ -546,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Drain: wait (bounded) for this CTA's copies still in flight and for
     // every MMA it issued, so nothing lands in shared memory or TMEM after
     // the CTA is gone.  In a pair some of a CTA's copies complete on the
-    // other CTA's barrier: a short settle time covers those.
+    // other CTA's barrier: a short settle time covers those.  An operand
+    // stage whose scale writers gave up before arriving never completes its
+    // phase; its wait runs out its bound, far longer than any copy's flight.
     if ((warp == 0 || warp == 14) && issued_mask) {
       uint64_t *bars = warp == 0 ? sm.full() : sm.sfull();
       for (int s = 0; s < (warp == 0 ? STAGES : C::SF_SLOTS); ++s)
