@@ -348,6 +348,36 @@ def test_tc_bounded_wait_gives_up_cleanly(lib, algo):
     assert_gemm_close(got, oracle.gemm_w4a4(xq, xs, ws.packed, ws.sf, alpha))
 
 
+@pytest.mark.parametrize("algo", [TC, TC_1SM])
+def test_tc_swiglu_bounded_wait_gives_up_cleanly(lib, algo):
+    """The fused gate_up instance with a wait limit of one poll: the scale
+    writers and the MMA thread give up at their first waits, so the operand
+    stages' full barriers (which count the writers' arrivals) never complete
+    and the drain's own bounded waits run out; the kernel records
+    NVFP4_ERR_DEVICE_TIMEOUT and returns, and the next normal call on the
+    same weights passes the requantize rule."""
+    m, n, k = 256, 1024, 1024
+    inter = n // 2
+    ws = small_weights(n, k, 6)
+    _, _, gs_x, xq, xs = quantized_activation(0, m, k)
+    alpha = np.float32(1.0) / (gs_x * ws.gs)
+    wdev = ws.device_interleaved(lib)
+    q = torch.zeros((m, inter // 2), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((lib.nvfp4_sf_bytes(m, inter),), dtype=torch.uint8, device="cuda")
+    w, nbytes = workspace(lib, m, n, k, algo)
+    assert lib.nvfp4_get_device_status() == 0
+    lib.nvfp4_set_wait_limit(1)
+    try:
+        lib.nvfp4_gemm_swiglu_quant_ex(dev(xq), dev(oracle.sf_swizzle_128x4(xs)), wdev[0], wdev[1], scalar(alpha),
+                                       scalar(1.0), q, s, m, n, k, w, nbytes, algo=algo)
+        torch.cuda.synchronize()
+    finally:
+        lib.nvfp4_set_wait_limit(0)
+    assert lib.nvfp4_get_device_status() == lib.ERR_DEVICE_TIMEOUT
+    assert lib.nvfp4_get_device_status() == 0          # read clears it
+    _swiglu_case(lib, 0, m, n, k, ws, algo)
+
+
 def test_auto_dispatch_matches_forced_paths(lib):
     """AUTO picks GEMV for decode-sized M and the tensor cores above; both
     give the same result within tolerance at the crossover."""
