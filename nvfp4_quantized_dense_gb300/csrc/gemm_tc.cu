@@ -9,8 +9,9 @@
 //     CTAs' halves, so each SM stages 32 KB of operands per 256-wide k-block
 //     instead of 48 KB, and five stages fit where one CTA per tile fits four.
 //     The pair's even CTA (the leader) issues the MMAs and owns the
-//     pipeline's full / scale barriers; both CTAs' loads complete on the
-//     leader's barrier, and the leader's commits free both CTAs' stages.
+//     pipeline's full barriers; both CTAs' loads and both CTAs' scale
+//     writers complete on the leader's barrier, and the leader's commits
+//     free both CTAs' stages.
 //   1-SM: one CTA per 128 x 256 tile loads the whole weight tile itself.
 // Roles per CTA (480 threads):
 //   warp 0      TMA producer of the operand tiles (2-D tensor maps, 128-byte
